@@ -1,0 +1,167 @@
+/*
+ * bonsai.h -- C ABI of libbonsai: matrix products of FP16 activations with
+ * sub-bit weights (binary {-1,+1} or ternary {-1,0,+1}) that share one FP16
+ * scale per group of 128 weights along K.
+ *
+ *   y[m][n] = sum_k x[m][k] * s[n][k/128] * w[n][k]              (FP32 accumulate)
+ *
+ * Sources (the "Bonsai" pages):
+ *   - "1-bit diffusion ... WebGPU" (richmindsetzone), section "1-bit 嘅數學":
+ *     each weight is binary and every group of weights shares one FP16 scale;
+ *     1.125 effective bits per binary weight, about 1.71 for ternary
+ *     {-1,0,+1}; a binary GEMM can be done with XOR + popcount.
+ *   - "OpenBonsai" (ainewscove), section "工作原理": one FP16 group scale per
+ *     128 weights, ternary codes {-1,0,+1}.
+ *   - "三值权重压缩" (kongchang), section "三值权重到底做了什么" and its
+ *     background paragraph: ternary multiplication reduces to addition and a
+ *     sign flip.
+ *   - "Bonsai 27B on phone" (xiaohu.ai), sections "第一の壁" and "速度は二層":
+ *     token-by-token decode re-streams every weight per token and is bound by
+ *     memory bandwidth at small batch.
+ * The pages fix no byte layout; the layout below is this library's own and is
+ * stated exactly so that any other implementation can produce it.
+ *
+ * ------------------------------------------------------------------------
+ * Data layout (all matrices row-major, PyTorch Linear convention W[n][k]):
+ *   x       FP16 bits, [m][k], row stride k elements.
+ *   scales  FP16 bits, [n][k/128], row stride k/128 elements; scale of
+ *           weight (n,k) is scales[n][k/128] (groups are contiguous runs of
+ *           128 along K). Effective weight = scale * code (a product).
+ *   y       FP16 bits, [m][n], row stride n elements; FP32 result rounded to
+ *           nearest-even.
+ *   BINARY  packed row n occupies row_bytes bytes at packed + n*row_bytes;
+ *           bit i (LSB first) of little-endian 32-bit word j holds code
+ *           k = 32*j + i; bit 1 means +1, bit 0 means -1. Bytes from k/8 to
+ *           row_bytes are padding (pack writes 0).
+ *   TERNARY byte b of row n holds the five codes k = 5b .. 5b+4 as the
+ *           base-3 number  sum_{i<5} (code(5b+i) + 1) * 3^i  (least
+ *           significant digit first, digit = code + 1 in {0,1,2}); codes past
+ *           k are 0 (digit 1). Valid bytes are 0..242; all -1 -> 0, all 0 ->
+ *           121, all +1 -> 242. Bytes from ceil(k/5) to row_bytes are padding
+ *           holding 121 (five zero codes). A byte may hold codes of two
+ *           adjacent 128-groups; the scale is applied per code.
+ *
+ * Size requirements checked on the host before any launch:
+ *   k % 128 == 0, k > 0, n > 0, m > 0.
+ *   BINARY : row_bytes >= k/8 and row_bytes % 16 == 0.
+ *   TERNARY: row_bytes >= 64*ceil(ceil(k/5)/64) and row_bytes % 64 == 0.
+ *   All device pointers 16-byte aligned.
+ *
+ * Conventions:
+ *   - Every pointer passed to a compute call is a DEVICE pointer owned by the
+ *     caller. The library allocates no device memory and keeps no pointer
+ *     after the call returns. Its only device state is one 32-bit status word
+ *     per device, a file-scope __device__ variable, written by kernels that
+ *     detect bad input codes or a bounded wait that ran out.
+ *   - Calls enqueue work on `stream` and return without synchronising (they
+ *     can be captured in a CUDA graph). A non-OK return means nothing was
+ *     launched. Kernel-side problems are reported by bonsai_check_async.
+ *   - Calls launched with programmatic dependent launch: a kernel may start
+ *     reading its weights before the previous kernel on the stream finishes,
+ *     but reads x (and writes y) only after it has finished.
+ *   - No C++ exceptions cross this interface.
+ * ------------------------------------------------------------------------
+ */
+#ifndef BONSAI_H
+#define BONSAI_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle; identical to cudaStream_t. NULL = legacy stream. */
+typedef struct CUstream_st* bonsai_stream;
+
+typedef enum {
+  BONSAI_OK = 0,
+  BONSAI_ERR_INVALID_ARG = 1,  /* null pointer, unknown enum, negative size   */
+  BONSAI_ERR_SHAPE = 2,        /* k % 128 != 0, row_bytes too small, ...       */
+  BONSAI_ERR_ALIGN = 3,        /* a pointer or row stride is not 16-B aligned  */
+  BONSAI_ERR_FORMAT = 4,       /* wrong weight format for this call            */
+  BONSAI_ERR_CUDA = 5,         /* a CUDA runtime call failed                   */
+  BONSAI_ERR_UNSUPPORTED = 6,  /* valid request this build does not handle     */
+  BONSAI_ERR_TIMEOUT = 7,      /* a bounded device-side wait ran out           */
+  BONSAI_ERR_BAD_CODE = 8      /* pack saw a code outside the format's set     */
+} bonsai_status;
+
+enum { BONSAI_FMT_BINARY = 1, BONSAI_FMT_TERNARY = 2 };
+
+/* A packed weight matrix W[n][k] with its FP16 group scales. */
+typedef struct {
+  int32_t format;          /* BONSAI_FMT_BINARY or BONSAI_FMT_TERNARY        */
+  int32_t reserved;        /* must be 0                                      */
+  int64_t n;               /* output features (rows of W)                    */
+  int64_t k;               /* input features, multiple of 128                */
+  int64_t row_bytes;       /* bytes per packed row (see layout above)        */
+  const void* packed;      /* device, n * row_bytes bytes                    */
+  const uint16_t* scales;  /* device, FP16 bits [n][k/128]                   */
+} bonsai_weights;
+
+/* Canonical packed row size: BINARY k/8; TERNARY 64*ceil(ceil(k/5)/64).
+ * Returns -1 for an unknown format or k <= 0 or k % 128 != 0. Host only. */
+int64_t bonsai_packed_row_bytes(int32_t format, int64_t k);
+
+/* Pack int8 codes [rows][k] (row stride k) into the BINARY layout.
+ * codes: device, values must be -1 or +1; out: device, rows*row_bytes bytes.
+ * A code outside {-1,+1} sets BONSAI_ERR_BAD_CODE in the device status word
+ * (the affected output word is unspecified); bonsai_check_async reports it.
+ * Follows the binary-weight-with-group-scale format ("1-bit 嘅數學"). */
+bonsai_status bonsai_pack_binary(const int8_t* codes, int64_t rows, int64_t k,
+                                 void* out, int64_t row_bytes,
+                                 bonsai_stream stream);
+
+/* Pack int8 codes [rows][k] into the TERNARY layout (5 codes per byte,
+ * base 3) including the 121-valued padding. Codes outside {-1,0,+1} set
+ * BONSAI_ERR_BAD_CODE. Follows the ternary value set of the OpenBonsai page
+ * ("工作原理") and "三值权重到底做了什么". */
+bonsai_status bonsai_pack_ternary(const int8_t* codes, int64_t rows, int64_t k,
+                                  void* out, int64_t row_bytes,
+                                  bonsai_stream stream);
+
+/* Batch-1 decode product y[n] = sum_k x[k] * s[n][k/128] * w[n][k].
+ * w: binary or ternary weights; x: device FP16 [k]; y: device FP16 [n].
+ * Packed bytes must be valid codes (ternary bytes <= 242, padding 121):
+ * kernels do not re-check them. Decode is memory-bandwidth bound
+ * ("第一の壁"): the kernel streams each packed byte once. */
+bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x,
+                          uint16_t* y, bonsai_stream stream);
+
+/* Multi-token product Y[m][n] = sum_k X[m][k] * s[n][k/128] * w[n][k],
+ * X FP16 [m][k], Y FP16 [m][n]. m <= 8 runs the streaming decode kernel with
+ * m columns (speculative verification, prefill of a few tokens); larger m
+ * runs the tensor-core GEMM that expands weight tiles to FP16 in on-chip
+ * memory (prompt processing and diffusion-transformer image tokens). */
+bonsai_status bonsai_gemm(const bonsai_weights* w, const uint16_t* x,
+                          int64_t m, uint16_t* y, bonsai_stream stream);
+
+/* XNOR-popcount product of +-1 activations with +-1 weights ("1-bit 嘅數學":
+ * binary GEMM via XOR + popcount).
+ *   a_bits  device uint32 [m][k/32], same bit layout as BINARY weights
+ *           (bit 1 = +1); row stride k/32 words.
+ *   a_scale device FP16 [m], one scale per activation row.
+ *   w       BINARY weights [n][k] with group scales.
+ *   d_out   device int32 [m][n] or NULL: D = sum_k a*w = k - 2*popc(a XOR w),
+ *           exact.
+ *   y_out   device FP16 [m][n] or NULL:
+ *           Y = a_scale[m] * sum_g s[n][g] * (128 - 2*popc over group g).
+ * At least one of d_out / y_out must be non-NULL. */
+bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale,
+                               int64_t m, const bonsai_weights* w,
+                               int32_t* d_out, uint16_t* y_out,
+                               bonsai_stream stream);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device: BONSAI_OK, BONSAI_ERR_BAD_CODE or BONSAI_ERR_TIMEOUT.
+ * Returns BONSAI_ERR_CUDA if the stream reported a CUDA error. */
+bonsai_status bonsai_check_async(bonsai_stream stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+const char* bonsai_status_string(bonsai_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BONSAI_H */

@@ -1,0 +1,378 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each pin_* function checks the oracle against something the oracle does not
+compute the same way: the numbers the Bonsai pages print (tests/golden), a
+closed form, an invariant, brute force through a second decoding route
+(numpy unpackbits / integer division, then a dense float64 matmul), or
+Python's own popcount. test_mutants_are_caught compiles deliberately broken
+copies of oracle.c and checks that some pin rejects every one of them.
+"""
+import ctypes
+import math
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from sub_bit_weight_binary_b300 import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLDEN = os.path.join(HERE, "golden", "pages_sizes.txt")
+
+BIN, TER = oracle.FMT_BINARY, oracle.FMT_TERNARY
+
+
+def golden():
+    vals = {}
+    with open(GOLDEN, encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            vals[parts[0]] = float(parts[1])
+    return vals
+
+
+# ---- independent decoding routes (numpy), used only by the pins ----------
+
+def np_decode_binary(packed_bytes, k):
+    bits = np.unpackbits(np.ascontiguousarray(packed_bytes, dtype=np.uint8),
+                         axis=1, bitorder="little")[:, :k]
+    return bits.astype(np.int8) * 2 - 1
+
+
+def np_decode_ternary(packed_bytes, k):
+    b = np.ascontiguousarray(packed_bytes, dtype=np.int64)
+    nbytes = (k + 4) // 5
+    digits = np.stack([(b[:, :nbytes] // 3 ** i) % 3 for i in range(5)], axis=2)
+    return (digits.reshape(b.shape[0], -1)[:, :k] - 1).astype(np.int8)
+
+
+def f16(bits):
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def dense(fmt, packed, scales, k):
+    codes = np_decode_binary(packed, k) if fmt == BIN else np_decode_ternary(packed, k)
+    s = np.repeat(f16(scales), 128, axis=1)
+    return codes.astype(np.float64) * s
+
+
+def rand_x(seed, m, k):
+    return synth.gen_x(seed, m, k)
+
+
+# ---- pins ----------------------------------------------------------------
+
+def pin_half_to_double():
+    h = np.arange(65536, dtype=np.uint16)
+    ref = h.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(v)) for v in h[::7]])
+    r = ref[::7]
+    assert np.array_equal(np.isnan(got), np.isnan(r))
+    ok = ~np.isnan(r)
+    assert np.array_equal(got[ok], r[ok])
+    for v in (0x0001, 0x03FF, 0x0400, 0x3C00, 0x7BFF, 0x7C00, 0x8001, 0xFBFF):
+        a, b = oracle.half_to_double(v), float(np.uint16(v).view(np.float16))
+        assert a == b or (math.isnan(a) and math.isnan(b))
+
+
+def pin_row_bytes():
+    for k in (128, 256, 1024, 5120, 17408):
+        assert oracle.row_bytes(BIN, k) == k // 8
+    assert oracle.row_bytes(TER, 128) == 64      # 26 data bytes
+    assert oracle.row_bytes(TER, 640) == 128     # exactly 128 data bytes
+    assert oracle.row_bytes(TER, 5120) == 1024
+    assert oracle.row_bytes(TER, 17408) == 3520  # 3482 data bytes
+    for bad in (0, -128, 100, 129):
+        assert oracle.row_bytes(BIN, bad) == -1
+        assert oracle.row_bytes(TER, bad) == -1
+    assert oracle.row_bytes(3, 128) == -1
+
+
+def pin_page_sizes():
+    g = golden()
+    assert g["group_size"] == oracle.GROUP == 128
+    for k in (128, 1024, 5120, 17408):
+        bpw = (oracle.row_bytes(BIN, k) * 8 + 16 * k / 128) / k
+        assert bpw == g["binary_bpw"]
+    assert round(math.log2(3), 2) == g["ternary_info_bpw"]
+    assert round(math.log2(3) + 16 / 128, 2) == g["ternary_bpw"]
+    # the stored layout (5 codes per byte) is within 1% of the pages' figure
+    k = 5120
+    stored = (oracle.row_bytes(TER, k) * 8 + 16 * k / 128) / k
+    assert abs(stored - g["ternary_bpw"]) / g["ternary_bpw"] < 0.01
+    params = 27e9
+    assert params * 2 / 1e9 == g["fp16_27b_gb"]
+    ter_gb = params * g["ternary_bpw"] / 8 / 1e9
+    assert ter_gb < g["ternary_27b_max_gb"]
+    assert round(g["fp16_27b_gb"] / ter_gb) == g["ternary_27b_ratio"]
+    assert round(params * g["binary_bpw"] / 8 / 1e9) == g["binary_27b_gb"]
+
+
+def pin_binary_round_trip():
+    for k, rows in ((128, 3), (640, 1), (5120, 3), (17408, 1)):
+        codes = synth.gen_binary_codes(11, rows, k)
+        packed = oracle.pack_binary(codes)
+        ref = np.packbits(((codes + 1) // 2).astype(np.uint8), axis=1, bitorder="little")
+        assert np.array_equal(packed, ref)
+        assert np.array_equal(oracle.unpack_binary(packed, k), codes)
+        assert np.array_equal(np_decode_binary(packed, k), codes)
+
+
+def pin_binary_single_hot():
+    k = 256
+    for pos in (0, 1, 7, 8, 31, 32, 100, 255):
+        codes = -np.ones((1, k), dtype=np.int8)
+        codes[0, pos] = 1
+        words = oracle.pack_binary(codes).view("<u4")[0]
+        expect = np.zeros(k // 32, dtype=np.uint32)
+        expect[pos // 32] = np.uint32(1) << np.uint32(pos % 32)
+        assert np.array_equal(words, expect), pos
+    words = oracle.pack_binary(np.ones((1, k), dtype=np.int8)).view("<u4")[0]
+    assert np.all(words == 0xFFFFFFFF)
+    padded = oracle.pack_binary(np.ones((2, k), dtype=np.int8), k // 8 + 16)
+    assert np.all(padded[:, k // 8:] == 0)
+
+
+def pin_ternary_byte_values():
+    k = 640
+    for c, byte in ((-1, 0), (0, 121), (1, 242)):
+        p = oracle.pack_ternary(np.full((1, k), c, dtype=np.int8))
+        assert np.all(p == byte)
+    for i in range(5):
+        for b in (0, 7, 127):
+            for sign in (1, -1):
+                codes = np.zeros((1, k), dtype=np.int8)
+                codes[0, 5 * b + i] = sign
+                p = oracle.pack_ternary(codes)[0]
+                assert p[b] == 121 + sign * 3 ** i
+                assert np.all(np.delete(p, b) == 121)
+
+
+def pin_ternary_all_bytes():
+    k = 1280  # 256 data bytes
+    vals = np.arange(256) % 243
+    digits = np.stack([(vals // 3 ** i) % 3 for i in range(5)], axis=1)
+    codes = (digits.reshape(1, -1) - 1).astype(np.int8)
+    packed = oracle.pack_ternary(codes)
+    assert np.array_equal(packed[0, :256], vals.astype(np.uint8))
+    assert np.array_equal(oracle.unpack_ternary(packed, k), codes)
+    for bad in (243, 250, 255):
+        p = packed.copy()
+        p[0, 3] = bad
+        with pytest.raises(oracle.OracleError) as e:
+            oracle.unpack_ternary(p, k)
+        assert e.value.status == oracle.ERR_BAD_CODE
+
+
+def pin_ternary_round_trip_and_padding():
+    for k, rows in ((128, 3), (640, 2), (5120, 1), (17408, 1)):
+        codes = synth.gen_ternary_codes(5, rows, k)
+        packed = oracle.pack_ternary(codes)
+        assert packed.shape == (rows, oracle.row_bytes(TER, k))
+        assert np.array_equal(oracle.unpack_ternary(packed, k), codes)
+        assert np.array_equal(np_decode_ternary(packed, k), codes)
+        nbytes = (k + 4) // 5
+        assert np.all(packed[:, nbytes:] == 121)
+        if k % 5:
+            last = packed[:, nbytes - 1].astype(np.int64)
+            for i in range(k - 5 * (nbytes - 1), 5):
+                assert np.all((last // 3 ** i) % 3 == 1)  # padded codes are 0
+
+
+def pin_bad_codes():
+    c = np.ones((1, 128), dtype=np.int8)
+    for bad in (0, 2, -2):
+        c2 = c.copy()
+        c2[0, 17] = bad
+        with pytest.raises(oracle.OracleError) as e:
+            oracle.pack_binary(c2)
+        assert e.value.status == oracle.ERR_BAD_CODE
+    for bad in (2, -2, 5):
+        c2 = np.zeros((1, 128), dtype=np.int8)
+        c2[0, 17] = bad
+        with pytest.raises(oracle.OracleError) as e:
+            oracle.pack_ternary(c2)
+        assert e.value.status == oracle.ERR_BAD_CODE
+
+
+def pin_all_plus_constant_scale():
+    k, n = 1024, 3
+    x = rand_x(1, 2, k)
+    packed = np.full((n, k // 8), 0xFF, dtype=np.uint8)
+    s = np.full((n, k // 128), np.float16(0.0371).view(np.uint16), dtype=np.uint16)
+    y, nrm = oracle.linear(BIN, packed, s, x)
+    expect = float(np.float16(0.0371)) * f16(x).sum(axis=1)
+    assert np.allclose(y, expect[:, None], rtol=0, atol=1e-12 * nrm.max())
+    assert np.allclose(nrm, float(np.float16(0.0371)) * np.abs(f16(x)).sum(axis=1)[:, None])
+
+
+def pin_group_scales():
+    k, n = 640, 2
+    x = rand_x(2, 1, k)
+    packed = np.full((n, k // 8), 0xFF, dtype=np.uint8)
+    s = synth.gen_scales(3, n, k)
+    y, nrm = oracle.linear(BIN, packed, s, x)
+    xs = f16(x)[0].reshape(-1, 128).sum(axis=1)
+    expect = (f16(s) * xs[None, :]).sum(axis=1)
+    assert np.allclose(y[0], expect, rtol=0, atol=1e-12 * nrm.max())
+
+
+def pin_zero_ternary():
+    k, n = 640, 4
+    x = rand_x(3, 2, k)
+    packed = oracle.pack_ternary(np.zeros((n, k), dtype=np.int8))
+    s = synth.gen_scales(4, n, k)
+    y, nrm = oracle.linear(TER, packed, s, x)
+    assert np.all(y == 0.0) and np.all(nrm == 0.0)
+
+
+def pin_flip_and_scale():
+    k, n = 512, 5
+    x = rand_x(4, 3, k)
+    w = synth.gen_binary_words(5, n, k)
+    s = synth.gen_scales(6, n, k)
+    y, _ = oracle.linear(BIN, w, s, x)
+    y_flip, _ = oracle.linear(BIN, ~w, s, x)
+    assert np.array_equal(y_flip, -y)
+    for j in (1, 3):
+        x2 = (f16(x) * 2.0 ** j).astype(np.float16).view(np.uint16)
+        assert np.array_equal(f16(x2), f16(x) * 2.0 ** j)
+        y2, _ = oracle.linear(BIN, w, s, x2)
+        assert np.array_equal(y2, y * 2.0 ** j)
+
+
+def pin_single_weight():
+    k, n = 640, 3
+    x = rand_x(5, 2, k)
+    s = synth.gen_scales(7, n, k)
+    for (n0, k0, sign) in ((1, 0, 1), (2, 129, -1), (0, 639, 1), (1, 384, -1)):
+        codes = np.zeros((n, k), dtype=np.int8)
+        codes[n0, k0] = sign
+        y, _ = oracle.linear(TER, oracle.pack_ternary(codes), s, x)
+        expect = np.zeros((2, n))
+        expect[:, n0] = sign * f16(s)[n0, k0 // 128] * f16(x)[:, k0]
+        assert np.array_equal(y, expect)
+
+
+def pin_brute_force():
+    for fmt in (BIN, TER):
+        for (m, n, k) in ((1, 1, 128), (3, 4, 128), (2, 3, 256), (1, 2, 640)):
+            x = rand_x(10 + m, m, k)
+            s = synth.gen_scales(20 + n, n, k)
+            if fmt == BIN:
+                packed = synth.gen_binary_words(30 + k, n, k).view(np.uint8).reshape(n, -1)
+            else:
+                packed = oracle.pack_ternary(synth.gen_ternary_codes(40 + k, n, k))
+            wd = dense(fmt, packed, s, k)
+            ref = f16(x) @ wd.T
+            nref = np.abs(f16(x)) @ np.abs(wd).T
+            y, nrm = oracle.linear(fmt, packed, s, x)
+            assert y.shape == (m, n)
+            assert np.allclose(nrm, nref, rtol=1e-12, atol=0)
+            assert np.all(np.abs(y - ref) <= 1e-12 * nref + 1e-300)
+            # a sub-selection of rows and columns picks the same entries
+            y2, _ = oracle.linear(fmt, packed, s, x, n_sel=[n - 1], m_sel=[m - 1])
+            assert y2[0, 0] == y[m - 1, n - 1]
+
+
+def pin_xnor():
+    m, n, k = 3, 5, 512
+    a_bits, a_s, w_bits, s = synth.gen_xnor_inputs(9, m, n, k)
+    d, y, nrm = oracle.xnor(a_bits, a_s, w_bits, s, k)
+    for i in range(m):
+        for j in range(n):
+            pc = [int(np.uint32(a_bits[i, t] ^ w_bits[j, t])).bit_count() for t in range(k // 32)]
+            assert d[i, j] == k - 2 * sum(pc)
+            dg = [128 - 2 * sum(pc[4 * g:4 * g + 4]) for g in range(k // 128)]
+            ref = f16(a_s)[i] * sum(f16(s)[j, g] * dg[g] for g in range(k // 128))
+            assert abs(y[i, j] - ref) <= 1e-12 * nrm[i, j]
+            assert nrm[i, j] == abs(f16(a_s)[i]) * 128 * np.abs(f16(s)[j]).sum()
+    # a = w gives D = K; a = NOT w gives D = -K
+    d2, y2, _ = oracle.xnor(w_bits[:2], a_s[:2], w_bits, s, k)
+    assert d2[0, 0] == k and d2[1, 1] == k
+    assert abs(y2[0, 0] - f16(a_s)[0] * 128 * f16(s)[0].sum()) <= 1e-12
+    d3, _, _ = oracle.xnor(~w_bits[:2], a_s[:2], w_bits, s, k)
+    assert d3[0, 0] == -k and d3[1, 1] == -k
+
+
+def pin_compare_rule():
+    ref = np.array([1.0, 1.0, 0.0, 1.0, 1.0])
+    nrm = np.array([10.0, 10.0, 0.0, 10.0, 10.0])
+    good = np.array([1.0, 1.015, -0.0, 0.99, 1.0], dtype=np.float16).view(np.uint16)
+    bad, first, worst = oracle.compare_f16(good, ref, nrm)
+    assert bad == 0 and first == -1 and worst <= 2e-3
+    y = good.copy()
+    y[1] = np.float16(1.03).view(np.uint16)      # 3e-3 of norm
+    y[2] = np.float16(1e-7).view(np.uint16)      # zero-norm entry must be 0
+    y[4] = np.float16(np.nan).view(np.uint16)
+    bad, first, _ = oracle.compare_f16(y, ref, nrm)
+    assert bad == 3 and first == 1
+
+
+PINS = [pin_half_to_double, pin_row_bytes, pin_page_sizes, pin_binary_round_trip,
+        pin_binary_single_hot, pin_ternary_byte_values, pin_ternary_all_bytes,
+        pin_ternary_round_trip_and_padding, pin_bad_codes,
+        pin_all_plus_constant_scale, pin_group_scales, pin_zero_ternary,
+        pin_flip_and_scale, pin_single_weight, pin_brute_force, pin_xnor,
+        pin_compare_rule]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin, oracle_lib):
+    pin()
+
+
+# Each mutant is a plausible slip in oracle.c; some pin must reject it.
+MUTANTS = {
+    "bit_polarity": ("if (c == 1)\n          word", "if (c == -1)\n          word"),
+    "bit_order": ("word |= (uint32_t)1 << i;", "word |= (uint32_t)1 << (31 - i);"),
+    "unpack_polarity": ("((word >> i) & 1u) ? 1 : -1", "((word >> i) & 1u) ? -1 : 1"),
+    "trit_digit_order": ("int64_t kk = 5 * b + i;\n        int c = 0;",
+                         "int64_t kk = 5 * b + (4 - i);\n        int c = 0;"),
+    "trit_offset": ("value = 3 * value + (c + 1);", "value = 3 * value + (1 - c);"),
+    "unpack_trit_order": ("if (kk < k) codes[r * k + kk] = (int8_t)(digit - 1);",
+                          "if (kk < k) codes[r * k + (5 * b + 4 - i)] = (int8_t)(digit - 1);"),
+    "group_index": ("scales[nn * groups + kk / GROUP]", "scales[nn * groups + kk / 64 % groups]"),
+    "scale_divides": ("double t = xv * sv * (double)w[kk];", "double t = xv / sv * (double)w[kk];"),
+    "dropped_abs": ("nrm += fabs(t);", "nrm += t;"),
+    "transposed_x": ("double xv = oracle_half_to_double(x[mm * k + kk]);",
+                     "double xv = oracle_half_to_double(x[kk * m % (m * k) + mm]);"),
+    "half_bias": ("ldexp((double)(1024 + f), e - 25)", "ldexp((double)(1024 + f), e - 24)"),
+    "half_subnormal": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "xnor_group_scale": ("acc += sg * (double)dg;", "acc += sg * (double)total;"),
+    "xnor_sign": ("dg += (int64_t)a[kk] * (int64_t)w[kk];", "dg -= (int64_t)a[kk] * (int64_t)w[kk];"),
+    "ter_pad_bytes": ("return 64 * ((data + 63) / 64);", "return 16 * ((data + 15) / 16);"),
+    "ter_bad_byte": ("if (value > 242) return O_ERR_BAD_CODE;", "if (value > 255) return O_ERR_BAD_CODE;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutants_are_caught(name, tmp_path, oracle_lib):
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = open(oracle.SRC, encoding="utf-8").read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, "mutation anchor not found exactly once: " + name
+    path = tmp_path / ("oracle_%s.c" % name)
+    path.write_text(src.replace(old, new), encoding="utf-8")
+    so = tmp_path / ("liboracle_%s.so" % name)
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-o", str(so),
+                           str(path), "-lm"])
+    mutant = oracle.configure(ctypes.CDLL(str(so)))
+    prev = oracle.use_library(mutant)
+    caught = []
+    try:
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, oracle.OracleError, ValueError, pytest.fail.Exception):
+                caught.append(pin.__name__)
+    finally:
+        oracle.use_library(prev)
+    assert caught, "no pin caught mutant " + name
