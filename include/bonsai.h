@@ -56,9 +56,12 @@
  *   - Calls enqueue work on `stream` and return without synchronising (they
  *     can be captured in a CUDA graph). A non-OK return means nothing was
  *     launched. Kernel-side problems are reported by bonsai_check_async.
- *   - Calls launched with programmatic dependent launch: a kernel may start
- *     reading its weights before the previous kernel on the stream finishes,
- *     but reads x (and writes y) only after it has finished.
+ *   - Compute calls use programmatic dependent launch: a kernel may be
+ *     scheduled while the previous kernel on the stream is still running,
+ *     but it reads x (and writes y) only after that kernel has finished.
+ *     It also waits before reading its weights, unless the weights carry
+ *     BONSAI_WEIGHTS_PREFETCH: then it streams them at once, overlapping the
+ *     previous kernel's tail (decode loops whose weights never change).
  *   - No C++ exceptions cross this interface.
  * ------------------------------------------------------------------------
  */
@@ -88,10 +91,18 @@ typedef enum {
 
 enum { BONSAI_FMT_BINARY = 1, BONSAI_FMT_TERNARY = 2 };
 
+/* bonsai_weights.flags bits. */
+enum {
+  /* The packed bytes and scales are not written by the kernel launched just
+   * before this call on the same stream, so they may be read before that
+   * kernel has finished. */
+  BONSAI_WEIGHTS_PREFETCH = 1
+};
+
 /* A packed weight matrix W[n][k] with its FP16 group scales. */
 typedef struct {
   int32_t format;          /* BONSAI_FMT_BINARY or BONSAI_FMT_TERNARY        */
-  int32_t reserved;        /* must be 0                                      */
+  int32_t flags;           /* BONSAI_WEIGHTS_* bits, 0 if none               */
   int64_t n;               /* output features (rows of W)                    */
   int64_t k;               /* input features, multiple of 128                */
   int64_t row_bytes;       /* bytes per packed row (see layout above)        */

@@ -1,1 +1,188 @@
-"""Sub-bit (binary / ternary) weight products on NVIDIA B300 (sm_103a)."""
+"""Sub-bit (binary / ternary) weight products on NVIDIA B300 (sm_103a).
+
+Thin ctypes binding of libbonsai (include/bonsai.h): the functions below have
+the C names and only marshal arguments; every step runs in the CUDA kernels
+of libbonsai.so. PyTorch supplies device memory and streams. If the library
+is missing the calls raise: there is no CPU path.
+
+Build the library with ``python -m sub_bit_weight_binary_b300.build``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libbonsai.so")
+
+BONSAI_FMT_BINARY = 1
+BONSAI_FMT_TERNARY = 2
+BONSAI_WEIGHTS_PREFETCH = 1
+
+STATUS = {
+    0: "BONSAI_OK", 1: "BONSAI_ERR_INVALID_ARG", 2: "BONSAI_ERR_SHAPE",
+    3: "BONSAI_ERR_ALIGN", 4: "BONSAI_ERR_FORMAT", 5: "BONSAI_ERR_CUDA",
+    6: "BONSAI_ERR_UNSUPPORTED", 7: "BONSAI_ERR_TIMEOUT", 8: "BONSAI_ERR_BAD_CODE",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+
+class BonsaiError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s returned %s" % (what, STATUS.get(status, status)))
+        self.status = status
+
+
+class bonsai_weights_t(C.Structure):
+    _fields_ = [("format", C.c_int32), ("flags", C.c_int32), ("n", C.c_int64),
+                ("k", C.c_int64), ("row_bytes", C.c_int64), ("packed", C.c_void_p),
+                ("scales", C.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libbonsai.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libbonsai.so is not built: run "
+                              "python -m sub_bit_weight_binary_b300.build")
+        L = C.CDLL(LIB_PATH)
+        P, I64, I32, S = C.c_void_p, C.c_int64, C.c_int32, C.c_int
+        W = C.POINTER(bonsai_weights_t)
+        L.bonsai_packed_row_bytes.argtypes = [I32, I64]
+        L.bonsai_packed_row_bytes.restype = I64
+        for f in (L.bonsai_pack_binary, L.bonsai_pack_ternary):
+            f.argtypes = [P, I64, I64, P, I64, P]
+            f.restype = S
+        L.bonsai_gemv.argtypes = [W, P, P, P]
+        L.bonsai_gemv.restype = S
+        L.bonsai_gemm.argtypes = [W, P, I64, P, P]
+        L.bonsai_gemm.restype = S
+        L.bonsai_xnor_gemm.argtypes = [P, P, I64, W, P, P, P]
+        L.bonsai_xnor_gemm.restype = S
+        L.bonsai_check_async.argtypes = [P]
+        L.bonsai_check_async.restype = S
+        L.bonsai_status_string.argtypes = [S]
+        L.bonsai_status_string.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t, dtypes, name):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype not in dtypes:
+        raise ValueError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _ok(st: int, what: str):
+    if st != 0:
+        raise BonsaiError(st, what)
+
+
+@dataclass
+class Weights:
+    """A packed weight matrix W[n][k] and its FP16 group scales (device tensors).
+
+    packed: uint8 [n][row_bytes]; scales: float16 [n][k/128]."""
+    format: int
+    n: int
+    k: int
+    packed: "object"
+    scales: "object"
+    flags: int = 0
+
+    @property
+    def row_bytes(self) -> int:
+        return int(self.packed.shape[-1]) if self.packed.dim() == 2 else \
+            int(self.packed.numel() // self.n)
+
+    def c_struct(self) -> bonsai_weights_t:
+        import torch
+        return bonsai_weights_t(
+            self.format, self.flags, self.n, self.k, self.row_bytes,
+            _ptr(self.packed, (torch.uint8, torch.int32, torch.int8), "packed"),
+            _ptr(self.scales, (torch.float16, torch.int16), "scales"))
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, same names
+
+def bonsai_packed_row_bytes(fmt: int, k: int) -> int:
+    return int(lib().bonsai_packed_row_bytes(fmt, k))
+
+
+def bonsai_pack_binary(codes, out, stream=None):
+    import torch
+    rows, k = codes.shape
+    _ok(lib().bonsai_pack_binary(_ptr(codes, (torch.int8,), "codes"), rows, k,
+                                 _ptr(out, (torch.uint8,), "out"), out.shape[-1], _stream(stream)),
+        "bonsai_pack_binary")
+
+
+def bonsai_pack_ternary(codes, out, stream=None):
+    import torch
+    rows, k = codes.shape
+    _ok(lib().bonsai_pack_ternary(_ptr(codes, (torch.int8,), "codes"), rows, k,
+                                  _ptr(out, (torch.uint8,), "out"), out.shape[-1], _stream(stream)),
+        "bonsai_pack_ternary")
+
+
+def bonsai_gemv(w: Weights, x, y, stream=None):
+    import torch
+    ws = w.c_struct()
+    _ok(lib().bonsai_gemv(C.byref(ws), _ptr(x, (torch.float16,), "x"),
+                          _ptr(y, (torch.float16,), "y"), _stream(stream)), "bonsai_gemv")
+
+
+def bonsai_gemm(w: Weights, x, y, stream=None):
+    import torch
+    ws = w.c_struct()
+    m = x.shape[0] if x.dim() == 2 else 1
+    _ok(lib().bonsai_gemm(C.byref(ws), _ptr(x, (torch.float16,), "x"), m,
+                          _ptr(y, (torch.float16,), "y"), _stream(stream)), "bonsai_gemm")
+
+
+def bonsai_xnor_gemm(a_bits, a_scale, w: Weights, d_out=None, y_out=None, stream=None):
+    import torch
+    ws = w.c_struct()
+    _ok(lib().bonsai_xnor_gemm(_ptr(a_bits, (torch.int32, torch.uint8), "a_bits"),
+                               _ptr(a_scale, (torch.float16,), "a_scale"), a_bits.shape[0],
+                               C.byref(ws), _ptr(d_out, (torch.int32,), "d_out"),
+                               _ptr(y_out, (torch.float16,), "y_out"), _stream(stream)),
+        "bonsai_xnor_gemm")
+
+
+def bonsai_check_async(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(lib().bonsai_check_async(_stream(stream)))
+
+
+def bonsai_status_string(status: int) -> str:
+    return lib().bonsai_status_string(status).decode()
+
+
+def check(stream=None):
+    """bonsai_check_async that raises BonsaiError on a non-OK status."""
+    _ok(bonsai_check_async(stream), "bonsai_check_async")

@@ -1,0 +1,191 @@
+// api.cu -- the C ABI of libbonsai (declared in include/bonsai.h): argument
+// checks on the host, then one asynchronous launch on the caller's stream.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace bonsai {
+
+// Launchers and status readers of the other translation units.
+bonsai_status pack_binary_launch(const int8_t*, int64_t, int64_t, void*, int64_t, cudaStream_t);
+bonsai_status pack_ternary_launch(const int8_t*, int64_t, int64_t, void*, int64_t, cudaStream_t);
+bonsai_status gemv_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, cudaStream_t);
+bonsai_status gemm_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, cudaStream_t);
+bonsai_status xnor_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
+                          int32_t*, uint16_t*, cudaStream_t);
+unsigned int read_clear_status_pack();
+unsigned int read_clear_status_gemv();
+unsigned int read_clear_status_gemm();
+unsigned int read_clear_status_xnor();
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+int g_smem[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return dev;
+}
+
+void query(int dev) {
+  std::call_once(g_once[dev], [dev] {
+    cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&g_smem[dev], cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  });
+}
+}  // namespace
+
+int device_sm_count() {
+  const int dev = current_device();
+  query(dev);
+  return g_sms[dev] > 0 ? g_sms[dev] : 1;
+}
+
+int device_max_smem_optin() {
+  const int dev = current_device();
+  query(dev);
+  return g_smem[dev];
+}
+
+}  // namespace bonsai
+
+namespace {
+
+using namespace bonsai;
+
+constexpr int64_t kMaxK = 1 << 20;
+constexpr int64_t kMaxN = 1 << 30;
+constexpr int64_t kMaxM = 1 << 24;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bonsai_status check_row_bytes(int32_t format, int64_t k, int64_t row_bytes) {
+  if (format == BONSAI_FMT_BINARY) {
+    if (row_bytes < k / 8 || row_bytes % 16) return BONSAI_ERR_SHAPE;
+  } else {
+    if (row_bytes < bonsai_packed_row_bytes(BONSAI_FMT_TERNARY, k) || row_bytes % 64)
+      return BONSAI_ERR_SHAPE;
+  }
+  return BONSAI_OK;
+}
+
+bonsai_status check_weights(const bonsai_weights* w) {
+  if (!w || !w->packed || !w->scales) return BONSAI_ERR_INVALID_ARG;
+  if (w->format != BONSAI_FMT_BINARY && w->format != BONSAI_FMT_TERNARY)
+    return BONSAI_ERR_INVALID_ARG;
+  if (w->flags & ~int32_t(BONSAI_WEIGHTS_PREFETCH)) return BONSAI_ERR_INVALID_ARG;
+  if (w->n <= 0 || w->k <= 0 || w->row_bytes <= 0) return BONSAI_ERR_INVALID_ARG;
+  if (w->k % 128) return BONSAI_ERR_SHAPE;
+  if (w->k > kMaxK || w->n > kMaxN) return BONSAI_ERR_UNSUPPORTED;
+  bonsai_status st = check_row_bytes(w->format, w->k, w->row_bytes);
+  if (st != BONSAI_OK) return st;
+  if (!aligned16(w->packed) || !aligned16(w->scales)) return BONSAI_ERR_ALIGN;
+  return BONSAI_OK;
+}
+
+bonsai_status check_pack(const int8_t* codes, int64_t rows, int64_t k, void* out,
+                         int64_t row_bytes, int32_t format) {
+  if (!codes || !out) return BONSAI_ERR_INVALID_ARG;
+  if (rows < 0 || k <= 0 || row_bytes <= 0) return BONSAI_ERR_INVALID_ARG;
+  if (k % 128) return BONSAI_ERR_SHAPE;
+  if (k > kMaxK || rows > kMaxN) return BONSAI_ERR_UNSUPPORTED;
+  bonsai_status st = check_row_bytes(format, k, row_bytes);
+  if (st != BONSAI_OK) return st;
+  if (!aligned16(codes) || !aligned16(out)) return BONSAI_ERR_ALIGN;
+  return BONSAI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t bonsai_packed_row_bytes(int32_t format, int64_t k) {
+  if (k <= 0 || k % 128) return -1;
+  if (format == BONSAI_FMT_BINARY) return k / 8;
+  if (format == BONSAI_FMT_TERNARY) {
+    const int64_t data = (k + 4) / 5;
+    return 64 * ((data + 63) / 64);
+  }
+  return -1;
+}
+
+bonsai_status bonsai_pack_binary(const int8_t* codes, int64_t rows, int64_t k, void* out,
+                                 int64_t row_bytes, bonsai_stream stream) {
+  bonsai_status st = check_pack(codes, rows, k, out, row_bytes, BONSAI_FMT_BINARY);
+  if (st != BONSAI_OK) return st;
+  return pack_binary_launch(codes, rows, k, out, row_bytes, stream);
+}
+
+bonsai_status bonsai_pack_ternary(const int8_t* codes, int64_t rows, int64_t k, void* out,
+                                  int64_t row_bytes, bonsai_stream stream) {
+  bonsai_status st = check_pack(codes, rows, k, out, row_bytes, BONSAI_FMT_TERNARY);
+  if (st != BONSAI_OK) return st;
+  return pack_ternary_launch(codes, rows, k, out, row_bytes, stream);
+}
+
+bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
+                          bonsai_stream stream) {
+  bonsai_status st = check_weights(w);
+  if (st != BONSAI_OK) return st;
+  if (!x || !y) return BONSAI_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
+  return gemv_launch(w, x, 1, y, stream);
+}
+
+bonsai_status bonsai_gemm(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
+                          bonsai_stream stream) {
+  bonsai_status st = check_weights(w);
+  if (st != BONSAI_OK) return st;
+  if (!x || !y || m <= 0) return BONSAI_ERR_INVALID_ARG;
+  if (m > kMaxM) return BONSAI_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
+  if (m <= 8) {
+    st = gemv_launch(w, x, m, y, stream);
+    if (st != BONSAI_ERR_UNSUPPORTED) return st;
+  }
+  return gemm_launch(w, x, m, y, stream);
+}
+
+bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,
+                               const bonsai_weights* w, int32_t* d_out, uint16_t* y_out,
+                               bonsai_stream stream) {
+  bonsai_status st = check_weights(w);
+  if (st != BONSAI_OK) return st;
+  if (w->format != BONSAI_FMT_BINARY) return BONSAI_ERR_FORMAT;
+  if (!a_bits || !a_scale || m <= 0 || (!d_out && !y_out)) return BONSAI_ERR_INVALID_ARG;
+  if (m > kMaxM) return BONSAI_ERR_UNSUPPORTED;
+  if (!aligned16(a_bits) || !aligned16(a_scale) || (d_out && !aligned16(d_out)) ||
+      (y_out && !aligned16(y_out)))
+    return BONSAI_ERR_ALIGN;
+  return xnor_launch(a_bits, a_scale, m, w, d_out, y_out, stream);
+}
+
+bonsai_status bonsai_check_async(bonsai_stream stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BONSAI_ERR_CUDA;
+  const unsigned int codes[4] = {read_clear_status_pack(), read_clear_status_gemv(),
+                                 read_clear_status_gemm(), read_clear_status_xnor()};
+  if (cudaGetLastError() != cudaSuccess) return BONSAI_ERR_CUDA;
+  for (unsigned int c : codes)
+    if (c != 0) return static_cast<bonsai_status>(c);
+  return BONSAI_OK;
+}
+
+const char* bonsai_status_string(bonsai_status status) {
+  switch (status) {
+    case BONSAI_OK: return "BONSAI_OK";
+    case BONSAI_ERR_INVALID_ARG: return "BONSAI_ERR_INVALID_ARG";
+    case BONSAI_ERR_SHAPE: return "BONSAI_ERR_SHAPE";
+    case BONSAI_ERR_ALIGN: return "BONSAI_ERR_ALIGN";
+    case BONSAI_ERR_FORMAT: return "BONSAI_ERR_FORMAT";
+    case BONSAI_ERR_CUDA: return "BONSAI_ERR_CUDA";
+    case BONSAI_ERR_UNSUPPORTED: return "BONSAI_ERR_UNSUPPORTED";
+    case BONSAI_ERR_TIMEOUT: return "BONSAI_ERR_TIMEOUT";
+    case BONSAI_ERR_BAD_CODE: return "BONSAI_ERR_BAD_CODE";
+  }
+  return "BONSAI_ERR_UNKNOWN";
+}
+
+}  // extern "C"

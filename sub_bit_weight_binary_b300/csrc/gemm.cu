@@ -1,0 +1,466 @@
+// gemm.cu -- multi-token product Y = X . (s (.) W)^T on the 5th-generation
+// tensor cores (tcgen05), for prompt processing (pp512) and
+// diffusion-transformer image tokens. This case is a dense contraction:
+// every dequantised weight tile is reused by 256 tokens.
+//
+// One persistent CTA per SM, 16 warps with fixed roles:
+//   warp 0      TMA producer: X tiles [256 tokens x 64 k] FP16, 128-byte
+//               swizzle, straight into the MMA's canonical K-major layout.
+//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, M=128
+//               features x N=256 tokens x K=16, FP32 accumulators in TMEM.
+//   warp 2      TMEM allocator (512 columns = two accumulators, so the
+//               epilogue of tile i overlaps the main loop of tile i+1).
+//   warps 4-7   epilogue: tcgen05.ld -> FP16 (round to nearest even) -> Y.
+//   warps 8-15  dequantisers: packed codes -> FP16 s*w written into the
+//               swizzled A stage. The value is exact: s*(+-1) only flips the
+//               sign bit and s*0 is 0, so FP16 x FP16 products are exact in
+//               FP32 and only the FP32 sums round.
+// Scales follow the one-FP16-per-128-weights rule of the OpenBonsai page
+// ("工作原理"); the weights are +-1 ("1-bit 嘅數學") or -1/0/+1 (ternary).
+// Every mbarrier wait is bounded; a wait that runs out records
+// BONSAI_ERR_TIMEOUT and the kernel drains and leaves.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace bonsai {
+BONSAI_DEFINE_STATUS(g_status_gemm)
+
+unsigned int read_clear_status_gemm() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_status_gemm, sizeof(v));
+  cudaMemcpyToSymbol(g_status_gemm, &z, sizeof(z));
+  return v;
+}
+
+namespace gemm {
+
+constexpr int BM = 128;                 // features per tile  (MMA M)
+constexpr int BN = 256;                 // tokens per tile    (MMA N)
+constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of FP16
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B_BYTES = BN * BK * 2;    // 32 KB
+constexpr int TMEM_COLS = 512;
+constexpr int THREADS = 512;
+constexpr int W_TMA = 0, W_MMA = 1, W_TMEM = 2, W_EPI = 4, W_DQ = 8;
+constexpr int LUT_BYTES = 256 * 128;    // byte -> five 2-bit digits, one copy per lane
+constexpr int PLUT_BYTES = 16 * 128;    // digit pair -> FP16 pair of -1/0/+1, per lane
+constexpr int BAR_BYTES = 256;
+
+struct Params {
+  const uint8_t* w;
+  const __half* scales;
+  __half* y;
+  long long row_bytes;
+  int m, n, k, G, nk;
+  int tiles, tok_tiles;
+  int prefetch;
+};
+
+// ---- tcgen05 / TMA wrappers ------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+#define TMEM_LD_32(taddr, v)                                                              \
+  asm volatile(                                                                           \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"     \
+      "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31},"  \
+      " [%32];"                                                                           \
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),            \
+        "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),          \
+        "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),      \
+        "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),      \
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),      \
+        "=r"(v[30]), "=r"(v[31])                                                           \
+      : "r"(taddr))
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
+// 8-row core groups 1024 bytes apart (stride byte offset), Blackwell
+// descriptor version 1 (bits 46-47), swizzle mode 2 (bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: D=F32 (bits 4-5 = 1), A=B=F16 (0),
+// both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// ---- dequantisation of one row x 64 k into the swizzled A stage ------------
+// Row r of the stage lives at r*128 bytes; its 16-byte chunk c (codes
+// 8c..8c+7) is stored at chunk position c ^ (r & 7).
+__device__ __forceinline__ void dq_binary(const uint8_t* wrow, int kk, uint32_t s2,
+                                          uint32_t dst_row, int sw) {
+  const uint2 wv = *reinterpret_cast<const uint2*>(wrow + 8 * kk);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t x = ~(c < 4 ? wv.x : wv.y) >> (8 * (c & 3));
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t t2 = (x >> (2 * i)) & 3u;  // bit0: code k is -1, bit1: code k+1 is -1
+      h[i] = ((t2 * 0x40008000u) & 0x80008000u) ^ s2;
+    }
+    sts128(dst_row + ((c ^ sw) << 4), h[0], h[1], h[2], h[3]);
+  }
+}
+
+// Ternary k-step kk = 5u + V covers codes 64V..64V+63 of the 64-byte block u
+// (320 codes): they start in byte 64V/5 at digit 64V%5, known at compile time.
+template <int V>
+__device__ __forceinline__ void dq_ternary(const uint32_t (&wd)[16], uint32_t s2, uint32_t lut,
+                                           uint32_t plut, uint32_t dst_row, int sw) {
+  constexpr int T0 = 64 * V;
+  constexpr int B0 = T0 / 5;
+  constexpr int B1 = (T0 + 63) / 5;
+  uint32_t F[B1 - B0 + 1];
+#pragma unroll
+  for (int b = B0; b <= B1; ++b) {
+    const uint32_t byte = (wd[b >> 2] >> (8 * (b & 3))) & 0xFFu;
+    F[b - B0] = lds32(lut + byte * 128u);
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int T = T0 + 8 * c + 2 * i;
+      const int b = T / 5 - B0, d = T % 5;
+      const uint32_t nib = d < 4 ? (F[b] >> (2 * d)) & 0xFu
+                                 : ((F[b] >> 8) | ((F[b + 1] & 3u) << 2));
+      h[i] = hmul2_u32(lds32(plut + nib * 128u), s2);
+    }
+    sts128(dst_row + ((c ^ sw) << 4), h[0], h[1], h[2], h[3]);
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sA = smem_u32(smem);
+  const uint32_t sB = sA + STAGES * A_BYTES;
+  const uint32_t sLut = sB + STAGES * B_BYTES;
+  const uint32_t sPlut = sLut + LUT_BYTES;
+  const uint32_t sBar = FMT == BONSAI_FMT_TERNARY ? sPlut + PLUT_BYTES : sLut;
+  const uint32_t full_x = sBar, full_w = sBar + 8 * STAGES, empty = sBar + 16 * STAGES;
+  const uint32_t acc_full = sBar + 24 * STAGES, acc_empty = acc_full + 16;
+  const uint32_t drain = acc_empty + 16;
+  const uint32_t tmem_slot = drain + 8;
+
+  if ((sA & 1023u) != 0) {  // the swizzle atoms need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(BONSAI_ERR_UNSUPPORTED);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_x + 8 * s, 1);
+      mbar_init(full_w + 8 * s, 4);  // the 4 dequant warps of one parity group
+      mbar_init(empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full + 8 * a, 1);
+      mbar_init(acc_empty + 8 * a, 4);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (FMT == BONSAI_FMT_TERNARY && warp >= W_DQ) {
+    const int t = threadIdx.x - W_DQ * 32;  // 0..255
+    for (int i = t; i < 256 * 32; i += 256) {
+      const int e = i >> 5, ln = i & 31;
+      uint32_t v = 0;
+      if (e < 243) {
+        int r = e;
+        for (int d = 0; d < 5; ++d) { v |= uint32_t(r % 3) << (2 * d); r /= 3; }
+      }
+      asm volatile("st.shared.b32 [%0], %1;" ::"r"(sLut + e * 128 + ln * 4), "r"(v) : "memory");
+    }
+    for (int i = t; i < 16 * 32; i += 256) {
+      const int e = i >> 5, ln = i & 31;
+      const uint16_t val[4] = {0xBC00, 0x0000, 0x3C00, 0x0000};  // digit -> -1, 0, +1
+      const uint32_t v = uint32_t(val[e & 3]) | (uint32_t(val[e >> 2]) << 16);
+      asm volatile("st.shared.b32 [%0], %1;" ::"r"(sPlut + e * 128 + ln * 4), "r"(v) : "memory");
+    }
+  }
+  if (warp == W_TMEM) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  uint32_t tmem_base;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot) : "memory");
+
+  if (warp == W_TMA) {
+    // ------------------------------ X producer ------------------------------
+    if (lane == 0) {
+      pdl_wait();
+      uint32_t g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % p.tok_tiles) * BN;
+        for (int kk = 0; kk < p.nk; ++kk, ++g) {
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1;
+          if (!mbar_wait(empty + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
+          mbar_arrive_expect_tx(full_x + 8 * s, B_BYTES);
+          tma_load_2d(sB + s * B_BYTES, &tmx, kk * BK, m0, full_x + 8 * s);
+        }
+      }
+    }
+  } else if (warp == W_MMA) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      uint32_t g = 0, it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++it) {
+        const uint32_t a = it & 1, use = it >> 1;
+        if (!mbar_wait(acc_empty + 8 * a, (use & 1) ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + a * 256;
+        for (int kk = 0; kk < p.nk; ++kk, ++g) {
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1;
+          if (!mbar_wait(full_x + 8 * s, ph) || !mbar_wait(full_w + 8 * s, ph)) {
+            set_status(BONSAI_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(sA + s * A_BYTES);
+          const uint64_t bd = smem_desc_sw128(sB + s * B_BYTES);
+#pragma unroll
+          for (int k4 = 0; k4 < BK / 16; ++k4)  // +32 bytes per K=16 step inside the atom
+            mma_f16_ss(d_tmem, ad + 2 * k4, bd + 2 * k4, kIdesc, (kk | k4) != 0);
+          mma_commit(empty + 8 * s);
+        }
+        if (ok) mma_commit(acc_full + 8 * a);
+      }
+      mma_commit(drain);
+      if (!mbar_wait(drain, 0)) set_status(BONSAI_ERR_TIMEOUT);
+    }
+  } else if (warp >= W_EPI && warp < W_EPI + 4) {
+    // ------------------------------- epilogue -------------------------------
+    pdl_wait();
+    const int e = warp - W_EPI;  // TMEM lanes 32e .. 32e+31
+    uint32_t it = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
+      const uint32_t a = it & 1, use = it >> 1;
+      if (!mbar_wait(acc_full + 8 * a, use & 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
+      tc_fence_after();
+      const int n0 = (tile / p.tok_tiles) * BM, m0 = (tile % p.tok_tiles) * BN;
+      const int feat = n0 + 32 * e + lane;
+      const bool fok = feat < p.n;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        TMEM_LD_32(tmem_base + ((uint32_t)(32 * e) << 16) + a * 256 + 32 * c, v);
+        tmem_ld_wait();
+        if (c == BN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty + 8 * a);
+        }
+        if (fok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tok = m0 + 32 * c + j;
+            if (tok < p.m) p.y[(size_t)tok * p.n + feat] = __float2half_rn(__uint_as_float(v[j]));
+          }
+        }
+      }
+    }
+  } else if (warp >= W_DQ) {
+    // ------------------------------ dequantisers -----------------------------
+    if (!p.prefetch) pdl_wait();
+    const int dq = warp - W_DQ;         // 0..7
+    const uint32_t h = dq >> 2;         // parity group: even / odd k-steps
+    const int r = (dq & 3) * 32 + lane; // feature row within the tile
+    const int sw = r & 7;
+    const uint32_t lut = sLut + lane * 4, plut = sPlut + lane * 4;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      const int n = (tile / p.tok_tiles) * BM + r;
+      const bool nok = n < p.n;
+      const uint8_t* wrow = p.w + (long long)(nok ? n : 0) * p.row_bytes;
+      const __half* srow = p.scales + (size_t)(nok ? n : 0) * p.G;
+      for (int kk = 0; kk < p.nk; ++kk, ++g) {
+        if ((g & 1) != h) continue;
+        const int s = g % STAGES;
+        const uint32_t ph = (g / STAGES) & 1;
+        const uint32_t dst = sA + s * A_BYTES + r * 128;
+        const __half sc = srow[kk >> 1];
+        const uint32_t s2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;
+        uint32_t wd[16];
+        if (FMT == BONSAI_FMT_TERNARY) {
+          const uint4* src = reinterpret_cast<const uint4*>(wrow + 64 * (kk / 5));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 q4 = src[i];
+            wd[4 * i] = q4.x; wd[4 * i + 1] = q4.y; wd[4 * i + 2] = q4.z; wd[4 * i + 3] = q4.w;
+          }
+        }
+        if (!mbar_wait(empty + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
+        if (FMT == BONSAI_FMT_BINARY) {
+          dq_binary(wrow, kk, s2, dst, sw);
+        } else {
+          switch (kk % 5) {
+            case 0: dq_ternary<0>(wd, s2, lut, plut, dst, sw); break;
+            case 1: dq_ternary<1>(wd, s2, lut, plut, dst, sw); break;
+            case 2: dq_ternary<2>(wd, s2, lut, plut, dst, sw); break;
+            case 3: dq_ternary<3>(wd, s2, lut, plut, dst, sw); break;
+            default: dq_ternary<4>(wd, s2, lut, plut, dst, sw); break;
+          }
+        }
+        fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full_w + 8 * s);
+      }
+    }
+  }
+
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == W_TMEM) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiled>(f);
+  }();
+  return fn;
+}
+
+}  // namespace gemm
+
+bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
+                          cudaStream_t stream) {
+  using namespace gemm;
+  if (m > 0x7FFFFFFF / 2) return BONSAI_ERR_UNSUPPORTED;
+  EncodeTiled enc = encoder();
+  if (!enc) return BONSAI_ERR_CUDA;
+  CUtensorMap tm;
+  const cuuint64_t gdim[2] = {(cuuint64_t)w->k, (cuuint64_t)m};
+  const cuuint64_t gstride[1] = {(cuuint64_t)w->k * 2};
+  const cuuint32_t box[2] = {BK, BN};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), gdim, gstride, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return BONSAI_ERR_CUDA;
+
+  Params p{};
+  p.w = static_cast<const uint8_t*>(w->packed);
+  p.scales = reinterpret_cast<const __half*>(w->scales);
+  p.y = reinterpret_cast<__half*>(y);
+  p.row_bytes = w->row_bytes;
+  p.m = (int)m;
+  p.n = (int)w->n;
+  p.k = (int)w->k;
+  p.G = p.k / 128;
+  p.nk = p.k / BK;
+  p.tok_tiles = (int)((m + BN - 1) / BN);
+  p.tiles = ((p.n + BM - 1) / BM) * p.tok_tiles;
+  p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
+
+  const bool ter = w->format == BONSAI_FMT_TERNARY;
+  const int smem = STAGES * (A_BYTES + B_BYTES) + (ter ? LUT_BYTES + PLUT_BYTES : 0) + BAR_BYTES;
+  if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
+  const void* fn = ter ? (const void*)gemm_kernel<BONSAI_FMT_TERNARY>
+                       : (const void*)gemm_kernel<BONSAI_FMT_BINARY>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return BONSAI_ERR_CUDA;
+
+  const int sms = device_sm_count();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.tiles < sms ? p.tiles : sms);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = ter ? cudaLaunchKernelEx(&cfg, gemm_kernel<BONSAI_FMT_TERNARY>, tm, p)
+                      : cudaLaunchKernelEx(&cfg, gemm_kernel<BONSAI_FMT_BINARY>, tm, p);
+  return cuda_status(e);
+}
+
+}  // namespace bonsai

@@ -1,0 +1,136 @@
+// xnor.cu -- XNOR-popcount product of +-1 activations and +-1 weights.
+//
+// "1-bit 嘅數學" (1-bit diffusion page): a binary GEMM can be done with
+// XOR + popcount. With bit 1 = +1 and bit 0 = -1, the product of two codes is
+// +1 when the bits agree, so over a 128-code group
+//     d_g = sum a*w = 128 - 2 * popc(a XOR w)      (4 words)
+//     D   = sum_g d_g = K - 2 * popc(a XOR w)       (exact int32)
+//     Y   = a_s[m] * sum_g s[n][g] * d_g            (FP32, FP16 out)
+// The kernel is bound by the popcount pipe: one XOR and one POPC per 32
+// codes of each (m, n) pair; everything else is amortised over a 64x64 tile.
+#include "common.cuh"
+
+namespace bonsai {
+BONSAI_DEFINE_STATUS(g_status_xnor)
+
+unsigned int read_clear_status_xnor() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_status_xnor, sizeof(v));
+  cudaMemcpyToSymbol(g_status_xnor, &z, sizeof(z));
+  return v;
+}
+
+namespace xnor {
+
+constexpr int kBM = 64, kBN = 64;      // output tile
+constexpr int kThreads = 256;          // 16 x 16 threads, 4 x 4 outputs each
+constexpr int kCW = 32;                // words of K per smem chunk (8 groups)
+constexpr int kPitch = kCW + 4;        // padded row pitch (words)
+
+__global__ void __launch_bounds__(kThreads) xnor_kernel(
+    const uint32_t* __restrict__ a_bits, const __half* __restrict__ a_scale,
+    const uint32_t* __restrict__ w_bits, long long w_row_words, const __half* __restrict__ scales,
+    int m, int n, int k, int32_t* __restrict__ d_out, __half* __restrict__ y_out) {
+  __shared__ __align__(16) uint32_t As[kBM * kPitch];
+  __shared__ __align__(16) uint32_t Ws[kBN * kPitch];
+  __shared__ float Ss[kBN * (kCW / 4)];
+
+  pdl_wait();
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+  const int kw = k / 32, G = k / 128;
+
+  int dacc[4][4];
+  float yacc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { dacc[i][j] = 0; yacc[i][j] = 0.f; }
+
+  for (int c0 = 0; c0 < kw; c0 += kCW) {
+    const int cw = min(kCW, kw - c0);  // multiple of 4
+    __syncthreads();
+    // stage A and W chunks (rows past m / n are clamped; never stored)
+    for (int t = threadIdx.x; t < kBM * (kCW / 4); t += kThreads) {
+      const int r = t / (kCW / 4), v = t - r * (kCW / 4);
+      if (4 * v < cw) {
+        const int ra = min(m0 + r, m - 1), rw = min(n0 + r, n - 1);
+        *reinterpret_cast<uint4*>(&As[r * kPitch + 4 * v]) =
+            *reinterpret_cast<const uint4*>(a_bits + (long long)ra * kw + c0 + 4 * v);
+        *reinterpret_cast<uint4*>(&Ws[r * kPitch + 4 * v]) =
+            *reinterpret_cast<const uint4*>(w_bits + (long long)rw * w_row_words + c0 + 4 * v);
+      }
+    }
+    for (int t = threadIdx.x; t < kBN * (kCW / 4); t += kThreads) {
+      const int r = t / (kCW / 4), gg = t - r * (kCW / 4);
+      const int rw = min(n0 + r, n - 1);
+      const int gi = min(c0 / 4 + gg, G - 1);
+      Ss[r * (kCW / 4) + gg] = __half2float(scales[(long long)rw * G + gi]);
+    }
+    __syncthreads();
+    for (int gg = 0; gg < cw / 4; ++gg) {
+      uint4 av[4], wv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        av[i] = *reinterpret_cast<const uint4*>(&As[(ty + 16 * i) * kPitch + 4 * gg]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        wv[j] = *reinterpret_cast<const uint4*>(&Ws[(tx + 16 * j) * kPitch + 4 * gg]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float sg = Ss[(tx + 16 * j) * (kCW / 4) + gg];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int pc = __popc(av[i].x ^ wv[j].x) + __popc(av[i].y ^ wv[j].y) +
+                         __popc(av[i].z ^ wv[j].z) + __popc(av[i].w ^ wv[j].w);
+          const int dg = 128 - 2 * pc;
+          dacc[i][j] += dg;
+          // exact int -> float for |dg| <= 128 without the conversion pipe
+          const float fd = __int_as_float(0x4B400000 + dg) - 12582912.0f;
+          yacc[i][j] = fmaf(sg, fd, yacc[i][j]);
+        }
+      }
+    }
+  }
+
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = m0 + ty + 16 * i;
+    if (row >= m) continue;
+    const float as = __half2float(a_scale[row]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = n0 + tx + 16 * j;
+      if (col >= n) continue;
+      if (d_out) d_out[(long long)row * n + col] = dacc[i][j];
+      if (y_out) y_out[(long long)row * n + col] = __float2half_rn(as * yacc[i][j]);
+    }
+  }
+}
+
+}  // namespace xnor
+
+bonsai_status xnor_launch(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,
+                          const bonsai_weights* w, int32_t* d_out, uint16_t* y_out,
+                          cudaStream_t stream) {
+  using namespace xnor;
+  dim3 grid((unsigned)((w->n + kBN - 1) / kBN), (unsigned)((m + kBM - 1) / kBM));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(
+      &cfg, xnor_kernel, a_bits, reinterpret_cast<const __half*>(a_scale),
+      static_cast<const uint32_t*>(w->packed), (long long)(w->row_bytes / 4),
+      reinterpret_cast<const __half*>(w->scales), (int)m, (int)w->n, (int)w->k, d_out,
+      reinterpret_cast<__half*>(y_out));
+  return cuda_status(e);
+}
+
+}  // namespace bonsai

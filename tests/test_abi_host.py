@@ -1,0 +1,127 @@
+"""C ABI checks that need no GPU: the libraries build for sm_103a, export
+every function the headers declare, and reject bad arguments on the host
+before any CUDA call."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import oracle
+import sub_bit_weight_binary_b300 as sb
+from sub_bit_weight_binary_b300 import build as sbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libs():
+    paths = sbuild.build()
+    return {os.path.basename(p): C.CDLL(p) for p in paths}
+
+
+def declared(header):
+    text = open(os.path.join(ROOT, "include", header), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bonsai_\w+)\s*\(", text)))
+
+
+def test_headers_declare_the_boundary():
+    names = declared("bonsai.h")
+    for f in ("bonsai_packed_row_bytes", "bonsai_pack_binary", "bonsai_pack_ternary",
+              "bonsai_gemv", "bonsai_gemm", "bonsai_xnor_gemm", "bonsai_check_async",
+              "bonsai_status_string"):
+        assert f in names
+
+
+@pytest.mark.parametrize("header,lib", [("bonsai.h", "libbonsai.so"),
+                                        ("bonsai_synth.h", "libbonsai_synth.so")])
+def test_every_declared_symbol_is_exported(libs, header, lib):
+    L = libs[lib]
+    for name in declared(header):
+        assert hasattr(L, name), "%s does not export %s" % (lib, name)
+
+
+def test_built_for_sm103a():
+    # the objects carry sm_103a code (cuobjdump is not used: only the
+    # compiler's own record of the target in the build flags is checked)
+    assert "arch=compute_103a,code=sm_103a" in " ".join(sbuild.ARCH)
+
+
+def test_row_bytes_and_status_strings(libs, oracle_lib):
+    for fmt in (1, 2):
+        for k in (128, 256, 640, 1024, 5120, 17408):
+            assert sb.bonsai_packed_row_bytes(fmt, k) == oracle.row_bytes(fmt, k)
+        for bad in (0, -128, 100, 129):
+            assert sb.bonsai_packed_row_bytes(fmt, bad) == -1
+    assert sb.bonsai_packed_row_bytes(3, 128) == -1
+    for code, name in sb.STATUS.items():
+        assert sb.bonsai_status_string(code) == name
+    assert sb.bonsai_status_string(99) == "BONSAI_ERR_UNKNOWN"
+
+
+def W(fmt=1, n=16, k=256, row_bytes=None, packed=0x10000, scales=0x20000, flags=0):
+    if row_bytes is None:
+        row_bytes = sb.bonsai_packed_row_bytes(fmt, k)
+    return sb.bonsai_weights_t(fmt, flags, n, k, row_bytes, packed, scales)
+
+
+# Each case fails a host check, so nothing is launched and no pointer is read.
+BAD_GEMV = [
+    ("null packed", dict(packed=None), "BONSAI_ERR_INVALID_ARG"),
+    ("null scales", dict(scales=None), "BONSAI_ERR_INVALID_ARG"),
+    ("format", dict(fmt=3), "BONSAI_ERR_INVALID_ARG"),
+    ("flags", dict(flags=4), "BONSAI_ERR_INVALID_ARG"),
+    ("n=0", dict(n=0), "BONSAI_ERR_INVALID_ARG"),
+    ("k%128", dict(k=200, row_bytes=32), "BONSAI_ERR_SHAPE"),
+    ("short row", dict(row_bytes=16), "BONSAI_ERR_SHAPE"),
+    ("row%16", dict(row_bytes=40), "BONSAI_ERR_SHAPE"),
+    ("ter row%64", dict(fmt=2, row_bytes=80), "BONSAI_ERR_SHAPE"),
+    ("ter short", dict(fmt=2, k=5120, row_bytes=960), "BONSAI_ERR_SHAPE"),
+    ("align packed", dict(packed=0x10008), "BONSAI_ERR_ALIGN"),
+    ("align scales", dict(scales=0x20002), "BONSAI_ERR_ALIGN"),
+    ("huge k", dict(k=1 << 21, row_bytes=1 << 18), "BONSAI_ERR_UNSUPPORTED"),
+]
+
+
+@pytest.mark.parametrize("what,kw,expect", BAD_GEMV, ids=[c[0] for c in BAD_GEMV])
+def test_gemv_host_checks(libs, what, kw, expect):
+    L = sb.lib()
+    w = W(**kw)
+    st = L.bonsai_gemv(C.byref(w), 0x30000, 0x40000, None)
+    assert sb.STATUS[st] == expect
+
+
+def test_other_host_checks(libs):
+    L = sb.lib()
+    w = W()
+    assert sb.STATUS[L.bonsai_gemv(None, 0x30000, 0x40000, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[L.bonsai_gemv(C.byref(w), None, 0x40000, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[L.bonsai_gemv(C.byref(w), 0x30004, 0x40000, None)] == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[L.bonsai_gemm(C.byref(w), 0x30000, 0, 0x40000, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[L.bonsai_gemm(C.byref(w), 0x30000, 4, 0x40002, None)] == "BONSAI_ERR_ALIGN"
+    wt = W(fmt=2)
+    assert sb.STATUS[L.bonsai_xnor_gemm(0x50000, 0x60000, 4, C.byref(wt), 0x70000, None, None)] \
+        == "BONSAI_ERR_FORMAT"
+    assert sb.STATUS[L.bonsai_xnor_gemm(0x50000, 0x60000, 4, C.byref(w), None, None, None)] \
+        == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[L.bonsai_xnor_gemm(0x50004, 0x60000, 4, C.byref(w), 0x70000, None, None)] \
+        == "BONSAI_ERR_ALIGN"
+    for f in (L.bonsai_pack_binary, L.bonsai_pack_ternary):
+        assert sb.STATUS[f(None, 2, 128, 0x10000, 64, None)] == "BONSAI_ERR_INVALID_ARG"
+        assert sb.STATUS[f(0x10000, -1, 128, 0x20000, 64, None)] == "BONSAI_ERR_INVALID_ARG"
+        assert sb.STATUS[f(0x10000, 2, 100, 0x20000, 64, None)] == "BONSAI_ERR_SHAPE"
+        assert sb.STATUS[f(0x10001, 2, 128, 0x20000, 64, None)] == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[L.bonsai_pack_binary(0x10000, 2, 128, 0x20000, 8, None)] == "BONSAI_ERR_SHAPE"
+    assert sb.STATUS[L.bonsai_pack_ternary(0x10000, 2, 128, 0x20000, 32, None)] == "BONSAI_ERR_SHAPE"
+    # zero rows is a valid no-op (no launch)
+    assert sb.STATUS[L.bonsai_pack_binary(0x10000, 0, 128, 0x20000, 16, None)] == "BONSAI_OK"
+
+
+def test_binding_refuses_cpu_tensors(libs):
+    import torch
+    w = sb.Weights(1, 4, 128, torch.zeros(4, 16, dtype=torch.uint8),
+                   torch.zeros(4, 1, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        sb.bonsai_gemv(w, torch.zeros(128, dtype=torch.float16),
+                       torch.zeros(4, dtype=torch.float16), stream=0)
