@@ -2,16 +2,21 @@
 """Benchmark of the sub-bit weight products on B300. Prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--no-secondary]
 
-Default workload (the headline metric's configuration): ternary decode
-product M=1, K=5120, N=17408 ("batch-1 packed-weight GB/s"). A step is one
-pass of the decode kernel over one weight matrix; the timed loop rotates
-through enough distinct weight replicas that the working set exceeds L2.
-Other workloads (--workload): bin_gemv_1k, sweep_ter, sweep_bin, gemm512_ter,
-gemm512_bin, gemm4096_ter, gemm4096_bin, xnor.
+Headline workload (default, --workload ter_gemv): the ternary decode product
+M=1, K=5120, N=17408, metric "batch-1 packed-weight GB/s". A step is one
+launch of the decode kernel over one weight matrix; the K timed launches are
+captured into one CUDA graph and rotate through enough distinct weight
+replicas that the working set exceeds L2.
 
-Multi-GPU: the path has no exchange step, so N GPUs run N independent
+The line also carries `secondary` measurements of the other workloads:
+the binary decode product (K=N=1024), the 64-layer decode sweep (binary and
+ternary, tokens/s; one step = 448 products = one token), the prefill GEMM
+M=512 (binary and ternary, TFLOP/s) and the XNOR product 512x4096x4096.
+Each can also be the headline with --workload.
+
+Multi-GPU: the products have no exchange step, so N GPUs run N independent
 replicas (weak scaling); rank 0 prints the whole-job throughput over the
 max-over-ranks time. --impl reference times the CPU oracle instead.
 """
@@ -33,6 +38,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "batch-1 packed-weight GB/s (% HBM peak); 64-layer tok/s; pp512 TFLOP/s"
 L2_BYTES = 126 * 2 ** 20
+FLUSH_BYTES = 512 * 2 ** 20
+POPC_PER_CLK_SM = 16  # popc lane-ops per clock per SM (measured on B300 by a probe)
 
 
 # ------------------------------------------------------------------ helpers
@@ -41,15 +48,17 @@ def peaks():
     if os.path.exists(p):
         d = json.load(open(p))
         return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"],
-                "bf16_sustained": d["bf16_tflops_sustained"], "src": "measured"}
-    return {"hbm": 6400.0, "bf16": 1800.0, "bf16_sustained": 1400.0, "src": "fallback"}
+                "bf16_sustained": d["bf16_tflops_sustained"], "sm_max_mhz": d.get("sm_max_mhz"),
+                "src": "measured"}
+    return {"hbm": 6400.0, "bf16": 1800.0, "bf16_sustained": 1400.0, "sm_max_mhz": 2032.0,
+            "src": "fallback"}
 
 
 class ClockSampler:
-    """NVML samples of SM clock and throttle reasons during the timed region."""
-    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-               0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
-               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    """NVML samples of SM clock and throttle reasons during a timed region."""
+    REASONS = {0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index):
         self.samples, self.reasons, self.stop_flag = [], 0, False
@@ -59,25 +68,23 @@ class ClockSampler:
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self.nv = None
-            self.max_mhz = None
+        except Exception as e:  # noqa: BLE001
+            self.nv, self.max_mhz, self.err = None, None, str(e)
 
     def _one(self):
         try:
             self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
             self.reasons |= self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-        except Exception:
+        except Exception:  # noqa: BLE001
             pass
 
     def _run(self):
         while not self.stop_flag:
             self._one()
-            time.sleep(0.01)
+            time.sleep(0.005)
 
     def __enter__(self):
         if self.nv:
-            self._one()
             self.t = threading.Thread(target=self._run, daemon=True)
             self.t.start()
         return self
@@ -86,17 +93,17 @@ class ClockSampler:
         if self.nv:
             self.stop_flag = True
             self.t.join()
-            self._one()
 
     def report(self):
         if not self.nv or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["nvml unavailable"]}
-        names = [v for k, v in self.REASONS.items() if self.reasons & k and k != 0x1]
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
+                    "reasons": ["nvml unavailable: %s" % getattr(self, "err", "no samples")]}
+        names = [v for k, v in self.REASONS.items() if self.reasons & k]
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "samples": len(self.samples), "reasons": names}
 
 
-def dist_setup(ngpus):
+def dist_setup():
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -126,94 +133,146 @@ def max_over_ranks(world, value):
     return float(t.item())
 
 
+def make_weights(fmt, n, k, seed, tid_w, tid_s, flags):
+    """Seeded weights generated on the device (codes -> pack for ternary)."""
+    import torch
+    import sub_bit_weight_binary_b300 as sb
+    from sub_bit_weight_binary_b300 import synth_device as sd
+    rb = sb.bonsai_packed_row_bytes(fmt, k)
+    packed = torch.empty((n, rb), dtype=torch.uint8, device="cuda")
+    if fmt == sb.BONSAI_FMT_TERNARY:
+        codes = torch.empty((n, k), dtype=torch.int8, device="cuda")
+        sd.ternary_codes(seed, tid_w, 0, codes)
+        sb.bonsai_pack_ternary(codes, packed)
+        del codes
+    else:
+        sd.bits32(seed, tid_w, 0, packed.view(torch.int32))
+    scales = torch.empty((n, k // 128), dtype=torch.float16, device="cuda")
+    sd.uniform_f16(seed, tid_s, 0, 0.01, 0.05, scales)
+    return sb.Weights(fmt, n, k, packed, scales, flags)
+
+
+def weight_bytes(fmt, n, k):
+    import sub_bit_weight_binary_b300 as sb
+    return n * sb.bonsai_packed_row_bytes(fmt, k) + n * (k // 128) * 2
+
+
+def graph_time(fn_steps, steps, warmup, clocks=None):
+    """Capture `steps` launches in a CUDA graph (and `warmup` in another),
+    replay, return the elapsed milliseconds of the timed graph."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn_steps(0, 1)  # eager call first: one-time attribute setup outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    gw, gt = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gw):
+        fn_steps(0, warmup)
+    with torch.cuda.graph(gt):
+        fn_steps(warmup, steps)
+    gw.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.__enter__()
+    e0.record()
+    gt.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.__exit__()
+    return e0.elapsed_time(e1)
+
+
 # ---------------------------------------------------------------- workloads
 class GemvWorkload:
     """Decode product M=1 over rotating weight replicas."""
+    kind = "gemv"
 
     def __init__(self, fmt, n, k, cfg_id, name):
         self.fmt, self.n, self.k, self.cfg_id, self.name = fmt, n, k, cfg_id, name
 
     def unit_bytes(self):
-        import sub_bit_weight_binary_b300 as sb
-        rb = sb.bonsai_packed_row_bytes(self.fmt, self.k)
-        return self.n * rb + self.n * (self.k // 128) * 2  # packed + scales
+        return weight_bytes(self.fmt, self.n, self.k)
 
     def setup(self):
         import torch
         import sub_bit_weight_binary_b300 as sb
-        from sub_bit_weight_binary_b300 import synth, synth_device as sd
+        from sub_bit_weight_binary_b300 import synth
         seed = synth.config_seed(self.cfg_id)
-        n, k = self.n, self.k
         self.reps = max(1, math.ceil(2 * L2_BYTES / self.unit_bytes()) + 1)
-        rb = sb.bonsai_packed_row_bytes(self.fmt, k)
-        self.w = []
-        codes = torch.empty(n * k, dtype=torch.int8, device="cuda") \
-            if self.fmt == sb.BONSAI_FMT_TERNARY else None
-        for r in range(self.reps):
-            tid = synth.TID_WTER if self.fmt == sb.BONSAI_FMT_TERNARY else synth.TID_WBIN
-            packed = torch.empty((n, rb), dtype=torch.uint8, device="cuda")
-            if self.fmt == sb.BONSAI_FMT_TERNARY:
-                sd.ternary_codes(seed, tid + 64 * r, 0, codes)
-                sb.bonsai_pack_ternary(codes.view(n, k), packed)
-            else:
-                sd.bits32(seed, tid + 64 * r, 0, packed.view(torch.int32))
-            scales = torch.empty((n, k // 128), dtype=torch.float16, device="cuda")
-            sd.uniform_f16(seed, synth.TID_SCALES + 64 * r, 0, 0.01, 0.05, scales)
-            self.w.append(sb.Weights(self.fmt, n, k, packed, scales, sb.BONSAI_WEIGHTS_PREFETCH))
-        x = synth.gen_x(seed, 1, k)
-        self.x_host = torch.from_numpy(x.view(np.float16)[0]).pin_memory()
+        tid = synth.TID_WTER if self.fmt == sb.BONSAI_FMT_TERNARY else synth.TID_WBIN
+        self.w = [make_weights(self.fmt, self.n, self.k, seed, tid + 64 * r,
+                               synth.TID_SCALES + 64 * r, sb.BONSAI_WEIGHTS_PREFETCH)
+                  for r in range(self.reps)]
+        x = synth.gen_x(seed, 1, self.k)
+        self.x_host = torch.from_numpy(x.view(np.float16)[0].copy()).pin_memory()
         self.x = self.x_host.cuda()
-        self.y = torch.empty(n, dtype=torch.float16, device="cuda")
-        self.y_host = torch.empty(n, dtype=torch.float16).pin_memory()
+        self.y = torch.empty(self.n, dtype=torch.float16, device="cuda")
+        self.y_host = torch.empty(self.n, dtype=torch.float16).pin_memory()
         torch.cuda.synchronize()
         sb.check()
 
-    def step(self, i):
+    def launches(self, start, count):
         import sub_bit_weight_binary_b300 as sb
-        sb.bonsai_gemv(self.w[i % self.reps], self.x, self.y)
+        for i in range(start, start + count):
+            sb.bonsai_gemv(self.w[i % self.reps], self.x, self.y)
 
-    def step_e2e(self, i):
+    def measure(self, steps, warmup, clocks=None):
+        ms = graph_time(self.launches, steps, warmup, clocks)
+        return {"ms": ms, "steps": steps, "launches": steps, "kernel_ms": ms / steps}
+
+    def measure_e2e(self, steps, warmup):
+        """Eager calls through the binding, host x in, host y out, per step."""
+        import torch
         import sub_bit_weight_binary_b300 as sb
-        self.x.copy_(self.x_host, non_blocking=True)
-        sb.bonsai_gemv(self.w[i % self.reps], self.x, self.y)
-        self.y_host.copy_(self.y, non_blocking=True)
 
-    def io_bytes(self):
-        return self.k * 2, self.n * 2
+        def one(i):
+            self.x.copy_(self.x_host, non_blocking=True)
+            sb.bonsai_gemv(self.w[i % self.reps], self.x, self.y)
+            self.y_host.copy_(self.y, non_blocking=True)
+        for i in range(warmup):
+            one(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            one(i)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), self.k * 2, self.n * 2
 
-    def launches_per_step(self):
-        return 1
+    def value(self, ms, steps):
+        return self.unit_bytes() * steps / (ms / 1e3) / 1e9, "GB/s"
+
+    def roofline(self, r, pk):
+        a = self.unit_bytes() / (r["kernel_ms"] / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "gemv_kernel<%s>" % ("TERNARY" if self.fmt == 2 else "BINARY"),
+                "achieved": round(a, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(a / pk["hbm"], 4), "traffic": None,
+                "peak_src": "%s HBM copy (burst)" % pk["src"],
+                "bytes_per_launch": self.unit_bytes()}
 
     def config(self):
         return {"workload": self.name, "m": 1, "k": self.k, "n": self.n,
                 "format": "ternary" if self.fmt == 2 else "binary",
-                "weights": "synthetic seeded, resident in HBM",
+                "timing": "K launches captured in one CUDA graph",
                 "l2": "inputs larger than L2: %d rotating weight replicas, %.0f MB" % (
                     self.reps, self.reps * self.unit_bytes() / 1e6)}
 
-    def metric(self, sec_per_step):
-        return self.unit_bytes() / sec_per_step / 1e9, "GB/s"
-
-    def roofline(self, sec_per_step, pk):
-        a = self.unit_bytes() / sec_per_step / 1e9
-        return {"bound": "hbm", "achieved": round(a, 1), "peak": pk["hbm"], "unit": "GB/s",
-                "frac": round(a / pk["hbm"], 4), "traffic": None,
-                "peak_src": pk["src"] + " burst copy"}
-
-    # CPU oracle on a bounded sample: whole products, repeated for >= 10 s
     def cpu_sample(self, min_seconds=10.0, max_rows=None):
         import oracle
         from sub_bit_weight_binary_b300 import synth
         seed = synth.config_seed(self.cfg_id)
-        n, k = self.n, self.k
-        rows = min(n, max_rows or n)
+        rows = min(self.n, max_rows or self.n)
         if self.fmt == 2:
-            codes = synth.gen_ternary_codes(seed, rows, k)
-            packed = oracle.pack_ternary(codes)
+            packed = oracle.pack_ternary(synth.gen_ternary_codes(seed, rows, self.k))
         else:
-            packed = synth.gen_binary_words(seed, rows, k).view(np.uint8).reshape(rows, -1)
-        scales = synth.gen_scales(seed, rows, k)
-        x = synth.gen_x(seed, 1, k)
+            packed = synth.gen_binary_words(seed, rows, self.k).view(np.uint8).reshape(rows, -1)
+        scales = synth.gen_scales(seed, rows, self.k)
+        x = synth.gen_x(seed, 1, self.k)
         t0 = time.perf_counter()
         passes = 0
         while True:
@@ -222,103 +281,306 @@ class GemvWorkload:
             el = time.perf_counter() - t0
             if el >= min_seconds or el > 30:
                 break
-        bytes_done = passes * rows * (packed.shape[1] + 2 * (k // 128))
-        return bytes_done / el / 1e9, "%d pass(es) over %d of %d rows (%.1f s)" % (
-            passes, rows, n, el)
+        done = passes * rows * (packed.shape[1] + 2 * (self.k // 128))
+        return done / el / 1e9, "GB/s", "%d pass(es) over rows 0..%d of %d, one thread (%.1f s)" % (
+            passes, rows - 1, self.n, el)
+
+
+SWEEP_SHAPES = [(5120, 5120)] * 4 + [(17408, 5120)] * 2 + [(5120, 17408)]  # q k v o gate up down
+
+
+class SweepWorkload:
+    """64-layer decode: 7 products per layer, 448 per token, weights resident."""
+    kind = "sweep"
+
+    def __init__(self, fmt, name, layers=64):
+        self.fmt, self.name, self.layers = fmt, name, layers
+
+    def unit_bytes(self):
+        return self.layers * sum(weight_bytes(self.fmt, n, k) for n, k in SWEEP_SHAPES)
+
+    def setup(self):
+        import torch
+        import sub_bit_weight_binary_b300 as sb
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(3)
+        self.w = []
+        for layer in range(self.layers):
+            for j, (n, k) in enumerate(SWEEP_SHAPES):
+                tid = synth.sweep_tid(layer, j)
+                self.w.append(make_weights(self.fmt, n, k, seed, tid, tid + 8,
+                                           sb.BONSAI_WEIGHTS_PREFETCH))
+        self.x = {k: torch.from_numpy(synth.gen_x(seed + k, 1, k).view(np.float16)[0].copy()).cuda()
+                  for k in (5120, 17408)}
+        self.y = {n: torch.empty(n, dtype=torch.float16, device="cuda") for n in (5120, 17408)}
+        torch.cuda.synchronize()
+        sb.check()
+
+    def token(self):
+        import sub_bit_weight_binary_b300 as sb
+        for w in self.w:
+            sb.bonsai_gemv(w, self.x[w.k], self.y[w.n])
+
+    def launches(self, start, count):
+        for _ in range(count):
+            self.token()
+
+    def measure(self, steps, warmup, clocks=None):
+        import torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.token()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.token()
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if clocks:
+            clocks.__enter__()
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.__exit__()
+        ms = e0.elapsed_time(e1)
+        n = len(self.w)
+        return {"ms": ms, "steps": steps, "launches": steps * n, "kernel_ms": ms / (steps * n)}
+
+    def value(self, ms, steps):
+        return steps / (ms / 1e3), "tok/s"
+
+    def roofline(self, r, pk):
+        a = self.unit_bytes() / (r["ms"] / r["steps"] / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "gemv_kernel (448 per token)", "achieved": round(a, 1),
+                "peak": pk["hbm"], "unit": "GB/s", "frac": round(a / pk["hbm"], 4),
+                "traffic": None, "peak_src": "%s HBM copy (burst)" % pk["src"],
+                "bytes_per_token": self.unit_bytes()}
+
+    def config(self):
+        return {"workload": self.name, "layers": self.layers,
+                "shapes_nk": SWEEP_SHAPES, "format": "ternary" if self.fmt == 2 else "binary",
+                "timing": "one CUDA graph per token (448 launches), replayed per step",
+                "l2": "inputs larger than L2: %.2f GB of weights per token" % (self.unit_bytes() / 1e9)}
+
+
+class GemmWorkload:
+    """Prefill / DiT product on the tensor cores, K=5120, N=17408."""
+    kind = "gemm"
+
+    def __init__(self, fmt, m, name, n=17408, k=5120):
+        self.fmt, self.m, self.n, self.k, self.name = fmt, m, n, k, name
+
+    def flops(self):
+        return 2.0 * self.m * self.n * self.k
+
+    def setup(self):
+        import torch
+        import sub_bit_weight_binary_b300 as sb
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(4)
+        tid = synth.TID_WTER if self.fmt == 2 else synth.TID_WBIN
+        self.w = make_weights(self.fmt, self.n, self.k, seed, tid, synth.TID_SCALES, 0)
+        self.x = torch.from_numpy(synth.gen_x(seed, self.m, self.k).view(np.float16)).cuda()
+        self.y = torch.empty((self.m, self.n), dtype=torch.float16, device="cuda")
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        sb.check()
+
+    def call(self):
+        import sub_bit_weight_binary_b300 as sb
+        sb.bonsai_gemm(self.w, self.x, self.y)
+
+    def measure(self, steps, warmup, clocks=None):
+        """Per-step event pairs around the product; an L2 flush (a 512 MB
+        write) runs between steps, outside the timed pairs."""
+        import torch
+        for _ in range(warmup):
+            self.call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        if clocks:
+            clocks.__enter__()
+        for a, b in ev:
+            self.flush.zero_()
+            a.record()
+            self.call()
+            b.record()
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.__exit__()
+        ms = sum(a.elapsed_time(b) for a, b in ev)
+        return {"ms": ms, "steps": steps, "launches": steps, "kernel_ms": ms / steps}
+
+    def value(self, ms, steps):
+        return self.flops() * steps / (ms / 1e3) / 1e12, "TFLOP/s"
+
+    def roofline(self, r, pk):
+        a = self.flops() / (r["kernel_ms"] / 1e3) / 1e12
+        return {"bound": "tensor", "kernel": "gemm_kernel<%s>" % ("TERNARY" if self.fmt == 2 else "BINARY"),
+                "achieved": round(a, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": round(a / pk["bf16"], 4), "traffic": None,
+                "peak_src": "%s dense bf16 cuBLAS burst (fp16 has the same dense rate)" % pk["src"]}
+
+    def config(self):
+        return {"workload": self.name, "m": self.m, "k": self.k, "n": self.n,
+                "format": "ternary" if self.fmt == 2 else "binary",
+                "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
+
+
+class XnorWorkload:
+    kind = "xnor"
+
+    def __init__(self, name, m=512, n=4096, k=4096):
+        self.name, self.m, self.n, self.k = name, m, n, k
+
+    def words(self):
+        return self.m * self.n * (self.k // 32)
+
+    def setup(self):
+        import torch
+        import sub_bit_weight_binary_b300 as sb
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(5)
+        a_bits, a_s, w_bits, s = synth.gen_xnor_inputs(seed, self.m, self.n, self.k)
+        self.a = torch.from_numpy(a_bits.view(np.int32)).cuda()
+        self.a_s = torch.from_numpy(a_s.view(np.float16)).cuda()
+        self.w = sb.Weights(1, self.n, self.k,
+                            torch.from_numpy(w_bits.view(np.uint8).reshape(self.n, -1)).cuda(),
+                            torch.from_numpy(s.view(np.float16)).cuda())
+        self.d = torch.empty((self.m, self.n), dtype=torch.int32, device="cuda")
+        self.y = torch.empty((self.m, self.n), dtype=torch.float16, device="cuda")
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+
+    def call(self):
+        import sub_bit_weight_binary_b300 as sb
+        sb.bonsai_xnor_gemm(self.a, self.a_s, self.w, self.d, self.y)
+
+    measure = GemmWorkload.measure
+
+    def value(self, ms, steps):
+        return 2.0 * self.m * self.n * self.k * steps / (ms / 1e3) / 1e12, "bit-TOPS"
+
+    def roofline(self, r, pk, mhz=None):
+        mhz = mhz or pk["sm_max_mhz"] or 2032.0
+        peak = POPC_PER_CLK_SM * 148 * mhz * 1e6 / 1e12  # T popc/s
+        a = self.words() / (r["kernel_ms"] / 1e3) / 1e12
+        return {"bound": "alu", "kernel": "xnor_kernel", "achieved": round(a, 3), "peak": round(peak, 3),
+                "unit": "T word-popc/s", "frac": round(a / peak, 4), "traffic": None,
+                "peak_src": "16 popc/clk/SM x 148 SMs x %.0f MHz (popc rate measured by a probe)" % mhz}
+
+    def config(self):
+        return {"workload": self.name, "m": self.m, "k": self.k, "n": self.n,
+                "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
 
 
 WORKLOADS = {
     "ter_gemv": lambda: GemvWorkload(2, 17408, 5120, 2,
-                                     "ternary GEMV M=1 K=5120 N=17408 (decode, config 2)"),
-    "bin_gemv_1k": lambda: GemvWorkload(1, 1024, 1024, 1,
-                                        "binary GEMV M=1 K=1024 N=1024 (decode, config 1)"),
+                                     "ternary GEMV M=1 K=5120 N=17408 (decode)"),
+    "bin_gemv_1k": lambda: GemvWorkload(1, 1024, 1024, 1, "binary GEMV M=1 K=1024 N=1024 (decode)"),
+    "sweep_bin": lambda: SweepWorkload(1, "64-layer decode sweep, binary, batch 1"),
+    "sweep_ter": lambda: SweepWorkload(2, "64-layer decode sweep, ternary, batch 1"),
+    "gemm512_bin": lambda: GemmWorkload(1, 512, "prefill GEMM M=512 K=5120 N=17408, binary"),
+    "gemm512_ter": lambda: GemmWorkload(2, 512, "prefill GEMM M=512 K=5120 N=17408, ternary"),
+    "gemm4096_bin": lambda: GemmWorkload(1, 4096, "DiT GEMM M=4096 K=5120 N=17408, binary"),
+    "gemm4096_ter": lambda: GemmWorkload(2, 4096, "DiT GEMM M=4096 K=5120 N=17408, ternary"),
+    "xnor": lambda: XnorWorkload("XNOR-popcount GEMM M=512 K=4096 N=4096"),
 }
+SECONDARY = [("bin_gemv_1k", 20000, 50), ("sweep_bin", 30, 3), ("sweep_ter", 30, 3),
+             ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
+             ("gemm4096_ter", 5, 2), ("xnor", 20, 3)]
 
 
 # -------------------------------------------------------------------- runs
-def run_ours(args, world, rank, wl):
+def run_ours(args, world, rank):
     import torch
     import sub_bit_weight_binary_b300 as sb
     pk = peaks()
+    wl = WORKLOADS[args.workload]()
     wl.setup()
-    for i in range(args.warmup):
-        wl.step(i)
-    torch.cuda.synchronize()
-    sb.check()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        e0.record(stream)
-        for i in range(args.steps):
-            wl.step(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
+    clk = ClockSampler(torch.cuda.current_device())
+    r = wl.measure(args.steps, args.warmup, clk)
     barrier(world)
-    ms = e0.elapsed_time(e1)
-    ms = max_over_ranks(world, ms)
-    sec = ms / 1e3 / args.steps
-    val, unit = wl.metric(sec)
+    ms = max_over_ranks(world, r["ms"])
+    val, unit = wl.value(ms, r["steps"])
     sb.check()
-
-    # end to end through the C ABI with host buffers (copies in the timed region)
-    for i in range(args.warmup):
-        wl.step_e2e(i)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0.record(stream)
-    for i in range(args.steps):
-        wl.step_e2e(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(world, e0.elapsed_time(e1))
-    e2e_val, _ = wl.metric(ms_e2e / 1e3 / args.steps)
-    bi, bo = wl.io_bytes()
-    sb.check()
-
-    if rank != 0:
-        return None
     line = {
-        "metric": METRIC, "value": round(val * world, 2), "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
+        "metric": METRIC, "value": round(val * world, 3), "unit": unit, "n_gpus": world,
+        "steps": r["steps"], "warmup": args.warmup, "ms_per_step": round(ms / r["steps"], 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic (seeded counter-based generator; no trained weights)",
-        "config": dict(wl.config(), parallelism="replicas only" if world > 1 else "1 GPU"),
-        "roofline": wl.roofline(sec, pk),
-        "e2e": {"value": round(e2e_val * world, 2), "unit": unit,
-                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
-        "gpu_launches": wl.launches_per_step() * args.steps,
+        "data": "synthetic (seeded counter-based generator; random weights, no checkpoint)",
+        "config": dict(wl.config(), parallelism="replicas only, %d GPU(s)" % world),
+        "roofline": wl.roofline(r, pk) if wl.kind != "xnor" else wl.roofline(r, pk, None),
+        "gpu_launches": r["launches"],
         "clocks": clk.report(),
     }
-    if not args.no_cpu_baseline and world == 1:
-        v, sample = wl.cpu_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": unit, "cores": 1, "kind": "oracle",
+    if wl.kind == "gemv":
+        ms_e, bi, bo = wl.measure_e2e(min(args.steps, 2000), args.warmup)
+        ms_e = max_over_ranks(world, ms_e)
+        ev, _ = wl.value(ms_e, min(args.steps, 2000))
+        line["e2e"] = {"value": round(ev * world, 3), "unit": unit, "h2d_bytes_per_step": bi,
+                       "d2h_bytes_per_step": bo,
+                       "how": "eager Python calls of the binding, pinned host x copied in and y "
+                              "copied out every step"}
+    sb.check()
+    if rank == 0 and not args.no_cpu_baseline and world == 1 and hasattr(wl, "cpu_sample"):
+        v, u, sample = wl.cpu_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(v, 5), "unit": u, "cores": 1, "kind": "oracle",
                                 "sample": sample}
-    return line
+    if rank == 0 and not args.no_secondary and world == 1:
+        sec = []
+        del wl
+        torch.cuda.empty_cache()
+        for name, steps, warm in SECONDARY:
+            if name == args.workload:
+                continue
+            w2 = WORKLOADS[name]()
+            w2.setup()
+            c2 = ClockSampler(torch.cuda.current_device())
+            r2 = w2.measure(steps, warm, c2)
+            v2, u2 = w2.value(r2["ms"], r2["steps"])
+            sec.append({"workload": w2.name, "value": round(v2, 3), "unit": u2,
+                        "steps": r2["steps"], "ms_per_step": round(r2["ms"] / r2["steps"], 6),
+                        "roofline": w2.roofline(r2, pk), "gpu_launches": r2["launches"],
+                        "clocks": c2.report()})
+            sb.check()
+            del w2
+            torch.cuda.empty_cache()
+        line["secondary"] = sec
+    return line if rank == 0 else None
 
 
-def run_reference(args, world, rank, wl):
+def run_reference(args, world, rank):
     if rank != 0:
         return None
-    # the oracle, as it stands, on the machine's host cores; each step is a
-    # bounded sample (a row slice) of the workload
-    per_step = []
+    wl = WORKLOADS[args.workload]()
+    if not hasattr(wl, "cpu_sample"):
+        return {"impl": "reference", "unavailable": "the CPU oracle arm is defined for the "
+                "decode workloads only"}
     rows = max(1, min(wl.n, 2048))
+    per_step = []
     for i in range(args.warmup + args.steps):
-        v, _ = wl.cpu_sample(min_seconds=0.0, max_rows=rows)
+        v, unit, _ = wl.cpu_sample(min_seconds=0.0, max_rows=rows)
         if i >= args.warmup:
             per_step.append(v)
     val = statistics.median(per_step)
-    sample = "each step: one oracle pass over %d of %d rows" % (rows, wl.n)
+    sample = "each step: one oracle pass over rows 0..%d of %d" % (rows - 1, wl.n)
     return {
-        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+        "impl": "reference", "metric": METRIC, "value": round(val, 5), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded counter-based generator)", "config": wl.config(),
-        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(val, 5), "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(val, 5), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 
@@ -326,24 +588,23 @@ def run_reference(args, world, rank, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="ter_gemv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
-        world = int(os.environ.get("WORLD_SIZE", "1"))
-        rank = int(os.environ.get("RANK", "0"))
-        line = run_reference(args, world, rank, wl)
+        line = run_reference(args, int(os.environ.get("WORLD_SIZE", "1")),
+                             int(os.environ.get("RANK", "0")))
     else:
         from sub_bit_weight_binary_b300 import build
         build.build()
-        world, rank, _ = dist_setup(args.gpus)
-        line = run_ours(args, world, rank, wl)
+        world, rank, _ = dist_setup()
+        line = run_ours(args, world, rank)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()

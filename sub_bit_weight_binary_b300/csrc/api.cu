@@ -50,6 +50,26 @@ int device_max_smem_optin() {
   return g_smem[dev];
 }
 
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
+  struct Entry { const void* fn; int dev; int bytes; };
+  static std::mutex mu;
+  static Entry table[256];
+  static int used = 0;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i) {
+    if (table[i].fn == kernel && table[i].dev == dev) {
+      if (table[i].bytes >= bytes) return cudaSuccess;
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) table[i].bytes = bytes;
+      return e;
+    }
+  }
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && used < 256) table[used++] = Entry{kernel, dev, bytes};
+  return e;
+}
+
 }  // namespace bonsai
 
 namespace {

@@ -149,5 +149,9 @@ inline bonsai_status cuda_status(cudaError_t e) {
 
 int device_sm_count();
 int device_max_smem_optin();
+// Raises a kernel's dynamic shared-memory limit on the current device once
+// (later calls with the same or a smaller size touch no CUDA API, so launches
+// can be captured into a CUDA graph after a first eager call).
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
 
 }  // namespace bonsai

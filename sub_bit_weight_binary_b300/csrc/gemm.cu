@@ -444,7 +444,7 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
   const void* fn = ter ? (const void*)gemm_kernel<BONSAI_FMT_TERNARY>
                        : (const void*)gemm_kernel<BONSAI_FMT_BINARY>;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (ensure_dynamic_smem(fn, smem) != cudaSuccess)
     return BONSAI_ERR_CUDA;
 
   const int sms = device_sm_count();

@@ -102,6 +102,74 @@ __device__ __forceinline__ uint32_t ter_operand(uint32_t f, uint32_t fl) {
 __constant__ int c_var_round[kTerVariants] = {0, 1, 1, 2, 3, 3, 4, 4, 5, 6, 6, 7};
 __constant__ int c_var_group[kTerVariants] = {0, 0, 1, 1, 1, 2, 2, 3, 3, 3, 4, 4};
 
+// Fills the operands of digit MD for rows g (fa*) and g+8 (fb*).
+template <int MD>
+__device__ __forceinline__ void ter_fill(uint32_t (&A)[5][4], uint32_t fa01, uint32_t fb01,
+                                         uint32_t fa23, uint32_t fb23) {
+  A[MD][0] = ter_operand<MD>(fa01, fa01 << 4);
+  A[MD][1] = ter_operand<MD>(fb01, fb01 << 4);
+  A[MD][2] = ter_operand<MD>(fa23, fa23 << 4);
+  A[MD][3] = ter_operand<MD>(fb23, fb23 << 4);
+}
+
+// Operands of a row whose five digits all equal 1 (code 0): the neutral
+// pattern whose MMA sum is subtracted from every row's sum.
+__device__ __forceinline__ void ter_neutral(uint32_t (&A)[5][4]) {
+#pragma unroll
+  for (int md = 0; md < 5; ++md) {
+    const int j = ter_j(md);
+    const uint32_t v = exp_base(j) | (1u << j) | (1u << (j + 16));
+    A[md][0] = A[md][1] = A[md][2] = A[md][3] = v;
+  }
+}
+
+// One 640-code super-group of a 16-row tile: 8 rounds of 80 codes, 5 MMAs
+// per round, plus a second pass with the next group's x-table variant when
+// a round straddles a 128-code group edge. `operands(rnd, A)` produces the
+// expanded codes of a round, `epi(grp, acc)` consumes a finished group.
+// The same sequence of MMAs runs for the neutral pattern in the prologue,
+// so an all-zero group cancels exactly.
+template <typename Ops, typename Epi>
+__device__ __forceinline__ void ter_supergroup(const uint8_t* xt, bool bcol, Ops&& operands,
+                                               Epi&& epi) {
+  float accA[4] = {0.f, 0.f, 0.f, 0.f}, accB[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int rnd = 0; rnd < 8; ++rnd) {
+    uint32_t A[5][4];
+    operands(rnd, A);
+    // first variant of the round; second one if the round straddles a group edge
+    const int v0 = (rnd == 0) ? 0 : (rnd == 1) ? 1 : (rnd == 2) ? 3 : (rnd == 3) ? 4
+                 : (rnd == 4) ? 6 : (rnd == 5) ? 8 : (rnd == 6) ? 9 : 11;
+    const bool split = (rnd == 1 || rnd == 3 || rnd == 4 || rnd == 6);
+    const int grp0 = (rnd <= 1) ? 0 : (rnd <= 3) ? 1 : (rnd == 4) ? 2 : (rnd <= 6) ? 3 : 4;
+    auto run = [&](float (&acc)[4], int v) {
+      const uint4* bp = reinterpret_cast<const uint4*>(xt + v * 4 * kTerEntry);
+      const uint4 b0 = bcol ? bp[0] : make_uint4(0, 0, 0, 0);
+      const uint4 b1 = bcol ? bp[1] : make_uint4(0, 0, 0, 0);
+      const uint4 b2 = bcol ? bp[2] : make_uint4(0, 0, 0, 0);
+      mma_16816(acc, A[0][0], A[0][1], A[0][2], A[0][3], b0.x, b0.y);
+      mma_16816(acc, A[1][0], A[1][1], A[1][2], A[1][3], b0.z, b0.w);
+      mma_16816(acc, A[2][0], A[2][1], A[2][2], A[2][3], b1.x, b1.y);
+      mma_16816(acc, A[3][0], A[3][1], A[3][2], A[3][3], b1.z, b1.w);
+      mma_16816(acc, A[4][0], A[4][1], A[4][2], A[4][3], b2.x, b2.y);
+    };
+    // groups 0,2,4 accumulate in accA, groups 1,3 in accB
+    if ((grp0 & 1) == 0) run(accA, v0); else run(accB, v0);
+    if (split) {
+      if ((grp0 & 1) == 0) {
+        run(accB, v0 + 1);
+        epi(grp0, accA);
+        accA[0] = accA[1] = accA[2] = accA[3] = 0.f;
+      } else {
+        run(accA, v0 + 1);
+        epi(grp0, accB);
+        accB[0] = accB[1] = accB[2] = accB[3] = 0.f;
+      }
+    }
+  }
+  epi(4, accA);  // group 4 ends with round 7
+}
+
 // ---- per-CTA tables from x -------------------------------------------------
 template <int FMT>
 __device__ void build_tables(const Params& p, uint8_t* smem) {
@@ -194,20 +262,24 @@ __device__ void build_tables(const Params& p, uint8_t* smem) {
       dst[1] = make_uint4(e[4], e[5], e[6], e[7]);
       dst[2] = make_uint4(e[8], e[9], e[10], e[11]);
     }
-    const int tg = p.n_sg * 5;
-    for (int t = tid; t < p.m * tg; t += nthr) {
-      const int col = t / tg, gi = t - col * tg;
-      const __half* xs = p.x + (size_t)col * p.k;
-      float S4 = 0.f, S6 = 0.f, S8 = 0.f, X = 0.f;
-      for (int kk = 128 * gi; kk < 128 * gi + 128 && kk < p.k; ++kk) {
-        const float v = __half2float(xs[kk]);
-        const int md = kk % 5;
-        if (md == 4) S8 += v;
-        else if (md & 1) S6 += v;
-        else S4 += v;
-        X += v;
+    // T = MMA sum of the neutral (all-zero-code) pattern per group and
+    // token, computed with the very MMA sequence of the main loop.
+    named_bar_sync(1, nthr);  // x table complete
+    {
+      const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+      const bool bcol = g < p.m;
+      const uint8_t* xt_col = smem + p.off_xt + (bcol ? g : 0) * p.xt_stride;
+      for (int sg = warp; sg < p.n_sg; sg += kWarps) {
+        const uint8_t* xt = xt_col + (sg * kTerVariants * 4 + q) * kTerEntry;
+        auto operands = [&](int, uint32_t (&A)[5][4]) { ter_neutral(A); };
+        auto epi = [&](int grp, const float (&acc)[4]) {
+          if (g == 0) {
+            T[(5 * sg + grp) * 8 + 2 * q] = acc[0];
+            T[(5 * sg + grp) * 8 + 2 * q + 1] = acc[1];
+          }
+        };
+        ter_supergroup(xt, bcol, operands, epi);
       }
-      T[gi * 8 + col] = X + 64.f * S4 + 16.f * S6 + 4.f * S8;
     }
   }
 }
@@ -360,69 +432,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           const uint32_t* r0 = stg + g * pw + warp * 32 + q;
           const uint32_t* r1 = stg + (g + 8) * pw + warp * 32 + q;
           const uint8_t* xt = xt_col + (sg * kTerVariants * 4 + q) * kTerEntry;
-          float accA[4] = {0.f, 0.f, 0.f, 0.f}, accB[4] = {0.f, 0.f, 0.f, 0.f};
-          auto lookup = [&](uint32_t wd, int i) -> uint32_t {
-            const uint32_t off = __byte_perm(wd, lut_lane, 0x5504 | (i << 4));
-            return *reinterpret_cast<const uint32_t*>(lut + off);
-          };
-#pragma unroll
-          for (int rnd = 0; rnd < 8; ++rnd) {
+          auto operands = [&](int rnd, uint32_t (&A)[5][4]) {
             const uint32_t wa = r0[4 * rnd], wb = r1[4 * rnd];
+            auto lookup = [&](uint32_t wd, int i) -> uint32_t {
+              const uint32_t off = __byte_perm(wd, lut_lane, 0x5504 | (i << 4));
+              return *reinterpret_cast<const uint32_t*>(lut + off);
+            };
             const uint32_t fa01 = lookup(wa, 0) + (lookup(wa, 1) << 16);
             const uint32_t fa23 = lookup(wa, 2) + (lookup(wa, 3) << 16);
             const uint32_t fb01 = lookup(wb, 0) + (lookup(wb, 1) << 16);
             const uint32_t fb23 = lookup(wb, 2) + (lookup(wb, 3) << 16);
-            const uint32_t fa01l = fa01 << 4, fa23l = fa23 << 4;
-            const uint32_t fb01l = fb01 << 4, fb23l = fb23 << 4;
-            const uint32_t A[5][4] = {
-                {ter_operand<0>(fa01, fa01l), ter_operand<0>(fb01, fb01l),
-                 ter_operand<0>(fa23, fa23l), ter_operand<0>(fb23, fb23l)},
-                {ter_operand<1>(fa01, fa01l), ter_operand<1>(fb01, fb01l),
-                 ter_operand<1>(fa23, fa23l), ter_operand<1>(fb23, fb23l)},
-                {ter_operand<2>(fa01, fa01l), ter_operand<2>(fb01, fb01l),
-                 ter_operand<2>(fa23, fa23l), ter_operand<2>(fb23, fb23l)},
-                {ter_operand<3>(fa01, fa01l), ter_operand<3>(fb01, fb01l),
-                 ter_operand<3>(fa23, fa23l), ter_operand<3>(fb23, fb23l)},
-                {ter_operand<4>(fa01, fa01l), ter_operand<4>(fb01, fb01l),
-                 ter_operand<4>(fa23, fa23l), ter_operand<4>(fb23, fb23l)}};
-            // variants of this round: first, and second if it straddles a group edge
-            const int v0 = (rnd == 0) ? 0 : (rnd == 1) ? 1 : (rnd == 2) ? 3 : (rnd == 3) ? 4
-                         : (rnd == 4) ? 6 : (rnd == 5) ? 8 : (rnd == 6) ? 9 : 11;
-            const bool split = (rnd == 1 || rnd == 3 || rnd == 4 || rnd == 6);
-            // accumulator of the first variant: groups 0,2,4 -> A; 1,3 -> B
-            const int grp0 = (rnd == 0 || rnd == 1) ? 0 : (rnd <= 3) ? 1 : (rnd == 4) ? 2
-                           : (rnd <= 6) ? 3 : 4;
-            auto run = [&](float (&acc)[4], int v) {
-              const uint4* bp = reinterpret_cast<const uint4*>(xt + v * 4 * kTerEntry);
-              const uint4 b0 = bcol ? bp[0] : make_uint4(0, 0, 0, 0);
-              const uint4 b1 = bcol ? bp[1] : make_uint4(0, 0, 0, 0);
-              const uint4 b2 = bcol ? bp[2] : make_uint4(0, 0, 0, 0);
-              mma_16816(acc, A[0][0], A[0][1], A[0][2], A[0][3], b0.x, b0.y);
-              mma_16816(acc, A[1][0], A[1][1], A[1][2], A[1][3], b0.z, b0.w);
-              mma_16816(acc, A[2][0], A[2][1], A[2][2], A[2][3], b1.x, b1.y);
-              mma_16816(acc, A[3][0], A[3][1], A[3][2], A[3][3], b1.z, b1.w);
-              mma_16816(acc, A[4][0], A[4][1], A[4][2], A[4][3], b2.x, b2.y);
-            };
-            if ((grp0 & 1) == 0) run(accA, v0); else run(accB, v0);
-            if (split) {
-              if ((grp0 & 1) == 0) run(accB, v0 + 1); else run(accA, v0 + 1);
-              // group grp0 is complete
-              const int gi = 5 * sg + grp0;
-              const float2 tt = *reinterpret_cast<const float2*>(T + gi * 8 + 2 * q);
-              if ((grp0 & 1) == 0) {
-                group_epilogue<FMT>(yacc, accA, tt, s0[grp0], s1[grp0]);
-                accA[0] = accA[1] = accA[2] = accA[3] = 0.f;
-              } else {
-                group_epilogue<FMT>(yacc, accB, tt, s0[grp0], s1[grp0]);
-                accB[0] = accB[1] = accB[2] = accB[3] = 0.f;
-              }
-            }
-          }
-          {  // group 4 ends with round 7
-            const int gi = 5 * sg + 4;
+            ter_fill<0>(A, fa01, fb01, fa23, fb23);
+            ter_fill<1>(A, fa01, fb01, fa23, fb23);
+            ter_fill<2>(A, fa01, fb01, fa23, fb23);
+            ter_fill<3>(A, fa01, fb01, fa23, fb23);
+            ter_fill<4>(A, fa01, fb01, fa23, fb23);
+          };
+          auto epi = [&](int grp, const float (&acc)[4]) {
+            const int gi = 5 * sg + grp;
             const float2 tt = *reinterpret_cast<const float2*>(T + gi * 8 + 2 * q);
-            group_epilogue<FMT>(yacc, accA, tt, s0[4], s1[4]);
-          }
+            yacc[0] = fmaf(s0[grp], (acc[0] - tt.x) * 1024.f, yacc[0]);
+            yacc[1] = fmaf(s0[grp], (acc[1] - tt.y) * 1024.f, yacc[1]);
+            yacc[2] = fmaf(s1[grp], (acc[2] - tt.x) * 1024.f, yacc[2]);
+            yacc[3] = fmaf(s1[grp], (acc[3] - tt.y) * 1024.f, yacc[3]);
+          };
+          ter_supergroup(xt, bcol, operands, epi);
         }
       }
       __syncwarp();
@@ -500,7 +534,7 @@ bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
 
   const void* fn = fmt == BONSAI_FMT_BINARY ? (const void*)gemv_kernel<BONSAI_FMT_BINARY>
                                             : (const void*)gemv_kernel<BONSAI_FMT_TERNARY>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_dynamic_smem(fn, smem);
   if (e != cudaSuccess) return BONSAI_ERR_CUDA;
 
   const int sms = device_sm_count();

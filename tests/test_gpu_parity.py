@@ -265,3 +265,38 @@ def test_xnor_workload():
         assert np.array_equal(dg[i:i + 64].astype(np.int64), ref)
     d.check()
     y.check()
+
+
+# ------------------------------------------------------------ graph capture
+def test_graph_capture_matches_eager():
+    """Launches captured into a CUDA graph (programmatic dependent launch
+    edges included) give the same bits as eager launches."""
+    t = torch()
+    wb, _, _ = weights(BIN, 5, 640, 1024, flags=sb.BONSAI_WEIGHTS_PREFETCH)
+    wt, _, _ = weights(TER, 6, 900, 5120, flags=sb.BONSAI_WEIGHTS_PREFETCH)
+    x1 = dev(synth.gen_x(1, 1, 1024)[0])
+    x2 = dev(synth.gen_x(2, 1, 5120)[0])
+    xm = dev(synth.gen_x(3, 300, 5120))
+
+    def run(ys):
+        sb.bonsai_gemv(wb, x1, ys[0])
+        sb.bonsai_gemv(wt, x2, ys[1])
+        sb.bonsai_gemm(wt, xm, ys[2])
+        sb.bonsai_gemv(wb, x1, ys[3])
+
+    def bufs():
+        return [t.empty(640, dtype=t.float16, device="cuda"),
+                t.empty(900, dtype=t.float16, device="cuda"),
+                t.empty((300, 900), dtype=t.float16, device="cuda"),
+                t.empty(640, dtype=t.float16, device="cuda")]
+    eager, graphed = bufs(), bufs()
+    run(eager)
+    t.cuda.synchronize()
+    g = t.cuda.CUDAGraph()
+    with t.cuda.graph(g):
+        run(graphed)
+    for _ in range(3):
+        g.replay()
+    assert sb.bonsai_check_async() == 0
+    for a, b in zip(eager, graphed):
+        assert t.equal(a.view(t.int16), b.view(t.int16))
