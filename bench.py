@@ -55,52 +55,81 @@ def peaks():
 
 
 class ClockSampler:
-    """NVML samples of SM clock and throttle reasons during a timed region."""
+    """SM clock and throttle reasons sampled during a timed region, from NVML
+    when pynvml is importable, else from `nvidia-smi -lms` polling."""
     REASONS = {0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
-        self.samples, self.reasons, self.stop_flag = [], 0, False
+        self.index, self.samples, self.reasons, self.stop_flag = index, [], set(), False
+        self.max_mhz, self.nv, self.proc = None, None, None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # noqa: BLE001
-            self.nv, self.max_mhz, self.err = None, None, str(e)
-
-    def _one(self):
-        try:
-            self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-            self.reasons |= self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
         except Exception:  # noqa: BLE001
-            pass
+            self.nv = None
 
-    def _run(self):
+    def _nvml_loop(self):
         while not self.stop_flag:
-            self._one()
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.reasons.update(v for k, v in self.REASONS.items() if r & k)
+            except Exception:  # noqa: BLE001
+                pass
             time.sleep(0.005)
 
     def __enter__(self):
         if self.nv:
-            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t = threading.Thread(target=self._nvml_loop, daemon=True)
             self.t.start()
+        else:
+            import subprocess
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.SMI_FIELDS,
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                time.sleep(0.2)  # let the first sample land before the timed region
+            except Exception:  # noqa: BLE001
+                self.proc = None
         return self
 
     def __exit__(self, *a):
         if self.nv:
             self.stop_flag = True
             self.t.join()
+        elif self.proc:
+            time.sleep(0.05)
+            self.proc.terminate()
+            out, _ = self.proc.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, val in zip(names, f[2:6]):
+                    if val.lower() == "active":
+                        self.reasons.add(name)
 
     def report(self):
-        if not self.nv or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
-                    "reasons": ["nvml unavailable: %s" % getattr(self, "err", "no samples")]}
-        names = [v for k, v in self.REASONS.items() if self.reasons & k]
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no clock samples"]}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "samples": len(self.samples), "reasons": names}
+                "samples": len(self.samples), "reasons": sorted(self.reasons),
+                "source": "nvml" if self.nv else "nvidia-smi -lms 20 (covers the timed region)"}
 
 
 def dist_setup():
@@ -485,6 +514,7 @@ WORKLOADS = {
     "ter_gemv": lambda: GemvWorkload(2, 17408, 5120, 2,
                                      "ternary GEMV M=1 K=5120 N=17408 (decode)"),
     "bin_gemv_1k": lambda: GemvWorkload(1, 1024, 1024, 1, "binary GEMV M=1 K=1024 N=1024 (decode)"),
+    "bin_gemv": lambda: GemvWorkload(1, 17408, 5120, 2, "binary GEMV M=1 K=5120 N=17408 (decode)"),
     "sweep_bin": lambda: SweepWorkload(1, "64-layer decode sweep, binary, batch 1"),
     "sweep_ter": lambda: SweepWorkload(2, "64-layer decode sweep, ternary, batch 1"),
     "gemm512_bin": lambda: GemmWorkload(1, 512, "prefill GEMM M=512 K=5120 N=17408, binary"),
@@ -493,7 +523,7 @@ WORKLOADS = {
     "gemm4096_ter": lambda: GemmWorkload(2, 4096, "DiT GEMM M=4096 K=5120 N=17408, ternary"),
     "xnor": lambda: XnorWorkload("XNOR-popcount GEMM M=512 K=4096 N=4096"),
 }
-SECONDARY = [("bin_gemv_1k", 20000, 50), ("sweep_bin", 30, 3), ("sweep_ter", 30, 3),
+SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("sweep_bin", 30, 3), ("sweep_ter", 30, 3),
              ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
              ("gemm4096_ter", 5, 2), ("xnor", 20, 3)]
 
@@ -518,7 +548,8 @@ def run_ours(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded counter-based generator; random weights, no checkpoint)",
         "config": dict(wl.config(), parallelism="replicas only, %d GPU(s)" % world),
-        "roofline": wl.roofline(r, pk) if wl.kind != "xnor" else wl.roofline(r, pk, None),
+        "roofline": wl.roofline(r, pk) if wl.kind != "xnor" else
+        wl.roofline(r, pk, clk.report().get("sm_mhz")),
         "gpu_launches": r["launches"],
         "clocks": clk.report(),
     }
@@ -549,7 +580,9 @@ def run_ours(args, world, rank):
             v2, u2 = w2.value(r2["ms"], r2["steps"])
             sec.append({"workload": w2.name, "value": round(v2, 3), "unit": u2,
                         "steps": r2["steps"], "ms_per_step": round(r2["ms"] / r2["steps"], 6),
-                        "roofline": w2.roofline(r2, pk), "gpu_launches": r2["launches"],
+                        "roofline": w2.roofline(r2, pk) if w2.kind != "xnor" else
+                        w2.roofline(r2, pk, c2.report().get("sm_mhz")),
+                        "gpu_launches": r2["launches"],
                         "clocks": c2.report()})
             sb.check()
             del w2
