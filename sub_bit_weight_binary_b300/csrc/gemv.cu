@@ -72,13 +72,18 @@ struct Params {
   int ncolp;       // binary: B columns per pass (4 for one token, 8 for two)
   int xt_stride;   // ternary: bytes per token column of the x table
   int prefetch;    // may read weights before the previous grid completes
+  int sc_tma;      // group scales travel with the weights (k % 1024 == 0)
+  int sc_chunk;    // groups per chunk (64 binary, 40 ternary)
+  int sc_pitch;    // smem bytes per row of staged scales
+  int stage_bytes; // weights (16 rows x pitch) + scales (16 rows x sc_pitch)
   int off_bar, off_red, off_p2e, off_lut, off_xt, off_stage;
 };
 
 // ---------------------------------------------------------------------------
-// producer: tiles of `rows` rows x chunks of <= kChunk bytes into the ring
+// producer warp: tiles of `rows` rows x chunks of <= kChunk bytes into the
+// ring; lane r copies row r's weights, lane 16+r row r's group scales.
 __device__ __forceinline__ void produce(const Params& p, uint32_t sbase, uint32_t bar_full,
-                                        uint32_t bar_empty) {
+                                        uint32_t bar_empty, int lane) {
   if (!p.prefetch) pdl_wait();
   const uint64_t pol = policy_evict_first();
   int s = 0;
@@ -86,18 +91,25 @@ __device__ __forceinline__ void produce(const Params& p, uint32_t sbase, uint32_
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
     const int row0 = tile * p.rows;
     const int rows = min(p.rows, p.n - row0);
-    const uint8_t* src = p.w + (long long)row0 * p.row_bytes;
     for (int c = 0; c < p.chunks; ++c) {
-      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
-        set_status(BONSAI_ERR_TIMEOUT);
-        return;
-      }
       const int off = c * kChunk;
       const int len = min(kChunk, p.data_bytes - off);
-      mbar_arrive_expect_tx(bar_full + 8 * s, uint32_t(rows * len));
-      const uint32_t dst = sbase + p.off_stage + s * 16 * p.pitch;
-      for (int r = 0; r < rows; ++r)
-        bulk_g2s(dst + r * p.pitch, src + r * p.row_bytes + off, len, bar_full + 8 * s, pol);
+      const int g0 = c * p.sc_chunk;
+      const int scb = p.sc_tma ? 2 * (min(g0 + p.sc_chunk, p.G) - g0) : 0;
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(bar_empty + 8 * s, ph ^ 1);
+        if (ok) mbar_arrive_expect_tx(bar_full + 8 * s, uint32_t(rows * (len + scb)));
+        else set_status(BONSAI_ERR_TIMEOUT);
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return;
+      const uint32_t dst = sbase + p.off_stage + s * p.stage_bytes;
+      if (lane < rows)
+        bulk_g2s(dst + lane * p.pitch, p.w + (long long)(row0 + lane) * p.row_bytes + off, len,
+                 bar_full + 8 * s, pol);
+      if (scb && lane >= 16 && lane - 16 < rows)
+        bulk_g2s(dst + 16 * p.pitch + (lane - 16) * p.sc_pitch,
+                 p.scales + (size_t)(row0 + lane - 16) * p.G + g0, scb, bar_full + 8 * s, pol);
       if (++s == kStages) { s = 0; ph ^= 1; }
     }
   }
@@ -158,35 +170,50 @@ __device__ void build_binary_tables(const Params& p, uint8_t* smem, int npass) {
   for (int i = tid; i < xt_bytes / 16; i += kWarps * 32)
     reinterpret_cast<uint4*>(xt)[i] = make_uint4(0, 0, 0, 0);
   named_bar_sync(1, kWarps * 32);
-  // one warp per (token, group); lane l holds codes 4l..4l+3 of the group
-  for (int item = warp; item < p.m * p.G; item += kWarps) {
-    const int tok = item / p.G, gi = item - tok * p.G;
-    const uint2 raw =
-        *reinterpret_cast<const uint2*>(p.x + (size_t)tok * p.k + 128 * gi + 4 * lane);
-    const __half2 h01 = *reinterpret_cast<const __half2*>(&raw.x);
-    const __half2 h23 = *reinterpret_cast<const __half2*>(&raw.y);
-    const float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23),
-                        __high2float(h23)};
-    const float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    const unsigned amax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(am));
-    // power-of-two scale putting the group maximum in [2^14, 2^15) (e5m2 max 57344)
-    const int E = amax ? int((amax >> 23) & 0xFF) - 127 : 0;
-    const int e = 14 - E;
-    const float up = __uint_as_float(uint32_t(127 + e) << 23);
-    if (lane == 0) p2e[tok * p.G + gi] = __uint_as_float(uint32_t(127 - e) << 23);
-    const int pass = tok >> 1, colbase = 4 * (tok & 1);
+  // one warp per (token, group); lane l holds codes 4l..4l+3 of the group.
+  // The x loads of up to 8 items are issued together, then processed.
+  const int items = p.m * p.G;
+  for (int base = warp; base < items; base += 8 * kWarps) {
+    uint2 raw[8];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int kg = 4 * lane + t;  // code within the group
-      const int q = kg >> 5, c = kg & 7, j = (kg >> 3) & 3;
-      float r = v[t] * up;          // exact: a power-of-two scale
-      uint8_t* dst = xt + (((size_t)pass * p.G + gi) * 2 + (c >> 2)) * (p.ncolp * 64) +
-                     q * 16 + (c & 3) * 4 + j;
+    for (int i = 0; i < 8; ++i) {
+      const int item = base + i * kWarps;
+      raw[i] = make_uint2(0, 0);
+      if (item < items) {
+        const int tok = item / p.G, gi = item - tok * p.G;
+        raw[i] = *reinterpret_cast<const uint2*>(p.x + (size_t)tok * p.k + 128 * gi + 4 * lane);
+      }
+    }
 #pragma unroll
-      for (int pc = 0; pc < 4; ++pc) {  // four e5m2 pieces
-        const uint32_t b = f32_to_e5m2(r);
-        r -= e5m2_to_f32(b);            // exact residual
-        dst[(colbase + pc) * 64] = uint8_t(b);
+    for (int i = 0; i < 8; ++i) {
+      const int item = base + i * kWarps;
+      if (item >= items) break;
+      const int tok = item / p.G, gi = item - tok * p.G;
+      const __half2 h01 = *reinterpret_cast<const __half2*>(&raw[i].x);
+      const __half2 h23 = *reinterpret_cast<const __half2*>(&raw[i].y);
+      const float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23),
+                          __high2float(h23)};
+      const float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      const unsigned amax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(am));
+      // power-of-two scale putting the group maximum in [2^14, 2^15) (e5m2 max 57344)
+      const int E = amax ? int((amax >> 23) & 0xFF) - 127 : 0;
+      const int e = 14 - E;
+      const float up = __uint_as_float(uint32_t(127 + e) << 23);
+      if (lane == 0) p2e[tok * p.G + gi] = __uint_as_float(uint32_t(127 - e) << 23);
+      const int pass = tok >> 1, colbase = 4 * (tok & 1);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int kg = 4 * lane + t;  // code within the group
+        const int q = kg >> 5, c = kg & 7, j = (kg >> 3) & 3;
+        float r = v[t] * up;          // exact: a power-of-two scale
+        uint8_t* dst = xt + (((size_t)pass * p.G + gi) * 2 + (c >> 2)) * (p.ncolp * 64) +
+                       q * 16 + (c & 3) * 4 + j;
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {  // four e5m2 pieces
+          const uint32_t b = f32_to_e5m2(r);
+          r -= e5m2_to_f32(b);            // exact residual
+          dst[(colbase + pc) * 64] = uint8_t(b);
+        }
       }
     }
   }
@@ -202,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_binary_kernel(const __grid_c
   __syncthreads();
   pdl_launch_dependents();
   if (warp == kWarps) {
-    if (lane == 0) produce(p, sbase, bar_full, bar_empty);
+    produce(p, sbase, bar_full, bar_empty, lane);
     return;
   }
   pdl_wait();  // x is written by earlier work on the stream; y may be read by it
@@ -233,20 +260,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_binary_kernel(const __grid_c
       const int gb = (warp * cg) >> 3, ge = ((warp + 1) * cg) >> 3;
       const int gbase = c * (kChunk / 16);
       float s0[8], s1[8];
+      if (!p.sc_tma) {  // scales not staged: global loads issued before the wait
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int gi = min(gbase + gb + j, p.G - 1);
-        s0[j] = __half2float(sc0p[gi]);
-        s1[j] = __half2float(sc1p[gi]);
+        for (int j = 0; j < 8; ++j) {
+          const int gi = min(gbase + gb + j, p.G - 1);
+          s0[j] = __half2float(sc0p[gi]);
+          s1[j] = __half2float(sc1p[gi]);
+        }
       }
-      const uint32_t* stg =
-          reinterpret_cast<const uint32_t*>(smem + p.off_stage + s * 16 * p.pitch);
+      const uint8_t* stage = smem + p.off_stage + s * p.stage_bytes;
+      const uint32_t* stg = reinterpret_cast<const uint32_t*>(stage);
+      const __half* scs = reinterpret_cast<const __half*>(stage + 16 * p.pitch);
+      const int scp = p.sc_pitch >> 1;
       if (alive && !mbar_wait(bar_full + 8 * s, ph)) { set_status(BONSAI_ERR_TIMEOUT); alive = false; }
       if (alive) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (gb + j < ge) {
             const int gl = gb + j, gi = gbase + gl;
+            if (p.sc_tma) {
+              s0[j] = __half2float(scs[g * scp + gl]);
+              s1[j] = __half2float(scs[(g + 8) * scp + gl]);
+            }
             const uint32_t w0 = stg[g * pw + gl * 4 + q];
             const uint32_t w1 = stg[(g + 8) * pw + gl * 4 + q];
             const uint32_t a00 = bin_cls<0>(w0), a01 = bin_cls<1>(w0), a02 = bin_cls<2>(w0),
@@ -326,19 +361,24 @@ __constant__ int c_var_group[kTerVariants] = {0, 0, 1, 1, 1, 2, 2, 3, 3, 3, 4, 4
 
 __device__ void build_ternary_tables(const Params& p, uint8_t* smem) {
   const int tid = threadIdx.x, nthr = kWarps * 32;
-  {  // byte -> digits, one copy per lane (entry e at e*256 + lane*4)
-    const int e = tid;  // 256 consumer threads, one entry each
-    uint32_t v = 0;
-    if (e < 243) {
-      int r = e;
+  // 1. x -> shared memory (the byte table's region, free until step 3)
+  __half* xs_all = reinterpret_cast<__half*>(smem + p.off_lut);
+  {
+    const int n16 = p.m * p.k / 8;  // 16-byte pieces
+    const uint4* src = reinterpret_cast<const uint4*>(p.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs_all);
+    for (int base = tid; base < n16; base += 8 * nthr) {
+      uint4 v[8];
 #pragma unroll
-      for (int i = 0; i < 5; ++i) { v |= uint32_t(r % 3) << (2 * i); r /= 3; }
+      for (int i = 0; i < 8; ++i)
+        if (base + i * nthr < n16) v[i] = src[base + i * nthr];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (base + i * nthr < n16) dst[base + i * nthr] = v[i];
     }
-    uint4* dst = reinterpret_cast<uint4*>(smem + p.off_lut + e * 256);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v, v, v, v);
   }
-  // x table: (token, super-group, variant, lane q) -> 10 words (b0,b1 per digit)
+  named_bar_sync(1, nthr);
+  // 2. x table: (token, super-group, variant, lane q) -> 10 words (b0,b1 per digit)
   const int items = p.m * p.n_sg * kTerVariants * 4;
   for (int t = tid; t < items; t += nthr) {
     int r = t;
@@ -349,7 +389,7 @@ __device__ void build_ternary_tables(const Params& p, uint8_t* smem) {
     const int sg = r % p.n_sg;
     const int col = r / p.n_sg;
     const int rnd = c_var_round[v], grp = c_var_group[v];
-    const __half* xs = p.x + (size_t)col * p.k;
+    const __half* xs = xs_all + (size_t)col * p.k;
     uint32_t e[12];
 #pragma unroll
     for (int md = 0; md < 5; ++md) {
@@ -369,6 +409,19 @@ __device__ void build_ternary_tables(const Params& p, uint8_t* smem) {
     dst[0] = make_uint4(e[0], e[1], e[2], e[3]);
     dst[1] = make_uint4(e[4], e[5], e[6], e[7]);
     dst[2] = make_uint4(e[8], e[9], e[10], e[11]);
+  }
+  named_bar_sync(1, nthr);
+  {  // 3. byte -> digits, one copy per lane (entry e at e*256 + lane*4)
+    const int e = tid;  // 256 consumer threads, one entry each
+    uint32_t v = 0;
+    if (e < 243) {
+      int r = e;
+#pragma unroll
+      for (int i = 0; i < 5; ++i) { v |= uint32_t(r % 3) << (2 * i); r /= 3; }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(smem + p.off_lut + e * 256);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v, v, v, v);
   }
 }
 
@@ -390,13 +443,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ternary_kernel(const __grid_
   // row 15 of every stage holds all-zero codes and is never overwritten
   for (int i = threadIdx.x; i < kStages * (p.pitch / 4); i += kThreads) {
     const int s = i / (p.pitch / 4), wd = i - s * (p.pitch / 4);
-    reinterpret_cast<uint32_t*>(smem + p.off_stage + s * 16 * p.pitch + 15 * p.pitch)[wd] =
+    reinterpret_cast<uint32_t*>(smem + p.off_stage + s * p.stage_bytes + 15 * p.pitch)[wd] =
         kZeroTrits * 0x01010101u;
+  }
+  for (int i = threadIdx.x; i < kStages * (p.sc_pitch / 4); i += kThreads) {
+    const int s = i / (p.sc_pitch / 4), wd = i - s * (p.sc_pitch / 4);
+    reinterpret_cast<uint32_t*>(smem + p.off_stage + s * p.stage_bytes + 16 * p.pitch +
+                                15 * p.sc_pitch)[wd] = 0u;
   }
   __syncthreads();
   pdl_launch_dependents();
   if (warp == kWarps) {
-    if (lane == 0) produce(p, sbase, bar_full, bar_empty);
+    produce(p, sbase, bar_full, bar_empty, lane);
     return;
   }
   pdl_wait();
@@ -424,15 +482,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ternary_kernel(const __grid_
       const int nsg = (len + 127) >> 7;
       const int sg = c * (kChunk / 128) + warp;
       float s0[5], s1[5];
+      if (!p.sc_tma) {  // scales not staged: global loads issued before the wait
 #pragma unroll
-      for (int j = 0; j < 5; ++j) {
-        const int gi = min(5 * sg + j, p.G - 1);
-        s0[j] = __half2float(sc0p[gi]);
-        s1[j] = __half2float(sc1p[gi]);
+        for (int j = 0; j < 5; ++j) {
+          const int gi = min(5 * sg + j, p.G - 1);
+          s0[j] = __half2float(sc0p[gi]);
+          s1[j] = __half2float(sc1p[gi]);
+        }
       }
-      const uint32_t* stg =
-          reinterpret_cast<const uint32_t*>(smem + p.off_stage + s * 16 * p.pitch);
+      const uint8_t* stage = smem + p.off_stage + s * p.stage_bytes;
+      const uint32_t* stg = reinterpret_cast<const uint32_t*>(stage);
       if (alive && !mbar_wait(bar_full + 8 * s, ph)) { set_status(BONSAI_ERR_TIMEOUT); alive = false; }
+      if (p.sc_tma && alive && warp < nsg) {
+        const __half* scs = reinterpret_cast<const __half*>(stage + 16 * p.pitch);
+        const int scp = p.sc_pitch >> 1;
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+          const int gl = min(5 * warp + j, p.G - 1 - c * p.sc_chunk);  // staged group
+          s0[j] = __half2float(scs[g * scp + gl]);
+          s1[j] = __half2float(scs[(g + 8) * scp + gl]);
+        }
+      }
       if (alive && warp < nsg) {
         const uint32_t* r0 = stg + g * pw + warp * 32 + q;
         const uint32_t* r1 = stg + (g + 8) * pw + warp * 32 + q;
@@ -552,12 +622,21 @@ bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
     p.n_sg = (p.data_bytes + 127) / 128;
     p.xt_stride = p.n_sg * kTerVariants * 4 * kTerEntry + 64;
   }
+  if (ter && p.m * k * 2 > kLutBytes) return BONSAI_ERR_UNSUPPORTED;  // x staged in the table region
   p.chunks = (p.data_bytes + kChunk - 1) / kChunk;
+  p.sc_chunk = ter ? kChunk * 5 / 128 : kChunk / 16;  // groups per chunk: 40 / 64
+  p.sc_tma = (p.G % 8 == 0) ? 1 : 0;
+  {
+    int scp = (2 * p.sc_chunk + 15) / 16 * 16;
+    if ((scp / 4) % 8 == 0) scp += 16;  // words = 4 mod 8: 8 rows hit 8 distinct banks
+    p.sc_pitch = scp;
+  }
   const int chunk_max = p.data_bytes < kChunk ? p.data_bytes : kChunk;
   const int cw = chunk_max / 4;
   const int pw = ((cw - 4 + 31) / 32) * 32 + 4;
   p.pitch = pw * 4;
   p.tiles = (n + p.rows - 1) / p.rows;
+  p.stage_bytes = 16 * p.pitch + 16 * p.sc_pitch;
 
   auto up = [](int v, int a) { return (v + a - 1) / a * a; };
   int off = 0;
@@ -567,7 +646,7 @@ bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   p.off_lut = off;   if (ter) off = up(off + kLutBytes, 128);
   p.off_xt = off;
   off = ter ? up(off + p.m * p.xt_stride, 1024) : up(off + npass * p.G * 2 * p.ncolp * 64, 1024);
-  p.off_stage = off; off = up(off + kStages * 16 * p.pitch, 128);
+  p.off_stage = off; off = up(off + kStages * p.stage_bytes, 128);
   const int smem = off;
   if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
 
