@@ -8,6 +8,7 @@
 //     Y   = a_s[m] * sum_g s[n][g] * d_g            (FP32, FP16 out)
 // The kernel is bound by the popcount pipe: one XOR and one POPC per 32
 // codes of each (m, n) pair; everything else is amortised over a 64x64 tile.
+// A carry-save step lets 3 popcounts cover the 4 words of a group.
 #include "common.cuh"
 
 namespace bonsai {
@@ -26,6 +27,19 @@ constexpr int kBM = 64, kBN = 64;      // output tile
 constexpr int kThreads = 256;          // 16 x 16 threads, 4 x 4 outputs each
 constexpr int kCW = 32;                // words of K per smem chunk (8 groups)
 constexpr int kPitch = kCW + 4;        // padded row pitch (words)
+
+// popc(a XOR w) over one 128-code group (4 words) with 3 popcounts: a full
+// adder over words 0..2 and a half adder with word 3 give per-bit
+// sum s (weight 1) and carries c1, c2 (weight 2):
+//   popc = popc(s) + 2 * (popc(c1) + popc(c2)).
+__device__ __forceinline__ int group_popc(uint4 a, uint4 w) {
+  const uint32_t x0 = a.x ^ w.x, x1 = a.y ^ w.y, x2 = a.z ^ w.z, x3 = a.w ^ w.w;
+  const uint32_t s1 = x0 ^ x1 ^ x2;
+  const uint32_t c1 = (x0 & x1) | (x2 & (x0 ^ x1));
+  const uint32_t s = s1 ^ x3;
+  const uint32_t c2 = s1 & x3;
+  return __popc(s) + 2 * (__popc(c1) + __popc(c2));
+}
 
 __global__ void __launch_bounds__(kThreads) xnor_kernel(
     const uint32_t* __restrict__ a_bits, const __half* __restrict__ a_scale,
@@ -81,8 +95,7 @@ __global__ void __launch_bounds__(kThreads) xnor_kernel(
         const float sg = Ss[(tx + 16 * j) * (kCW / 4) + gg];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int pc = __popc(av[i].x ^ wv[j].x) + __popc(av[i].y ^ wv[j].y) +
-                         __popc(av[i].z ^ wv[j].z) + __popc(av[i].w ^ wv[j].w);
+          const int pc = group_popc(av[i], wv[j]);
           const int dg = 128 - 2 * pc;
           dacc[i][j] += dg;
           // exact int -> float for |dg| <= 128 without the conversion pipe
