@@ -49,7 +49,8 @@ namespace gemv {
 
 constexpr int kWarps = 8;                  // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;
-constexpr int kStages = 3;
+constexpr int kMaxStages = 8;
+constexpr int kStageBudget = 96 * 1024;   // bytes in flight per CTA (HBM read saturates near this)
 constexpr int kChunk = 1024;               // packed bytes per row per stage
 constexpr int kLutBytes = 256 * 256;       // ternary: 256 entries x (32 lanes x 4 B + pad)
 constexpr int kTerEntry = 48;              // ternary x-table bytes per (variant, lane)
@@ -76,12 +77,15 @@ struct Params {
   int sc_chunk;    // groups per chunk (64 binary, 40 ternary)
   int sc_pitch;    // smem bytes per row of staged scales
   int stage_bytes; // weights (16 rows x pitch) + scales (16 rows x sc_pitch)
+  int stages;      // ring depth
   int off_bar, off_red, off_p2e, off_lut, off_xt, off_stage;
 };
 
 // ---------------------------------------------------------------------------
 // producer warp: tiles of `rows` rows x chunks of <= kChunk bytes into the
-// ring; lane r copies row r's weights, lane 16+r row r's group scales.
+// ring with 16-byte asynchronous copies from all 32 lanes (weights, then the
+// chunk's group scales); each lane's completion is one arrival on the
+// stage's full barrier (count 32).
 __device__ __forceinline__ void produce(const Params& p, uint32_t sbase, uint32_t bar_full,
                                         uint32_t bar_empty, int lane) {
   if (!p.prefetch) pdl_wait();
@@ -99,26 +103,32 @@ __device__ __forceinline__ void produce(const Params& p, uint32_t sbase, uint32_
       int ok = 1;
       if (lane == 0) {
         ok = mbar_wait(bar_empty + 8 * s, ph ^ 1);
-        if (ok) mbar_arrive_expect_tx(bar_full + 8 * s, uint32_t(rows * (len + scb)));
-        else set_status(BONSAI_ERR_TIMEOUT);
+        if (!ok) set_status(BONSAI_ERR_TIMEOUT);
       }
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return;
       const uint32_t dst = sbase + p.off_stage + s * p.stage_bytes;
-      if (lane < rows)
-        bulk_g2s(dst + lane * p.pitch, p.w + (long long)(row0 + lane) * p.row_bytes + off, len,
-                 bar_full + 8 * s, pol);
-      if (scb && lane >= 16 && lane - 16 < rows)
-        bulk_g2s(dst + 16 * p.pitch + (lane - 16) * p.sc_pitch,
-                 p.scales + (size_t)(row0 + lane - 16) * p.G + g0, scb, bar_full + 8 * s, pol);
-      if (++s == kStages) { s = 0; ph ^= 1; }
+      const uint8_t* src = p.w + (long long)row0 * p.row_bytes + off;
+      for (int r = 0; r < rows; ++r)
+        for (int b = lane * 16; b < len; b += 32 * 16)
+          cp_async16(dst + r * p.pitch + b, src + (long long)r * p.row_bytes + b, pol);
+      if (scb) {
+        const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(p.scales + (size_t)row0 * p.G + g0);
+        const int pieces = scb / 16;
+        for (int i = lane; i < rows * pieces; i += 32) {
+          const int r = i / pieces, b = (i - r * pieces) * 16;
+          cp_async16(dst + 16 * p.pitch + r * p.sc_pitch + b, ssrc + (size_t)r * p.G * 2 + b, pol);
+        }
+      }
+      cp_async_arrive(bar_full + 8 * s);
+      if (++s == p.stages) { s = 0; ph ^= 1; }
     }
   }
 }
 
-__device__ __forceinline__ void init_barriers(uint32_t bar_full, uint32_t bar_empty) {
+__device__ __forceinline__ void init_barriers(uint32_t bar_full, uint32_t bar_empty, int stages) {
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(bar_full + 8 * s, 32);  // one arrival per producer lane
       mbar_init(bar_empty + 8 * s, kWarps);
     }
     fence_barrier_init();
@@ -224,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_binary_kernel(const __grid_c
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kStages;
-  init_barriers(bar_full, bar_empty);
+  const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
+  init_barriers(bar_full, bar_empty, p.stages);
   __syncthreads();
   pdl_launch_dependents();
   if (warp == kWarps) {
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_binary_kernel(const __grid_c
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-      if (++s == kStages) { s = 0; ph ^= 1; }
+      if (++s == p.stages) { s = 0; ph ^= 1; }
     }
     // reduction over warps and over the two lanes holding a token's pieces
     float* red = reinterpret_cast<float*>(smem + p.off_red) + (tcount & 1) * (kWarps * 16 * 16);
@@ -438,15 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ternary_kernel(const __grid_
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kStages;
-  init_barriers(bar_full, bar_empty);
+  const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
+  init_barriers(bar_full, bar_empty, p.stages);
   // row 15 of every stage holds all-zero codes and is never overwritten
-  for (int i = threadIdx.x; i < kStages * (p.pitch / 4); i += kThreads) {
+  for (int i = threadIdx.x; i < p.stages * (p.pitch / 4); i += kThreads) {
     const int s = i / (p.pitch / 4), wd = i - s * (p.pitch / 4);
     reinterpret_cast<uint32_t*>(smem + p.off_stage + s * p.stage_bytes + 15 * p.pitch)[wd] =
         kZeroTrits * 0x01010101u;
   }
-  for (int i = threadIdx.x; i < kStages * (p.sc_pitch / 4); i += kThreads) {
+  for (int i = threadIdx.x; i < p.stages * (p.sc_pitch / 4); i += kThreads) {
     const int s = i / (p.sc_pitch / 4), wd = i - s * (p.sc_pitch / 4);
     reinterpret_cast<uint32_t*>(smem + p.off_stage + s * p.stage_bytes + 16 * p.pitch +
                                 15 * p.sc_pitch)[wd] = 0u;
@@ -570,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ternary_kernel(const __grid_
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-      if (++s == kStages) { s = 0; ph ^= 1; }
+      if (++s == p.stages) { s = 0; ph ^= 1; }
     }
     float* red = reinterpret_cast<float*>(smem + p.off_red) + (tcount & 1) * (kWarps * 16 * 8);
     red[(warp * 16 + g) * 8 + 2 * q] = yacc[0];
@@ -640,15 +650,22 @@ bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
 
   auto up = [](int v, int a) { return (v + a - 1) / a * a; };
   int off = 0;
-  p.off_bar = off;   off = up(off + 16 * kStages, 128);
+  p.off_bar = off;   off = up(off + 16 * kMaxStages, 128);
   p.off_red = off;   off = up(off + 2 * kWarps * 16 * 16 * 4, 128);
   p.off_p2e = off;   if (!ter) off = up(off + p.m * p.G * 4, 128);
   p.off_lut = off;   if (ter) off = up(off + kLutBytes, 128);
   p.off_xt = off;
   off = ter ? up(off + p.m * p.xt_stride, 1024) : up(off + npass * p.G * 2 * p.ncolp * 64, 1024);
-  p.off_stage = off; off = up(off + kStages * p.stage_bytes, 128);
+  p.off_stage = off;
+  {
+    const int room = (device_max_smem_optin() - off) / p.stage_bytes;
+    int st = kStageBudget / p.stage_bytes;
+    st = st < 3 ? 3 : (st > kMaxStages ? kMaxStages : st);
+    p.stages = st < room ? st : room;
+  }
+  if (p.stages < 2) return BONSAI_ERR_UNSUPPORTED;
+  off = up(off + p.stages * p.stage_bytes, 128);
   const int smem = off;
-  if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
 
   const void* fn;
   if (ter) fn = (const void*)gemv_ternary_kernel;
