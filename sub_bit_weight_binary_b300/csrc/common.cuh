@@ -6,6 +6,7 @@
 // accumulator by the streaming decode kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -120,6 +121,16 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// 2-D TMA tile load into shared memory, completion as transaction bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
 // ---------------- programmatic dependent launch ----------------
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -164,5 +175,10 @@ int device_max_smem_optin();
 // (later calls with the same or a smaller size touch no CUDA API, so launches
 // can be captured into a CUDA graph after a first eager call).
 cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
+// 2-D tiled tensor map (no swizzle unless given), out-of-range elements
+// read as zero. Returns false if the driver rejects it.
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, void* base,
+                          uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
+                          uint32_t box1, CUtensorMapSwizzle swizzle);
 
 }  // namespace bonsai

@@ -19,8 +19,6 @@
 // ("工作原理"); the weights are +-1 ("1-bit 嘅數學") or -1/0/+1 (ternary).
 // Every mbarrier wait is bounded; a wait that runs out records
 // BONSAI_ERR_TIMEOUT and the kernel drains and leaves.
-#include <cuda.h>
-
 #include "common.cuh"
 
 namespace bonsai {
@@ -91,15 +89,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-
 #define TMEM_LD_32(taddr, v)                                                              \
   asm volatile(                                                                           \
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"     \
@@ -389,40 +378,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == W_TMEM) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encoder() {
-  static EncodeTiled fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      f = nullptr;
-    return reinterpret_cast<EncodeTiled>(f);
-  }();
-  return fn;
-}
-
 }  // namespace gemm
 
 bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
                           cudaStream_t stream) {
   using namespace gemm;
   if (m > 0x7FFFFFFF / 2) return BONSAI_ERR_UNSUPPORTED;
-  EncodeTiled enc = encoder();
-  if (!enc) return BONSAI_ERR_CUDA;
   CUtensorMap tm;
-  const cuuint64_t gdim[2] = {(cuuint64_t)w->k, (cuuint64_t)m};
-  const cuuint64_t gstride[1] = {(cuuint64_t)w->k * 2};
-  const cuuint32_t box[2] = {BK, BN};
-  const cuuint32_t estr[2] = {1, 1};
-  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), gdim, gstride, box,
-          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  if (!encode_tensor_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<uint16_t*>(x),
+                            (uint64_t)w->k, (uint64_t)m, (uint64_t)w->k * 2, BK, BN,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
     return BONSAI_ERR_CUDA;
 
   Params p{};

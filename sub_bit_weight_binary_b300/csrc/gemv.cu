@@ -3,36 +3,38 @@
 // verification). Memory-bandwidth bound ("第一の壁": every weight is
 // re-streamed per token): each packed byte is read from HBM once.
 //
-// Shared structure (sm_103a):
-//  * A persistent grid, one CTA per SM. A producer warp streams tiles of
-//    16 rows of packed weights into a 3-stage shared-memory ring with 1-D
-//    bulk copies (TMA engine), one copy per row and chunk of <= 1024 bytes,
-//    completion counted on an mbarrier. With BONSAI_WEIGHTS_PREFETCH the
-//    producer starts before the previous kernel on the stream has finished
-//    (programmatic dependent launch), so consecutive products keep HBM busy.
-//  * Eight consumer warps split each chunk along K, expand codes to MMA
-//    operands in registers and accumulate on the tensor core with warp-level
-//    mma.sync; the FP16 group scale (one per 128 codes, OpenBonsai page,
-//    "工作原理") multiplies each group's FP32 partial. A shared-memory
-//    reduction across the warps finishes each tile.
+// Structure (sm_103a):
+//  * A persistent grid, one CTA per SM: 16 consumer warps and one producer
+//    warp. The producer streams tiles of 16 rows (15 + a neutral row for
+//    ternary) in chunks of <= 1024 bytes per row into a shared-memory ring
+//    with 2-D TMA boxes, one box for the weights and one for the chunk's
+//    group scales. A box is as wide as the padded row pitch (pitch/4 = 4
+//    mod 32 words), so the consumers' word loads are conflict-free; the
+//    extra columns are either the next chunk's first bytes or read as zero.
+//    About 96 KB are in flight per SM.
+//  * With BONSAI_WEIGHTS_PREFETCH the producer starts before the previous
+//    kernel on the stream has finished (programmatic dependent launch).
+//  * Consumers split each chunk along K, expand codes to FP16 operands in
+//    registers and accumulate 16 rows x 16 codes per mma.sync m16n8k16
+//    (FP16 x FP16 -> FP32; the B columns carry the tokens). The FP16 group
+//    scale (one per 128 codes, OpenBonsai page, "工作原理") multiplies each
+//    group's FP32 partial; a shared-memory reduction finishes a tile.
 //
-// Binary (gemv_binary_kernel): operands are exact e4m3 +1/-1, four codes per
-// LOP3 (the sign bit of each byte is the code bit). x is split per token and
-// 128-group into four e5m2 pieces after a power-of-two scale,
-//   x * 2^e = p0 + p1 + p2 + p3  (exact for every x within 2^20 of the group
-//   maximum), and the pieces ride in the MMA's N columns, so one
-//   m16n8k32 e4m3 x e5m2 instruction applies 16 rows x 32 codes to all four
-//   pieces: y_g = s_g * 2^-e * sum over pieces.
-//
-// Ternary (gemv_ternary_kernel): a 256-entry table (byte -> five 2-bit
-// digits, one copy per lane) decodes the base-3 bytes. Each digit c in
-// {0,1,2} is placed into mantissa bits j..j+1 of an FP16 whose exponent is
-// 15-j, giving 2^-j + c*2^-10 with one LOP3 per two codes ("multiplication
-// degenerates to addition and sign flip", 三值权重 page). The constant part
-// is removed exactly by the tile's 16th row, which holds the all-zero code
-// byte 121: its MMA sum is the correction, computed by the same instruction
-// as every real row, so an all-zero group contributes exactly 0:
-//   sum_k (c_k - 1) x_k = 2^10 * (acc_row - acc_neutral).
+// Codes -> FP16 without a multiply per code: a code value c in {0,1,2}
+// (binary bit, or ternary digit = code + 1) placed into mantissa bits j..
+// of an FP16 whose exponent field is 15-j is the number 2^-j + c*2^-10, one
+// LOP3 per two codes ("multiplication degenerates to addition and sign
+// flip", 三值权重 page). The same 2^-10 step for every j gives, per group,
+//   acc = sum_k 2^-j(k) x_k + 2^-10 sum_k c_k x_k.
+//  * binary:  sum (2b-1) x = 2^11 acc - T,  T = sum (2^(11-j)+1) x, built
+//    once per CTA from x.
+//  * ternary: the tile's 16th row holds byte 121 (five zero codes); its MMA
+//    sum comes from the same instruction as every real row, so
+//    sum (c-1) x = 2^10 (acc_row - acc_neutral) and an all-zero group gives
+//    exactly 0. The correction is linear, so a group may be split across
+//    rounds and warps, each part subtracting its own neutral part.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace bonsai {
@@ -47,410 +49,450 @@ unsigned int read_clear_status_gemv() {
 
 namespace gemv {
 
-constexpr int kWarps = 8;                  // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kWarps = 16;                 // consumer warps
+constexpr int kProducer = kWarps;          // warp that issues the TMA copies
+constexpr int kReducer = kWarps + 1;       // warp that sums the warps' partials of a tile
+constexpr int kThreads = (kWarps + 2) * 32;
 constexpr int kMaxStages = 8;
-constexpr int kStageBudget = 96 * 1024;   // bytes in flight per CTA (HBM read saturates near this)
+constexpr int kStageBudget = 96 * 1024;    // bytes in flight per CTA
 constexpr int kChunk = 1024;               // packed bytes per row per stage
 constexpr int kLutBytes = 256 * 256;       // ternary: 256 entries x (32 lanes x 4 B + pad)
-constexpr int kTerEntry = 48;              // ternary x-table bytes per (variant, lane)
-constexpr int kTerVariants = 12;           // (round, group) pairs per 640-code super-group
+constexpr int kTerEntry = 48;              // ternary x-table bytes per (round, side, lane)
+constexpr int kTerMaxTokens = 4;           // two B columns (group parities) per token
 constexpr uint32_t kZeroTrits = 121;       // byte of five zero codes
 
 struct Params {
-  const uint8_t* w;
   const __half* scales;
   const __half* x;
   __half* y;
-  long long row_bytes;
   int n, k, m, G;
-  int rows;        // real rows per tile: 16 binary, 15 ternary (row 15 = neutral)
-  int data_bytes;  // packed bytes per row that are streamed
-  int chunks;      // stages per tile
-  int pitch;       // smem row pitch, bytes (pitch/4 = 4 mod 32: conflict-free words)
+  int rows;         // real rows per tile: 16 binary, 15 ternary (row 15 = neutral)
+  int data_bytes;   // packed bytes per row that are streamed
+  int chunks;       // stages per tile
+  int pitch;        // smem row pitch, bytes = TMA box width
   int tiles;
-  int n_sg;        // ternary: super-groups per row
-  int ncolp;       // binary: B columns per pass (4 for one token, 8 for two)
-  int xt_stride;   // ternary: bytes per token column of the x table
-  int prefetch;    // may read weights before the previous grid completes
-  int sc_tma;      // group scales travel with the weights (k % 1024 == 0)
-  int sc_chunk;    // groups per chunk (64 binary, 40 ternary)
-  int sc_pitch;    // smem bytes per row of staged scales
-  int stage_bytes; // weights (16 rows x pitch) + scales (16 rows x sc_pitch)
-  int stages;      // ring depth
-  int off_bar, off_red, off_p2e, off_lut, off_xt, off_stage;
+  int n_sg;         // ternary: 640-code super-groups per row
+  int xt_stride;    // bytes per token of the x table
+  int prefetch;     // may read weights before the previous grid completes
+  int sc_tma;       // group scales streamed with the weights (G % 8 == 0)
+  int sc_chunk;     // groups per chunk (64 binary, 40 ternary)
+  int sc_pitch;     // smem bytes per row of streamed scales = TMA box width
+  int stage_bytes;  // 16 rows x pitch + 16 rows x sc_pitch, rounded to 128
+  int stages;       // ring depth
+  int off_bar, off_red, off_t, off_lut, off_xt, off_stage;
 };
 
 // ---------------------------------------------------------------------------
-// producer warp: tiles of `rows` rows x chunks of <= kChunk bytes into the
-// ring with 16-byte asynchronous copies from all 32 lanes (weights, then the
-// chunk's group scales); each lane's completion is one arrival on the
-// stage's full barrier (count 32).
-__device__ __forceinline__ void produce(const Params& p, uint32_t sbase, uint32_t bar_full,
-                                        uint32_t bar_empty, int lane) {
-  if (!p.prefetch) pdl_wait();
-  const uint64_t pol = policy_evict_first();
-  int s = 0;
-  uint32_t ph = 0;
-  for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
-    const int row0 = tile * p.rows;
-    const int rows = min(p.rows, p.n - row0);
-    for (int c = 0; c < p.chunks; ++c) {
-      const int off = c * kChunk;
-      const int len = min(kChunk, p.data_bytes - off);
-      const int g0 = c * p.sc_chunk;
-      const int scb = p.sc_tma ? 2 * (min(g0 + p.sc_chunk, p.G) - g0) : 0;
-      int ok = 1;
-      if (lane == 0) {
-        ok = mbar_wait(bar_empty + 8 * s, ph ^ 1);
-        if (!ok) set_status(BONSAI_ERR_TIMEOUT);
-      }
-      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return;
-      const uint32_t dst = sbase + p.off_stage + s * p.stage_bytes;
-      const uint8_t* src = p.w + (long long)row0 * p.row_bytes + off;
-      for (int r = 0; r < rows; ++r)
-        for (int b = lane * 16; b < len; b += 32 * 16)
-          cp_async16(dst + r * p.pitch + b, src + (long long)r * p.row_bytes + b, pol);
-      if (scb) {
-        const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(p.scales + (size_t)row0 * p.G + g0);
-        const int pieces = scb / 16;
-        for (int i = lane; i < rows * pieces; i += 32) {
-          const int r = i / pieces, b = (i - r * pieces) * 16;
-          cp_async16(dst + 16 * p.pitch + r * p.sc_pitch + b, ssrc + (size_t)r * p.G * 2 + b, pol);
-        }
-      }
-      cp_async_arrive(bar_full + 8 * s);
-      if (++s == p.stages) { s = 0; ph ^= 1; }
-    }
-  }
-}
-
+// Barriers at off_bar: full[kMaxStages], empty[kMaxStages] of the weight
+// ring, then red_full[2], red_empty[2] of the two partial-sum slots.
 __device__ __forceinline__ void init_barriers(uint32_t bar_full, uint32_t bar_empty, int stages) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(bar_full + 8 * s, 32);  // one arrival per producer lane
+      mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, kWarps);
+    }
+    const uint32_t red_full = bar_full + 16 * kMaxStages;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(red_full + 8 * s, kWarps);
+      mbar_init(red_full + 16 + 8 * s, 1);
     }
     fence_barrier_init();
   }
 }
 
-// ===========================================================================
-// binary: e4m3 x e5m2 MMA
-// ===========================================================================
-
-// Codes c, c+8, c+16, c+24 of a word as e4m3 +1 (0x38) / -1 (0xB8): the
-// code bit is moved to the byte's sign bit.
-template <int C>
-__device__ __forceinline__ uint32_t bin_cls(uint32_t w) {
-  const uint32_t s = C == 7 ? w : (w << (7 - C));
-  return (s & 0x80808080u) ^ 0xB8B8B8B8u;
+// Partial sums of a tile: red[slot][warp][row][token], two slots used in
+// turn. A consumer warp waits until its slot is free, stores its partials
+// and arrives on red_full; the reducer warp sums the 16 warps' partials,
+// writes y and frees the slot. The consumer warps never wait for each other.
+__device__ __forceinline__ float* partial_slot(const Params& p, uint8_t* smem, uint32_t red_full,
+                                               int tcount, bool& alive) {
+  const int slot = tcount & 1;
+  const uint32_t ph = (tcount >> 1) & 1;
+  if (alive && !__all_sync(0xFFFFFFFFu, mbar_wait(red_full + 16 + 8 * slot, ph ^ 1))) {
+    set_status(BONSAI_ERR_TIMEOUT);
+    alive = false;
+  }
+  return reinterpret_cast<float*>(smem + p.off_red) + slot * (kWarps * 16 * 8);
 }
 
-__device__ __forceinline__ void mma_e4m3_e5m2(float (&d)[4], uint32_t a0, uint32_t a1,
-                                              uint32_t a2, uint32_t a3, uint32_t b0,
-                                              uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e5m2.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+__device__ __forceinline__ void partial_done(uint32_t red_full, int tcount, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(red_full + 8 * (tcount & 1));
 }
 
-// FP32 -> e5m2 (round to nearest even, low byte) and back.
-__device__ __forceinline__ uint32_t f32_to_e5m2(float v) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(v));
-  return r & 0xFFu;
-}
-__device__ __forceinline__ float e5m2_to_f32(uint32_t b) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(b)));
-  return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFFu)));
-}
-
-// x table: for pass P, group gi, half h (MMAs 2h, 2h+1), column col and
-// lane-quad index q, 16 bytes = 4 B-registers {b0,b1 of MMA 2h; b0,b1 of
-// MMA 2h+1}. Byte j of the register of class c holds the piece of code
-// k = 32q + c + 8j of the group. p2e[token][gi] = 2^-e.
-__device__ void build_binary_tables(const Params& p, uint8_t* smem, int npass) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint8_t* xt = smem + p.off_xt;
-  float* p2e = reinterpret_cast<float*>(smem + p.off_p2e);
-  const int xt_bytes = npass * p.G * 2 * p.ncolp * 64;
-  for (int i = tid; i < xt_bytes / 16; i += kWarps * 32)
-    reinterpret_cast<uint4*>(xt)[i] = make_uint4(0, 0, 0, 0);
-  named_bar_sync(1, kWarps * 32);
-  // one warp per (token, group); lane l holds codes 4l..4l+3 of the group.
-  // The x loads of up to 8 items are issued together, then processed.
-  const int items = p.m * p.G;
-  for (int base = warp; base < items; base += 8 * kWarps) {
-    uint2 raw[8];
+__device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int lane) {
+  pdl_wait();  // y may be read by earlier work on the stream
+  int tcount = 0;
+  for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tcount) {
+    const int slot = tcount & 1;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(red_full + 8 * slot, (tcount >> 1) & 1))) {
+      set_status(BONSAI_ERR_TIMEOUT);
+      return;
+    }
+    const float* red = reinterpret_cast<const float*>(smem + p.off_red) + slot * (kWarps * 16 * 8);
+    const int row0 = tile * p.rows;
+    for (int o = lane; o < 16 * p.m; o += 32) {
+      const int row = o & 15, col = o >> 4;
+      if (row < p.rows && row0 + row < p.n) {
+        float sum = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int item = base + i * kWarps;
-      raw[i] = make_uint2(0, 0);
-      if (item < items) {
-        const int tok = item / p.G, gi = item - tok * p.G;
-        raw[i] = *reinterpret_cast<const uint2*>(p.x + (size_t)tok * p.k + 128 * gi + 4 * lane);
+        for (int w = 0; w < kWarps; ++w) sum += red[(w * 16 + row) * 8 + col];
+        p.y[(size_t)col * p.n + row0 + row] = __float2half_rn(sum);
       }
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int item = base + i * kWarps;
-      if (item >= items) break;
-      const int tok = item / p.G, gi = item - tok * p.G;
-      const __half2 h01 = *reinterpret_cast<const __half2*>(&raw[i].x);
-      const __half2 h23 = *reinterpret_cast<const __half2*>(&raw[i].y);
-      const float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23),
-                          __high2float(h23)};
-      const float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-      const unsigned amax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(am));
-      // power-of-two scale putting the group maximum in [2^14, 2^15) (e5m2 max 57344)
-      const int E = amax ? int((amax >> 23) & 0xFF) - 127 : 0;
-      const int e = 14 - E;
-      const float up = __uint_as_float(uint32_t(127 + e) << 23);
-      if (lane == 0) p2e[tok * p.G + gi] = __uint_as_float(uint32_t(127 - e) << 23);
-      const int pass = tok >> 1, colbase = 4 * (tok & 1);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int kg = 4 * lane + t;  // code within the group
-        const int q = kg >> 5, c = kg & 7, j = (kg >> 3) & 3;
-        float r = v[t] * up;          // exact: a power-of-two scale
-        uint8_t* dst = xt + (((size_t)pass * p.G + gi) * 2 + (c >> 2)) * (p.ncolp * 64) +
-                       q * 16 + (c & 3) * 4 + j;
-#pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {  // four e5m2 pieces
-          const uint32_t b = f32_to_e5m2(r);
-          r -= e5m2_to_f32(b);            // exact residual
-          dst[(colbase + pc) * 64] = uint8_t(b);
-        }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(red_full + 16 + 8 * slot);
+  }
+}
+
+// Producer (one thread): per chunk one weight box and, if streamed, one
+// scale box, both completing on the stage's full barrier.
+__device__ __forceinline__ void produce(const CUtensorMap* tmw, const CUtensorMap* tms,
+                                        const Params& p, uint32_t sbase, uint32_t bar_full,
+                                        uint32_t bar_empty) {
+  if (!p.prefetch) pdl_wait();
+  const uint32_t tx = uint32_t(p.rows * p.pitch + (p.sc_tma ? p.rows * p.sc_pitch : 0));
+  int s = 0;
+  uint32_t ph = 0;
+  for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+    const int row0 = tile * p.rows;
+    for (int c = 0; c < p.chunks; ++c) {
+      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
+        set_status(BONSAI_ERR_TIMEOUT);
+        return;
       }
+      mbar_arrive_expect_tx(bar_full + 8 * s, tx);
+      const uint32_t dst = sbase + p.off_stage + s * p.stage_bytes;
+      tma_load_2d(dst, tmw, c * (kChunk / 8), row0, bar_full + 8 * s);
+      if (p.sc_tma) tma_load_2d(dst + 16 * p.pitch, tms, c * p.sc_chunk, row0, bar_full + 8 * s);
+      if (++s == p.stages) { s = 0; ph ^= 1; }
     }
   }
 }
 
-template <int NPASS>
-__global__ void __launch_bounds__(kThreads, 1) gemv_binary_kernel(const __grid_constant__ Params p) {
+// Consumer wait on a stage, with the same outcome in every lane of the warp.
+__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t ph, bool& alive) {
+  if (alive) {
+    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar, ph));
+    if (!ok) {
+      set_status(BONSAI_ERR_TIMEOUT);
+      alive = false;
+    }
+  }
+  return alive;
+}
+
+// Scale of (row, group gi), gl = gi's index within the chunk: the streamed
+// copy, else a global load.
+template <bool SC>
+__device__ __forceinline__ float scale_of(const Params& p, const uint8_t* stage, int row_in_tile,
+                                          int row_global, int gl, int gi) {
+  if constexpr (SC)
+    return __half2float(
+        reinterpret_cast<const __half*>(stage + 16 * p.pitch + row_in_tile * p.sc_pitch)[gl]);
+  return __half2float(p.scales[(size_t)min(row_global, p.n - 1) * p.G + min(gi, p.G - 1)]);
+}
+
+__host__ __device__ constexpr uint32_t exp_base(int j) {
+  return (uint32_t(15 - j) << 10) | (uint32_t(15 - j) << 26);
+}
+
+// Exponent fields exp_base(0..9) held in registers: (src & mask) | E is then
+// one LOP3 with the mask as its immediate.
+struct ExpRegs {
+  uint32_t e[10];
+  __device__ __forceinline__ ExpRegs() {
+#pragma unroll
+    for (int j = 0; j < 10; ++j) {
+      uint32_t v = exp_base(j);
+      asm volatile("" : "+r"(v));  // keep the value in a register
+      e[j] = v;
+    }
+  }
+};
+
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t e) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(e));
+  return d;
+}
+
+// ===========================================================================
+// binary
+// ===========================================================================
+// Bit p (0..15) of each 16-bit half is used as mantissa bit j(p): bits 0..9
+// in place, bits 10..15 from w>>6 (j = 4..9).
+__host__ __device__ constexpr int bin_j(int p) { return p <= 9 ? p : p - 6; }
+
+template <int P>
+__device__ __forceinline__ uint32_t bin_operand(uint32_t w, uint32_t wr, const ExpRegs& E) {
+  constexpr int j = bin_j(P);
+  return and_or<(1u << j) | (1u << (j + 16))>(P <= 9 ? w : wr, E.e[j]);
+}
+
+// x table (binary): token t, group gi, pair c2 (MMAs 2c2, 2c2+1), lane quad
+// index q -> 16 bytes {b0,b1 of MMA 2c2; b0,b1 of MMA 2c2+1} at
+// t*stride + gi*256 + c2*64 + q*16. MMA i takes the codes of class i
+// (bits i, i+16 of word q of the group) and class i+8 (bits i+8, i+24).
+// T[gi][t] = sum over the group of (2^(11-j)+1) x. One thread per word of
+// x; the four words of a group sit in four neighbouring lanes.
+__device__ void build_binary_tables(const Params& p, uint8_t* smem) {
+  const int lane = threadIdx.x & 31, nthr = kWarps * 32;
+  float* T = reinterpret_cast<float*>(smem + p.off_t);
+  const int words = p.k / 32, total = p.m * words;
+  for (int base = threadIdx.x - lane; base < total; base += nthr) {
+    const int t = base + lane;
+    const bool valid = t < total;
+    const int col = valid ? t / words : 0, wd = valid ? t - col * words : 0;
+    uint4 v[4] = {};
+    if (valid) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)col * p.k + 32 * wd);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = src[i];
+    }
+    uint32_t u[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      u[4 * i] = v[i].x;
+      u[4 * i + 1] = v[i].y;
+      u[4 * i + 2] = v[i].z;
+      u[4 * i + 3] = v[i].w;
+    }
+    // x of code i of the word: half (i & 1) of u[i >> 1]
+    auto xh = [&](int i) -> uint32_t { return (u[i >> 1] >> (16 * (i & 1))) & 0xFFFFu; };
+    uint32_t e[16];
+    float tsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      e[2 * i] = xh(i) | (xh(i + 16) << 16);
+      e[2 * i + 1] = xh(i + 8) | (xh(i + 24) << 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      tsum = fmaf(float((1 << (11 - bin_j(i & 15))) + 1), __half2float(__ushort_as_half(xh(i))),
+                  tsum);
+    tsum += __shfl_xor_sync(0xFFFFFFFFu, tsum, 1);
+    tsum += __shfl_xor_sync(0xFFFFFFFFu, tsum, 2);
+    if (valid) {
+      uint4* dst = reinterpret_cast<uint4*>(smem + p.off_xt + col * p.xt_stride + (wd >> 2) * 256 +
+                                            (wd & 3) * 16);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        dst[c * 4] = make_uint4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
+      if ((wd & 3) == 0) T[(wd >> 2) * 8 + col] = tsum;
+    }
+  }
+}
+
+template <bool SC>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_binary_kernel(const __grid_constant__ CUtensorMap tmw,
+                       const __grid_constant__ CUtensorMap tms, const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t red_full = bar_full + 16 * kMaxStages;
   init_barriers(bar_full, bar_empty, p.stages);
   __syncthreads();
   pdl_launch_dependents();
-  if (warp == kWarps) {
-    produce(p, sbase, bar_full, bar_empty, lane);
+  if (warp == kProducer) {
+    if (lane == 0) produce(&tmw, &tms, p, sbase, bar_full, bar_empty);
     return;
   }
-  pdl_wait();  // x is written by earlier work on the stream; y may be read by it
-  build_binary_tables(p, smem, NPASS);
+  if (warp == kReducer) {
+    reducer(p, smem, red_full, lane);
+    return;
+  }
+  pdl_wait();  // x is written by earlier work on the stream
+  build_binary_tables(p, smem);
   named_bar_sync(1, kWarps * 32);
 
   const int g = lane >> 2, q = lane & 3;
-  const bool bcol = g < p.ncolp;
+  const bool bcol = g < p.m;
   const int pw = p.pitch >> 2;
-  const uint8_t* xt = smem + p.off_xt + (bcol ? g : 0) * 64 + q * 16;
-  const float* p2e = reinterpret_cast<const float*>(smem + p.off_p2e);
-  const int pass_stride = p.G * 2 * p.ncolp * 64;
+  const uint8_t* xt_col = smem + p.off_xt + (bcol ? g : 0) * p.xt_stride;
+  const float* T = reinterpret_cast<const float*>(smem + p.off_t);
+  const ExpRegs E;
+  uint4 bx = make_uint4(0, 0, 0, 0);
   int s = 0;
   uint32_t ph = 0;
   bool alive = true;
   int tcount = 0;
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tcount) {
     const int row0 = tile * 16;
-    const int rg = min(row0 + g, p.n - 1), rg8 = min(row0 + g + 8, p.n - 1);
-    const __half* sc0p = p.scales + (size_t)rg * p.G;
-    const __half* sc1p = p.scales + (size_t)rg8 * p.G;
-    float yacc[NPASS][2];
-#pragma unroll
-    for (int ps = 0; ps < NPASS; ++ps) yacc[ps][0] = yacc[ps][1] = 0.f;
+    float yacc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int c = 0; c < p.chunks; ++c) {
       const int len = min(kChunk, p.data_bytes - c * kChunk);
       const int cg = len >> 4;  // 128-code groups in this chunk
-      const int gb = (warp * cg) >> 3, ge = ((warp + 1) * cg) >> 3;
-      const int gbase = c * (kChunk / 16);
-      float s0[8], s1[8];
-      if (!p.sc_tma) {  // scales not staged: global loads issued before the wait
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int gi = min(gbase + gb + j, p.G - 1);
-          s0[j] = __half2float(sc0p[gi]);
-          s1[j] = __half2float(sc1p[gi]);
-        }
-      }
       const uint8_t* stage = smem + p.off_stage + s * p.stage_bytes;
       const uint32_t* stg = reinterpret_cast<const uint32_t*>(stage);
-      const __half* scs = reinterpret_cast<const __half*>(stage + 16 * p.pitch);
-      const int scp = p.sc_pitch >> 1;
-      if (alive && !mbar_wait(bar_full + 8 * s, ph)) { set_status(BONSAI_ERR_TIMEOUT); alive = false; }
-      if (alive) {
+      if (wait_full(bar_full + 8 * s, ph, alive)) {
+        // Groups gl = r, r + kWarps, ... of the chunk; r alternates between
+        // the two halves of the warp range from tile to tile, so a warp's
+        // share evens out over two tiles. x-table loads only in the lanes of
+        // real columns (the others keep stale values, and their columns are
+        // not stored).
+        const int r = (warp + (kWarps / 2) * (tcount & 1)) % kWarps;
+        for (int gl = r; gl < cg; gl += kWarps) {
+          const int gi = c * (kChunk / 16) + gl;
+          const uint32_t w0 = stg[g * pw + gl * 4 + q];
+          const uint32_t w1 = stg[(g + 8) * pw + gl * 4 + q];
+          const uint32_t w0r = w0 >> 6, w1r = w1 >> 6;
+          const uint4* xt = reinterpret_cast<const uint4*>(xt_col + gi * 256) + q;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#define BIN_MMA(I, BX, BY)                                                  \
+  mma_16816(acc, bin_operand<I>(w0, w0r, E), bin_operand<I>(w1, w1r, E),    \
+            bin_operand<I + 8>(w0, w0r, E), bin_operand<I + 8>(w1, w1r, E), BX, BY)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (gb + j < ge) {
-            const int gl = gb + j, gi = gbase + gl;
-            if (p.sc_tma) {
-              s0[j] = __half2float(scs[g * scp + gl]);
-              s1[j] = __half2float(scs[(g + 8) * scp + gl]);
-            }
-            const uint32_t w0 = stg[g * pw + gl * 4 + q];
-            const uint32_t w1 = stg[(g + 8) * pw + gl * 4 + q];
-            const uint32_t a00 = bin_cls<0>(w0), a01 = bin_cls<1>(w0), a02 = bin_cls<2>(w0),
-                           a03 = bin_cls<3>(w0), a04 = bin_cls<4>(w0), a05 = bin_cls<5>(w0),
-                           a06 = bin_cls<6>(w0), a07 = bin_cls<7>(w0);
-            const uint32_t a10 = bin_cls<0>(w1), a11 = bin_cls<1>(w1), a12 = bin_cls<2>(w1),
-                           a13 = bin_cls<3>(w1), a14 = bin_cls<4>(w1), a15 = bin_cls<5>(w1),
-                           a16 = bin_cls<6>(w1), a17 = bin_cls<7>(w1);
-#pragma unroll
-            for (int ps = 0; ps < NPASS; ++ps) {
-              const uint8_t* xg = xt + ps * pass_stride + gi * 2 * (p.ncolp * 64);
-              const uint4 b0 = bcol ? *reinterpret_cast<const uint4*>(xg) : make_uint4(0, 0, 0, 0);
-              const uint4 b1 = bcol ? *reinterpret_cast<const uint4*>(xg + p.ncolp * 64)
-                                    : make_uint4(0, 0, 0, 0);
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_e4m3_e5m2(acc, a00, a10, a01, a11, b0.x, b0.y);
-              mma_e4m3_e5m2(acc, a02, a12, a03, a13, b0.z, b0.w);
-              mma_e4m3_e5m2(acc, a04, a14, a05, a15, b1.x, b1.y);
-              mma_e4m3_e5m2(acc, a06, a16, a07, a17, b1.z, b1.w);
-              // columns 2q, 2q+1 are two pieces of token 2*ps + q/2
-              const int tok = min(2 * ps + (q >> 1), p.m - 1);
-              const float f = p2e[tok * p.G + gi];
-              yacc[ps][0] = fmaf(s0[j] * f, acc[0] + acc[1], yacc[ps][0]);
-              yacc[ps][1] = fmaf(s1[j] * f, acc[2] + acc[3], yacc[ps][1]);
+          for (int c2 = 0; c2 < 4; ++c2) {
+            if (bcol) bx = xt[4 * c2];
+            switch (c2) {
+              case 0: BIN_MMA(0, bx.x, bx.y); BIN_MMA(1, bx.z, bx.w); break;
+              case 1: BIN_MMA(2, bx.x, bx.y); BIN_MMA(3, bx.z, bx.w); break;
+              case 2: BIN_MMA(4, bx.x, bx.y); BIN_MMA(5, bx.z, bx.w); break;
+              default: BIN_MMA(6, bx.x, bx.y); BIN_MMA(7, bx.z, bx.w); break;
             }
           }
+#undef BIN_MMA
+          const float2 tt = *reinterpret_cast<const float2*>(T + gi * 8 + 2 * q);
+          const float s0 = scale_of<SC>(p, stage, g, row0 + g, gl, gi);
+          const float s1 = scale_of<SC>(p, stage, g + 8, row0 + g + 8, gl, gi);
+          yacc[0] = fmaf(s0, fmaf(acc[0], 2048.f, -tt.x), yacc[0]);
+          yacc[1] = fmaf(s0, fmaf(acc[1], 2048.f, -tt.y), yacc[1]);
+          yacc[2] = fmaf(s1, fmaf(acc[2], 2048.f, -tt.x), yacc[2]);
+          yacc[3] = fmaf(s1, fmaf(acc[3], 2048.f, -tt.y), yacc[3]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
       if (++s == p.stages) { s = 0; ph ^= 1; }
     }
-    // reduction over warps and over the two lanes holding a token's pieces
-    float* red = reinterpret_cast<float*>(smem + p.off_red) + (tcount & 1) * (kWarps * 16 * 16);
-#pragma unroll
-    for (int ps = 0; ps < NPASS; ++ps) {
-      red[(warp * 16 + g) * 16 + ps * 4 + q] = yacc[ps][0];
-      red[(warp * 16 + g + 8) * 16 + ps * 4 + q] = yacc[ps][1];
-    }
-    named_bar_sync(1, kWarps * 32);
-    if (threadIdx.x < 16 * p.m) {
-      const int row = threadIdx.x & 15, tok = threadIdx.x >> 4;
-      if (row0 + row < p.n) {
-        const int slot = (tok >> 1) * 4 + (tok & 1) * 2;
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w)
-          sum += red[(w * 16 + row) * 16 + slot] + red[(w * 16 + row) * 16 + slot + 1];
-        p.y[(size_t)tok * p.n + row0 + row] = __float2half_rn(sum);
-      }
-    }
+    float* red = partial_slot(p, smem, red_full, tcount, alive);
+    red[(warp * 16 + g) * 8 + 2 * q] = yacc[0];
+    red[(warp * 16 + g) * 8 + 2 * q + 1] = yacc[1];
+    red[(warp * 16 + g + 8) * 8 + 2 * q] = yacc[2];
+    red[(warp * 16 + g + 8) * 8 + 2 * q + 1] = yacc[3];
+    partial_done(red_full, tcount, lane);
   }
 }
 
 // ===========================================================================
-// ternary: FP16 MMA with the neutral 16th row
+// ternary
 // ===========================================================================
+// A 640-code super-group (128 bytes, exactly 5 groups) is processed in 8
+// rounds of 80 codes: in a round lane q of a quad takes word 4*round+q of
+// its two rows, and digit md (0..4) of the word's 4 bytes feeds MMA md.
+// Four rounds straddle a group edge (128 codes = 25.6 bytes); instead of a
+// second MMA, B carries two columns per token: column 2t+side holds token
+// t's x restricted to the groups of parity `side`, so one MMA accumulates
+// both groups of a round apart.
+// The byte table gives digit i at bits 2i..2i+1, used in place as mantissa
+// bits j = 2i, 2i+1.
 __host__ __device__ constexpr uint32_t mant_mask2(int j) { return (3u << j) | (3u << (j + 16)); }
-__host__ __device__ constexpr uint32_t exp_base(int j) {
-  return (uint32_t(15 - j) << 10) | (uint32_t(15 - j) << 26);
-}
-// The table gives digit i at bits 2i..2i+1; digits 0,1 are used from F<<4
-// (mantissa bits j = 4, 6), digits 2,3,4 in place (j = 4, 6, 8): j >= 4
-// keeps the constant 2^-j within 2^6 of the step 2^-10.
-__host__ __device__ constexpr int ter_j(int md) { return md <= 1 ? 2 * md + 4 : 2 * md; }
 
 template <int MD>
-__device__ __forceinline__ uint32_t ter_operand(uint32_t f, uint32_t fl) {
-  constexpr int j = ter_j(MD);
-  return ((MD <= 1 ? fl : f) & mant_mask2(j)) | exp_base(j);
+__device__ __forceinline__ uint32_t ter_operand(uint32_t f, const ExpRegs& E) {
+  return and_or<mant_mask2(2 * MD)>(f, E.e[2 * MD]);
 }
 
-// variant v of a super-group: round (4 words = 80 codes) and the group
-// (0..4) whose codes it keeps
-__constant__ int c_var_round[kTerVariants] = {0, 1, 1, 2, 3, 3, 4, 4, 5, 6, 6, 7};
-__constant__ int c_var_group[kTerVariants] = {0, 0, 1, 1, 1, 2, 2, 3, 3, 3, 4, 4};
+// group (0..4) of the super-group that the first / last code of round r falls in
+__host__ __device__ constexpr int round_first_group(int r) { return (80 * r) >> 7; }
+__host__ __device__ constexpr int round_last_group(int r) { return (80 * r + 79) >> 7; }
 
-__device__ void build_ternary_tables(const Params& p, uint8_t* smem) {
-  const int tid = threadIdx.x, nthr = kWarps * 32;
-  // 1. x -> shared memory (the byte table's region, free until step 3)
-  __half* xs_all = reinterpret_cast<__half*>(smem + p.off_lut);
-  {
-    const int n16 = p.m * p.k / 8;  // 16-byte pieces
-    const uint4* src = reinterpret_cast<const uint4*>(p.x);
-    uint4* dst = reinterpret_cast<uint4*>(xs_all);
-    for (int base = tid; base < n16; base += 8 * nthr) {
-      uint4 v[8];
+// the super-group's 8 rounds are split over kTerParts warps
+constexpr int kTerParts = kWarps / 8;
+static_assert(kTerParts == 2 || kTerParts == 4, "8 rounds over 2 or 4 warps");
+
+struct TerDigits {
+  uint32_t a01, a23, b01, b23;  // rows g (a) and g+8 (b), bytes (0,1) and (2,3)
+};
+
+// Rounds [R0, R0+N) of a super-group: all lookups first (their shared-memory
+// latencies overlap), then the MMAs; a group is flushed after its last round
+// in the range.
+template <int R0, int N, typename Fetch, typename Round, typename Epi>
+__device__ __forceinline__ void ter_range(Fetch& fetch, Round& round, Epi& epi) {
+  TerDigits f[N];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (base + i * nthr < n16) v[i] = src[base + i * nthr];
+  for (int i = 0; i < N; ++i) fetch(R0 + i, f[i]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (base + i * nthr < n16) dst[base + i * nthr] = v[i];
-    }
+  for (int i = 0; i < N; ++i) {
+    round(R0 + i, f[i]);
+    if (round_last_group(R0 + i) != round_first_group(R0 + i)) epi(round_first_group(R0 + i));
   }
-  named_bar_sync(1, nthr);
-  // 2. x table: (token, super-group, variant, lane q) -> 10 words (b0,b1 per digit)
-  const int items = p.m * p.n_sg * kTerVariants * 4;
-  for (int t = tid; t < items; t += nthr) {
-    int r = t;
-    const int q = r & 3;
-    r >>= 2;
-    const int v = r % kTerVariants;
-    r /= kTerVariants;
-    const int sg = r % p.n_sg;
-    const int col = r / p.n_sg;
-    const int rnd = c_var_round[v], grp = c_var_group[v];
-    const __half* xs = xs_all + (size_t)col * p.k;
-    uint32_t e[12];
-#pragma unroll
-    for (int md = 0; md < 5; ++md) {
-      __half h[4];
-#pragma unroll
-      for (int bj = 0; bj < 4; ++bj) {
-        const int kr = 5 * (4 * (4 * rnd + q) + bj) + md;  // code index in the super-group
-        const int kg = 640 * sg + kr;
-        h[bj] = (kg < p.k && (kr >> 7) == grp) ? xs[kg] : __ushort_as_half(0);
-      }
-      e[2 * md] = pack_half2(h[0], h[1]);
-      e[2 * md + 1] = pack_half2(h[2], h[3]);
-    }
-    e[10] = e[11] = 0;
-    uint4* dst = reinterpret_cast<uint4*>(smem + p.off_xt + col * p.xt_stride +
-                                          ((sg * kTerVariants + v) * 4 + q) * kTerEntry);
-    dst[0] = make_uint4(e[0], e[1], e[2], e[3]);
-    dst[1] = make_uint4(e[4], e[5], e[6], e[7]);
-    dst[2] = make_uint4(e[8], e[9], e[10], e[11]);
-  }
-  named_bar_sync(1, nthr);
-  {  // 3. byte -> digits, one copy per lane (entry e at e*256 + lane*4)
-    const int e = tid;  // 256 consumer threads, one entry each
+  epi(round_last_group(R0 + N - 1));
+}
+
+// Byte -> digits table, one copy per lane (entry e at e*256 + lane*4):
+// digit i at bits 2i..2i+1. Independent of x, so it is built before the
+// wait for the previous grid.
+__device__ void build_byte_table(uint8_t* smem) {
+  for (int e = threadIdx.x; e < 256; e += kWarps * 32) {
     uint32_t v = 0;
     if (e < 243) {
       int r = e;
 #pragma unroll
       for (int i = 0; i < 5; ++i) { v |= uint32_t(r % 3) << (2 * i); r /= 3; }
     }
-    uint4* dst = reinterpret_cast<uint4*>(smem + p.off_lut + e * 256);
+    uint4* dst = reinterpret_cast<uint4*>(smem + e * 256);
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v, v, v, v);
   }
 }
 
-template <int MD>
-__device__ __forceinline__ void ter_fill(uint32_t (&A)[5][4], uint32_t fa01, uint32_t fb01,
-                                         uint32_t fa23, uint32_t fb23) {
-  A[MD][0] = ter_operand<MD>(fa01, fa01 << 4);
-  A[MD][1] = ter_operand<MD>(fb01, fb01 << 4);
-  A[MD][2] = ter_operand<MD>(fa23, fa23 << 4);
-  A[MD][3] = ter_operand<MD>(fb23, fb23 << 4);
+// x table: item (token, super-group, round, side, lane q) -> 10 words, the B
+// pair (b0, b1) of each digit MMA, at token*stride + (item within the
+// token)*48. An item covers the 20 consecutive codes 640 sg + 80 rnd + 20 q
+// (bytes 4 (4 rnd + q) + 0..3), read from global memory as 5 x 8 bytes.
+__device__ void build_ternary_xtable(const Params& p, uint8_t* smem) {
+  const int per_token = p.n_sg * 64;
+  for (int t = threadIdx.x; t < p.m * per_token; t += kWarps * 32) {
+    const int col = t / per_token, it = t - col * per_token;
+    const int q = it & 3, side = (it >> 2) & 1, rnd = (it >> 3) & 7, sg = it >> 6;
+    const int k0 = 640 * sg + 80 * rnd + 20 * q;
+    uint32_t u[10];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      uint2 v = make_uint2(0, 0);
+      if (k0 + 4 * i < p.k)  // k % 128 == 0: a 4-code piece is all in or all out
+        v = *reinterpret_cast<const uint2*>(p.x + (size_t)col * p.k + k0 + 4 * i);
+      u[2 * i] = v.x;
+      u[2 * i + 1] = v.y;
+    }
+    // code c of the item (0..19): half (c & 1) of u[c >> 1]; it is kept if
+    // its group within the super-group has parity `side`
+    auto xh = [&](int c) -> uint32_t {
+      const int kr = 80 * rnd + 20 * q + c;
+      return (((kr >> 7) & 1) == side) ? (u[c >> 1] >> (16 * (c & 1))) & 0xFFFFu : 0u;
+    };
+    uint32_t e[12];
+#pragma unroll
+    for (int md = 0; md < 5; ++md) {
+      e[2 * md] = xh(md) | (xh(5 + md) << 16);
+      e[2 * md + 1] = xh(10 + md) | (xh(15 + md) << 16);
+    }
+    e[10] = e[11] = 0;
+    uint4* dst = reinterpret_cast<uint4*>(smem + p.off_xt + col * p.xt_stride + it * kTerEntry);
+    dst[0] = make_uint4(e[0], e[1], e[2], e[3]);
+    dst[1] = make_uint4(e[4], e[5], e[6], e[7]);
+    dst[2] = make_uint4(e[8], e[9], e[10], e[11]);
+  }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gemv_ternary_kernel(const __grid_constant__ Params p) {
+template <bool SC>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_ternary_kernel(const __grid_constant__ CUtensorMap tmw,
+                        const __grid_constant__ CUtensorMap tms, const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t red_full = bar_full + 16 * kMaxStages;
   init_barriers(bar_full, bar_empty, p.stages);
-  // row 15 of every stage holds all-zero codes and is never overwritten
+  // Row 15 of every stage holds zero codes (and zero scales); the 15-row
+  // boxes never write it.
   for (int i = threadIdx.x; i < p.stages * (p.pitch / 4); i += kThreads) {
     const int s = i / (p.pitch / 4), wd = i - s * (p.pitch / 4);
     reinterpret_cast<uint32_t*>(smem + p.off_stage + s * p.stage_bytes + 15 * p.pitch)[wd] =
@@ -463,176 +505,154 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ternary_kernel(const __grid_
   }
   __syncthreads();
   pdl_launch_dependents();
-  if (warp == kWarps) {
-    produce(p, sbase, bar_full, bar_empty, lane);
+  if (warp == kProducer) {
+    if (lane == 0) produce(&tmw, &tms, p, sbase, bar_full, bar_empty);
     return;
   }
-  pdl_wait();
-  build_ternary_tables(p, smem);
+  if (warp == kReducer) {
+    reducer(p, smem, red_full, lane);
+    return;
+  }
+  build_byte_table(smem);
+  pdl_wait();  // x is written by earlier work on the stream
+  build_ternary_xtable(p, smem);
   named_bar_sync(1, kWarps * 32);
 
   const int g = lane >> 2, q = lane & 3;
-  const bool bcol = g < p.m;
-  const uint8_t* xt_col = smem + p.off_xt + (bcol ? g : 0) * p.xt_stride;
+  const bool bcol = (g >> 1) < p.m;  // B column g = token g>>1, side g&1
+  const uint8_t* xt_lane = smem + p.off_xt + (bcol ? (g >> 1) : 0) * p.xt_stride +
+                           ((g & 1) * 4 + q) * kTerEntry;
   const uint32_t lut_lane = uint32_t(lane * 4);
-  const uint8_t* lut = smem + p.off_lut;
+  const uint8_t* lut = smem;  // the byte table sits at offset 0
   const int pw = p.pitch >> 2;
+  const int sgw = warp / kTerParts, part = warp % kTerParts;  // super-group of the chunk, rounds
+  const ExpRegs E;
+  uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0, b2 = b0;
   int s = 0;
   uint32_t ph = 0;
   bool alive = true;
   int tcount = 0;
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tcount) {
     const int row0 = tile * 15;
-    const int rg = min(row0 + g, p.n - 1), rg8 = min(row0 + g + 8, p.n - 1);
-    const __half* sc0p = p.scales + (size_t)rg * p.G;
-    const __half* sc1p = p.scales + (size_t)rg8 * p.G;
-    float yacc[4] = {0.f, 0.f, 0.f, 0.f};
+    float yacc[2] = {0.f, 0.f};  // token q, rows g and g+8
     for (int c = 0; c < p.chunks; ++c) {
       const int len = min(kChunk, p.data_bytes - c * kChunk);
       const int nsg = (len + 127) >> 7;
-      const int sg = c * (kChunk / 128) + warp;
-      float s0[5], s1[5];
-      if (!p.sc_tma) {  // scales not staged: global loads issued before the wait
-#pragma unroll
-        for (int j = 0; j < 5; ++j) {
-          const int gi = min(5 * sg + j, p.G - 1);
-          s0[j] = __half2float(sc0p[gi]);
-          s1[j] = __half2float(sc1p[gi]);
-        }
-      }
+      const int sg = c * (kChunk / 128) + sgw;
       const uint8_t* stage = smem + p.off_stage + s * p.stage_bytes;
       const uint32_t* stg = reinterpret_cast<const uint32_t*>(stage);
-      if (alive && !mbar_wait(bar_full + 8 * s, ph)) { set_status(BONSAI_ERR_TIMEOUT); alive = false; }
-      if (p.sc_tma && alive && warp < nsg) {
-        const __half* scs = reinterpret_cast<const __half*>(stage + 16 * p.pitch);
-        const int scp = p.sc_pitch >> 1;
-#pragma unroll
-        for (int j = 0; j < 5; ++j) {
-          const int gl = min(5 * warp + j, p.G - 1 - c * p.sc_chunk);  // staged group
-          s0[j] = __half2float(scs[g * scp + gl]);
-          s1[j] = __half2float(scs[(g + 8) * scp + gl]);
-        }
-      }
-      if (alive && warp < nsg) {
-        const uint32_t* r0 = stg + g * pw + warp * 32 + q;
-        const uint32_t* r1 = stg + (g + 8) * pw + warp * 32 + q;
-        const uint8_t* xt = xt_col + (sg * kTerVariants * 4 + q) * kTerEntry;
-        float accA[4] = {0.f, 0.f, 0.f, 0.f}, accB[4] = {0.f, 0.f, 0.f, 0.f};
-        // finished group: subtract the neutral row's sum (lanes 28..31 hold row 15)
-        auto epi = [&](int grp, const float (&acc)[4]) {
-          const float t0 = __shfl_sync(0xFFFFFFFFu, acc[2], 28 + q);
-          const float t1 = __shfl_sync(0xFFFFFFFFu, acc[3], 28 + q);
-          yacc[0] = fmaf(s0[grp], (acc[0] - t0) * 1024.f, yacc[0]);
-          yacc[1] = fmaf(s0[grp], (acc[1] - t1) * 1024.f, yacc[1]);
-          yacc[2] = fmaf(s1[grp], (acc[2] - t0) * 1024.f, yacc[2]);
-          yacc[3] = fmaf(s1[grp], (acc[3] - t1) * 1024.f, yacc[3]);
+      if (wait_full(bar_full + 8 * s, ph, alive) && sgw < nsg) {
+        const uint32_t* r0 = stg + g * pw + sgw * 32 + q;
+        const uint32_t* r1 = stg + (g + 8) * pw + sgw * 32 + q;
+        const uint8_t* xt = xt_lane + sg * (64 * kTerEntry);
+        // acc: (row g, token q, side 0 / 1), (row g+8, token q, side 0 / 1)
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // the part of group grp held in this warp -> yacc; clears its side
+        auto epi = [&](int grp) {
+          const int side = grp & 1;
+          const int gl = min(5 * sgw + grp, p.G - 1 - c * p.sc_chunk);  // group within the chunk
+          const int gi = 5 * sg + grp;
+          const float sa = scale_of<SC>(p, stage, g, row0 + g, gl, gi);
+          const float sb = scale_of<SC>(p, stage, g + 8, row0 + g + 8, gl, gi);  // row 15: unused
+          const float va = side ? acc[1] : acc[0];
+          const float vb = side ? acc[3] : acc[2];
+          const float t = __shfl_sync(0xFFFFFFFFu, vb, 28 + q);  // neutral row 15
+          yacc[0] = fmaf(sa, (va - t) * 1024.f, yacc[0]);
+          yacc[1] = fmaf(sb, (vb - t) * 1024.f, yacc[1]);
+          if (side) {
+            acc[1] = 0.f;
+            acc[3] = 0.f;
+          } else {
+            acc[0] = 0.f;
+            acc[2] = 0.f;
+          }
         };
-#pragma unroll
-        for (int rnd = 0; rnd < 8; ++rnd) {
-          uint32_t A[5][4];
-          {
-            const uint32_t wa = r0[4 * rnd], wb = r1[4 * rnd];
-            auto lookup = [&](uint32_t wd, int i) -> uint32_t {
-              const uint32_t off = __byte_perm(wd, lut_lane, 0x5504 | (i << 4));
-              return *reinterpret_cast<const uint32_t*>(lut + off);
-            };
-            const uint32_t fa01 = lookup(wa, 0) + (lookup(wa, 1) << 16);
-            const uint32_t fa23 = lookup(wa, 2) + (lookup(wa, 3) << 16);
-            const uint32_t fb01 = lookup(wb, 0) + (lookup(wb, 1) << 16);
-            const uint32_t fb23 = lookup(wb, 2) + (lookup(wb, 3) << 16);
-            ter_fill<0>(A, fa01, fb01, fa23, fb23);
-            ter_fill<1>(A, fa01, fb01, fa23, fb23);
-            ter_fill<2>(A, fa01, fb01, fa23, fb23);
-            ter_fill<3>(A, fa01, fb01, fa23, fb23);
-            ter_fill<4>(A, fa01, fb01, fa23, fb23);
-          }
-          // first variant of the round; a second if it straddles a group edge
-          const int v0 = (rnd == 0) ? 0 : (rnd == 1) ? 1 : (rnd == 2) ? 3 : (rnd == 3) ? 4
-                       : (rnd == 4) ? 6 : (rnd == 5) ? 8 : (rnd == 6) ? 9 : 11;
-          const bool split = (rnd == 1 || rnd == 3 || rnd == 4 || rnd == 6);
-          const int grp0 = (rnd <= 1) ? 0 : (rnd <= 3) ? 1 : (rnd == 4) ? 2 : (rnd <= 6) ? 3 : 4;
-          auto run = [&](float (&acc)[4], int v) {
-            const uint4* bp = reinterpret_cast<const uint4*>(xt + v * 4 * kTerEntry);
-            const uint4 b0 = bcol ? bp[0] : make_uint4(0, 0, 0, 0);
-            const uint4 b1 = bcol ? bp[1] : make_uint4(0, 0, 0, 0);
-            const uint4 b2 = bcol ? bp[2] : make_uint4(0, 0, 0, 0);
-            mma_16816(acc, A[0][0], A[0][1], A[0][2], A[0][3], b0.x, b0.y);
-            mma_16816(acc, A[1][0], A[1][1], A[1][2], A[1][3], b0.z, b0.w);
-            mma_16816(acc, A[2][0], A[2][1], A[2][2], A[2][3], b1.x, b1.y);
-            mma_16816(acc, A[3][0], A[3][1], A[3][2], A[3][3], b1.z, b1.w);
-            mma_16816(acc, A[4][0], A[4][1], A[4][2], A[4][3], b2.x, b2.y);
+        // word loads and byte-table lookups of a round (digits of bytes (0,1)
+        // and (2,3) side by side in the two halves)
+        auto fetch = [&](int rnd, TerDigits& f) {
+          const uint32_t wa = r0[4 * rnd], wb = r1[4 * rnd];
+          auto lookup = [&](uint32_t wd, int i) -> uint32_t {
+            const uint32_t off = __byte_perm(wd, lut_lane, 0x5504 | (i << 4));
+            return *reinterpret_cast<const uint32_t*>(lut + off);
           };
-          // groups 0,2,4 accumulate in accA, groups 1,3 in accB
-          if ((grp0 & 1) == 0) run(accA, v0); else run(accB, v0);
-          if (split) {
-            if ((grp0 & 1) == 0) {
-              run(accB, v0 + 1);
-              epi(grp0, accA);
-              accA[0] = accA[1] = accA[2] = accA[3] = 0.f;
-            } else {
-              run(accA, v0 + 1);
-              epi(grp0, accB);
-              accB[0] = accB[1] = accB[2] = accB[3] = 0.f;
-            }
+          f.a01 = __byte_perm(lookup(wa, 0), lookup(wa, 1), 0x5410);
+          f.a23 = __byte_perm(lookup(wa, 2), lookup(wa, 3), 0x5410);
+          f.b01 = __byte_perm(lookup(wb, 0), lookup(wb, 1), 0x5410);
+          f.b23 = __byte_perm(lookup(wb, 2), lookup(wb, 3), 0x5410);
+        };
+        // the round's five digit MMAs
+        auto round = [&](int rnd, const TerDigits& f) {
+          // only lanes of real tokens load x; the other columns are not stored
+          const uint4* bp = reinterpret_cast<const uint4*>(xt + rnd * (8 * kTerEntry));
+          if (bcol) {
+            b0 = bp[0];
+            b1 = bp[1];
+            b2 = bp[2];
+          }
+#define TER_MMA(MD, BX, BY)                                                    \
+  mma_16816(acc, ter_operand<MD>(f.a01, E), ter_operand<MD>(f.b01, E),         \
+            ter_operand<MD>(f.a23, E), ter_operand<MD>(f.b23, E), BX, BY)
+          TER_MMA(0, b0.x, b0.y);
+          TER_MMA(1, b0.z, b0.w);
+          TER_MMA(2, b1.x, b1.y);
+          TER_MMA(3, b1.z, b1.w);
+          TER_MMA(4, b2.x, b2.y);
+#undef TER_MMA
+        };
+        // this warp's rounds of the super-group; a group is flushed after its
+        // last round in the range
+        if constexpr (kTerParts == 2) {
+          if (part == 0) ter_range<0, 4>(fetch, round, epi);
+          else ter_range<4, 4>(fetch, round, epi);
+        } else {
+          switch (part) {
+            case 0: ter_range<0, 2>(fetch, round, epi); break;
+            case 1: ter_range<2, 2>(fetch, round, epi); break;
+            case 2: ter_range<4, 2>(fetch, round, epi); break;
+            default: ter_range<6, 2>(fetch, round, epi); break;
           }
         }
-        epi(4, accA);  // group 4 ends with round 7
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
       if (++s == p.stages) { s = 0; ph ^= 1; }
     }
-    float* red = reinterpret_cast<float*>(smem + p.off_red) + (tcount & 1) * (kWarps * 16 * 8);
-    red[(warp * 16 + g) * 8 + 2 * q] = yacc[0];
-    red[(warp * 16 + g) * 8 + 2 * q + 1] = yacc[1];
-    red[(warp * 16 + g + 8) * 8 + 2 * q] = yacc[2];
-    red[(warp * 16 + g + 8) * 8 + 2 * q + 1] = yacc[3];
-    named_bar_sync(1, kWarps * 32);
-    if (threadIdx.x < 128) {
-      const int row = threadIdx.x & 15, col = threadIdx.x >> 4;
-      if (row < 15 && col < p.m && row0 + row < p.n) {
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) sum += red[(w * 16 + row) * 8 + col];
-        p.y[(size_t)col * p.n + row0 + row] = __float2half_rn(sum);
-      }
-    }
+    float* red = partial_slot(p, smem, red_full, tcount, alive);
+    red[(warp * 16 + g) * 8 + q] = yacc[0];
+    red[(warp * 16 + g + 8) * 8 + q] = yacc[1];
+    partial_done(red_full, tcount, lane);
   }
 }
 
 }  // namespace gemv
 
-// Host launcher. Returns UNSUPPORTED when the per-CTA tables do not fit.
-bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
-                          uint16_t* y, cudaStream_t stream) {
+// One launch for up to 8 binary / 4 ternary tokens. Returns UNSUPPORTED
+// when the per-CTA tables do not fit in shared memory.
+static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x, int m,
+                                     uint16_t* y, cudaStream_t stream) {
   using namespace gemv;
   const bool ter = w->format == BONSAI_FMT_TERNARY;
   const int k = (int)w->k;
   const int n = (int)w->n;
-  if (m < 1 || m > 8) return BONSAI_ERR_UNSUPPORTED;
   Params p{};
-  p.w = static_cast<const uint8_t*>(w->packed);
   p.scales = reinterpret_cast<const __half*>(w->scales);
   p.x = reinterpret_cast<const __half*>(x);
   p.y = reinterpret_cast<__half*>(y);
-  p.row_bytes = w->row_bytes;
   p.n = n;
   p.k = k;
-  p.m = (int)m;
+  p.m = m;
   p.G = k / 128;
   p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
-  const int npass = (p.m + 1) / 2;
   if (!ter) {
     p.rows = 16;
     p.data_bytes = k / 8;
-    p.ncolp = p.m == 1 ? 4 : 8;
+    p.xt_stride = p.G * 256 + 64;
   } else {
     p.rows = 15;
     p.data_bytes = (int)bonsai_packed_row_bytes(BONSAI_FMT_TERNARY, k);
     p.n_sg = (p.data_bytes + 127) / 128;
-    p.xt_stride = p.n_sg * kTerVariants * 4 * kTerEntry + 64;
+    p.xt_stride = p.n_sg * 64 * kTerEntry + 64;
   }
-  if (ter && p.m * k * 2 > kLutBytes) return BONSAI_ERR_UNSUPPORTED;  // x staged in the table region
   p.chunks = (p.data_bytes + kChunk - 1) / kChunk;
   p.sc_chunk = ter ? kChunk * 5 / 128 : kChunk / 16;  // groups per chunk: 40 / 64
   p.sc_tma = (p.G % 8 == 0) ? 1 : 0;
@@ -640,22 +660,21 @@ bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
     int scp = (2 * p.sc_chunk + 15) / 16 * 16;
     if ((scp / 4) % 8 == 0) scp += 16;  // words = 4 mod 8: 8 rows hit 8 distinct banks
     p.sc_pitch = scp;
+    const int chunk_max = p.data_bytes < kChunk ? p.data_bytes : kChunk;
+    const int cw = chunk_max / 4;
+    const int pw = ((cw - 4 + 31) / 32) * 32 + 4;  // >= cw words, = 4 mod 32
+    p.pitch = pw * 4;
   }
-  const int chunk_max = p.data_bytes < kChunk ? p.data_bytes : kChunk;
-  const int cw = chunk_max / 4;
-  const int pw = ((cw - 4 + 31) / 32) * 32 + 4;
-  p.pitch = pw * 4;
   p.tiles = (n + p.rows - 1) / p.rows;
-  p.stage_bytes = 16 * p.pitch + 16 * p.sc_pitch;
+  p.stage_bytes = (16 * p.pitch + 16 * p.sc_pitch + 127) / 128 * 128;
 
   auto up = [](int v, int a) { return (v + a - 1) / a * a; };
   int off = 0;
-  p.off_bar = off;   off = up(off + 16 * kMaxStages, 128);
-  p.off_red = off;   off = up(off + 2 * kWarps * 16 * 16 * 4, 128);
-  p.off_p2e = off;   if (!ter) off = up(off + p.m * p.G * 4, 128);
-  p.off_lut = off;   if (ter) off = up(off + kLutBytes, 128);
-  p.off_xt = off;
-  off = ter ? up(off + p.m * p.xt_stride, 1024) : up(off + npass * p.G * 2 * p.ncolp * 64, 1024);
+  p.off_lut = off;   if (ter) off = up(off + kLutBytes, 128);  // at 0: the kernel relies on it
+  p.off_bar = off;   off = up(off + 8 * (2 * kMaxStages + 4), 128);
+  p.off_red = off;   off = up(off + 2 * kWarps * 16 * 8 * 4, 128);
+  p.off_t = off;     if (!ter) off = up(off + p.G * 8 * 4, 128);
+  p.off_xt = off;    off = up(off + p.m * p.xt_stride, 1024);
   p.off_stage = off;
   {
     const int room = (device_max_smem_optin() - off) / p.stage_bytes;
@@ -667,12 +686,23 @@ bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   off = up(off + p.stages * p.stage_bytes, 128);
   const int smem = off;
 
-  const void* fn;
-  if (ter) fn = (const void*)gemv_ternary_kernel;
-  else if (npass == 1) fn = (const void*)gemv_binary_kernel<1>;
-  else if (npass == 2) fn = (const void*)gemv_binary_kernel<2>;
-  else if (npass == 3) fn = (const void*)gemv_binary_kernel<3>;
-  else fn = (const void*)gemv_binary_kernel<4>;
+  CUtensorMap tmw, tms;
+  if (!encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT64, const_cast<void*>(w->packed),
+                            (uint64_t)(w->row_bytes / 8), (uint64_t)n, (uint64_t)w->row_bytes,
+                            (uint32_t)(p.pitch / 8), (uint32_t)p.rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return BONSAI_ERR_CUDA;
+  tms = tmw;  // unused unless the scales are streamed
+  if (p.sc_tma &&
+      !encode_tensor_map_2d(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<uint16_t*>(w->scales),
+                            (uint64_t)p.G, (uint64_t)n, (uint64_t)p.G * 2,
+                            (uint32_t)(p.sc_pitch / 2), (uint32_t)p.rows,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+    return BONSAI_ERR_CUDA;
+
+  const void* fn = ter ? (p.sc_tma ? (const void*)gemv_ternary_kernel<true>
+                                   : (const void*)gemv_ternary_kernel<false>)
+                       : (p.sc_tma ? (const void*)gemv_binary_kernel<true>
+                                   : (const void*)gemv_binary_kernel<false>);
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return BONSAI_ERR_CUDA;
 
   const int sms = device_sm_count();
@@ -686,8 +716,20 @@ bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {&p};
+  void* args[] = {&tmw, &tms, &p};
   return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
+}
+
+// Up to 8 tokens; ternary products of more than 4 tokens take two launches.
+bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
+                          cudaStream_t stream) {
+  if (m < 1 || m > 8) return BONSAI_ERR_UNSUPPORTED;
+  if (w->format != BONSAI_FMT_TERNARY || m <= gemv::kTerMaxTokens)
+    return gemv_launch_one(w, x, (int)m, y, stream);
+  const bonsai_status st = gemv_launch_one(w, x, gemv::kTerMaxTokens, y, stream);
+  if (st != BONSAI_OK) return st;
+  return gemv_launch_one(w, x + gemv::kTerMaxTokens * w->k, (int)m - gemv::kTerMaxTokens,
+                         y + gemv::kTerMaxTokens * w->n, stream);
 }
 
 }  // namespace bonsai
