@@ -36,7 +36,13 @@ namespace gemm {
 constexpr int BM = 128;                 // features per tile  (MMA M)
 constexpr int BN = 256;                 // tokens per tile    (MMA N)
 constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of FP16
-constexpr int STAGES = 4;
+// Separate rings: dequantised weight tiles (A) are produced on chip, X
+// tiles (B) arrive by TMA from L2. Ternary dequantisation has the longer
+// latency per stage, so it gets the deeper A ring.
+template <int FMT> struct Ring {
+  static constexpr int A = FMT == BONSAI_FMT_TERNARY ? 6 : 4;
+  static constexpr int B = FMT == BONSAI_FMT_TERNARY ? 3 : 4;
+};
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B_BYTES = BN * BK * 2;    // 32 KB
 constexpr int TMEM_COLS = 512;
@@ -137,9 +143,7 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 // ---- dequantisation of one row x 64 k into the swizzled A stage ------------
 // Row r of the stage lives at r*128 bytes; its 16-byte chunk c (codes
 // 8c..8c+7) is stored at chunk position c ^ (r & 7).
-__device__ __forceinline__ void dq_binary(const uint8_t* wrow, int kk, uint32_t s2,
-                                          uint32_t dst_row, int sw) {
-  const uint2 wv = *reinterpret_cast<const uint2*>(wrow + 8 * kk);
+__device__ __forceinline__ void dq_binary(uint2 wv, uint32_t s2, uint32_t dst_row, int sw) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const uint32_t x = ~(c < 4 ? wv.x : wv.y) >> (8 * (c & 3));
@@ -167,33 +171,39 @@ __device__ __forceinline__ void dq_ternary(const uint32_t (&wd)[16], uint32_t s2
     const uint32_t byte = (wd[b >> 2] >> (8 * (b & 3))) & 0xFFu;
     F[b - B0] = lds32(lut + byte * 128u);
   }
+  // all 32 pair lookups first, so their latencies overlap
+  uint32_t pv[32];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t h[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int T = T0 + 8 * c + 2 * i;
-      const int b = T / 5 - B0, d = T % 5;
-      const uint32_t nib = d < 4 ? (F[b] >> (2 * d)) & 0xFu
-                                 : ((F[b] >> 8) | ((F[b + 1] & 3u) << 2));
-      h[i] = hmul2_u32(lds32(plut + nib * 128u), s2);
-    }
-    sts128(dst_row + ((c ^ sw) << 4), h[0], h[1], h[2], h[3]);
+  for (int j = 0; j < 32; ++j) {
+    const int T = T0 + 2 * j;
+    const int b = T / 5 - B0, d = T % 5;
+    const uint32_t nib = d < 4 ? (F[b] >> (2 * d)) & 0xFu
+                               : ((F[b] >> 8) | ((F[b + 1] & 3u) << 2));
+    pv[j] = lds32(plut + nib * 128u);
   }
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    sts128(dst_row + ((c ^ sw) << 4), hmul2_u32(pv[4 * c], s2), hmul2_u32(pv[4 * c + 1], s2),
+           hmul2_u32(pv[4 * c + 2], s2), hmul2_u32(pv[4 * c + 3], s2));
 }
 
 template <int FMT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int A_STAGES = Ring<FMT>::A, B_STAGES = Ring<FMT>::B;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sA = smem_u32(smem);
-  const uint32_t sB = sA + STAGES * A_BYTES;
-  const uint32_t sLut = sB + STAGES * B_BYTES;
+  const uint32_t sB = sA + A_STAGES * A_BYTES;
+  const uint32_t sLut = sB + B_STAGES * B_BYTES;
   const uint32_t sPlut = sLut + LUT_BYTES;
   const uint32_t sBar = FMT == BONSAI_FMT_TERNARY ? sPlut + PLUT_BYTES : sLut;
-  const uint32_t full_x = sBar, full_w = sBar + 8 * STAGES, empty = sBar + 16 * STAGES;
-  const uint32_t acc_full = sBar + 24 * STAGES, acc_empty = acc_full + 16;
+  // full_a[s]: the 4 dequantiser warps of the k-step's parity group;
+  // full_b[s]: the X copy (transaction bytes); empty_a / empty_b: the MMAs
+  // that read the stage have completed.
+  const uint32_t full_a = sBar, empty_a = full_a + 8 * A_STAGES;
+  const uint32_t full_b = empty_a + 8 * A_STAGES, empty_b = full_b + 8 * B_STAGES;
+  const uint32_t acc_full = empty_b + 8 * B_STAGES, acc_empty = acc_full + 16;
   const uint32_t drain = acc_empty + 16;
   const uint32_t tmem_slot = drain + 8;
 
@@ -202,10 +212,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     return;
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_x + 8 * s, 1);
-      mbar_init(full_w + 8 * s, 4);  // the 4 dequant warps of one parity group
-      mbar_init(empty + 8 * s, 1);
+    for (int s = 0; s < A_STAGES; ++s) {
+      mbar_init(full_a + 8 * s, 4);
+      mbar_init(empty_a + 8 * s, 1);
+    }
+    for (int s = 0; s < B_STAGES; ++s) {
+      mbar_init(full_b + 8 * s, 1);
+      mbar_init(empty_b + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(acc_full + 8 * a, 1);
@@ -251,11 +264,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
         const int m0 = (tile % p.tok_tiles) * BN;
         for (int kk = 0; kk < p.nk; ++kk, ++g) {
-          const int s = g % STAGES;
-          const uint32_t ph = (g / STAGES) & 1;
-          if (!mbar_wait(empty + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
-          mbar_arrive_expect_tx(full_x + 8 * s, B_BYTES);
-          tma_load_2d(sB + s * B_BYTES, &tmx, kk * BK, m0, full_x + 8 * s);
+          const int s = g % B_STAGES;
+          const uint32_t ph = (g / B_STAGES) & 1;
+          if (!mbar_wait(empty_b + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
+          mbar_arrive_expect_tx(full_b + 8 * s, B_BYTES);
+          tma_load_2d(sB + s * B_BYTES, &tmx, kk * BK, m0, full_b + 8 * s);
         }
       }
     }
@@ -270,20 +283,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + a * 256;
         for (int kk = 0; kk < p.nk; ++kk, ++g) {
-          const int s = g % STAGES;
-          const uint32_t ph = (g / STAGES) & 1;
-          if (!mbar_wait(full_x + 8 * s, ph) || !mbar_wait(full_w + 8 * s, ph)) {
+          const int sa = g % A_STAGES, sb = g % B_STAGES;
+          if (!mbar_wait(full_b + 8 * sb, (g / B_STAGES) & 1) ||
+              !mbar_wait(full_a + 8 * sa, (g / A_STAGES) & 1)) {
             set_status(BONSAI_ERR_TIMEOUT);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(sA + s * A_BYTES);
-          const uint64_t bd = smem_desc_sw128(sB + s * B_BYTES);
+          const uint64_t ad = smem_desc_sw128(sA + sa * A_BYTES);
+          const uint64_t bd = smem_desc_sw128(sB + sb * B_BYTES);
 #pragma unroll
           for (int k4 = 0; k4 < BK / 16; ++k4)  // +32 bytes per K=16 step inside the atom
             mma_f16_ss(d_tmem, ad + 2 * k4, bd + 2 * k4, kIdesc, (kk | k4) != 0);
-          mma_commit(empty + 8 * s);
+          mma_commit(empty_a + 8 * sa);
+          mma_commit(empty_b + 8 * sb);
         }
         if (ok) mma_commit(acc_full + 8 * a);
       }
@@ -329,6 +343,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = (dq & 3) * 32 + lane; // feature row within the tile
     const int sw = r & 7;
     const uint32_t lut = sLut + lane * 4, plut = sPlut + lane * 4;
+    // Ternary: the packed row is read in 64-byte blocks (320 codes = 5
+    // k-steps) one block ahead, so the load latency hides behind the
+    // dequantisation of the current block; the block's group scales travel
+    // with it. Binary: 8 bytes and one scale per k-step, loaded directly
+    // (measured faster than the block scheme for this cheap expansion).
+    constexpr int KPB = 5;
+    const int nblk = (p.nk + KPB - 1) / KPB;
+    uint32_t cur[16], nxt[16];
+    uint16_t csc[3], nsc[3];
+    int cur_key = -1, nxt_key = -1;
+    auto load_block = [&](int tile, int u, uint32_t (&dst)[16], uint16_t (&sc)[3]) {
+      const int n = (tile / p.tok_tiles) * BM + r;
+      const bool nok = n < p.n;
+      const unsigned short* srow = reinterpret_cast<const unsigned short*>(p.scales) +
+                                   (size_t)(nok ? n : 0) * p.G;
+      const int g0 = (KPB * u) >> 1;
+#pragma unroll
+      for (int i = 0; i < 3; ++i) sc[i] = (nok && g0 + i < p.G) ? srow[g0 + i] : (uint16_t)0;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(p.w + (long long)(nok ? n : 0) * p.row_bytes + 64 * u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 q4 = src[i];  // ternary rows hold whole 64-byte blocks
+        dst[4 * i] = q4.x; dst[4 * i + 1] = q4.y; dst[4 * i + 2] = q4.z; dst[4 * i + 3] = q4.w;
+      }
+    };
     uint32_t g = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
@@ -338,35 +378,51 @@ __global__ void __launch_bounds__(THREADS, 1)
       const __half* srow = p.scales + (size_t)(nok ? n : 0) * p.G;
       for (int kk = 0; kk < p.nk; ++kk, ++g) {
         if ((g & 1) != h) continue;
-        const int s = g % STAGES;
-        const uint32_t ph = (g / STAGES) & 1;
+        const int s = g % A_STAGES;
+        const uint32_t ph = (g / A_STAGES) & 1;
         const uint32_t dst = sA + s * A_BYTES + r * 128;
-        const __half sc = srow[kk >> 1];
-        const uint32_t s2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;
-        uint32_t wd[16];
-        if (FMT == BONSAI_FMT_TERNARY) {
-          const uint4* src = reinterpret_cast<const uint4*>(wrow + 64 * (kk / 5));
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 q4 = src[i];
-            wd[4 * i] = q4.x; wd[4 * i + 1] = q4.y; wd[4 * i + 2] = q4.z; wd[4 * i + 3] = q4.w;
-          }
-        }
-        if (!mbar_wait(empty + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
-        if (FMT == BONSAI_FMT_BINARY) {
-          dq_binary(wrow, kk, s2, dst, sw);
+        if constexpr (FMT == BONSAI_FMT_BINARY) {
+          const uint2 wv = *reinterpret_cast<const uint2*>(wrow + 8 * kk);
+          const __half sc = srow[kk >> 1];
+          const uint32_t s2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;
+          if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
+          dq_binary(wv, s2, dst, sw);
         } else {
+          const int u = kk / KPB;
+          const int key = tile * nblk + u;
+          if (key != cur_key) {
+            if (key == nxt_key) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
+#pragma unroll
+              for (int i = 0; i < 3; ++i) csc[i] = nsc[i];
+            } else {
+              load_block(tile, u, cur, csc);
+            }
+            cur_key = key;
+            // prefetch the block that follows in this thread's order
+            const int nt = u + 1 < nblk ? tile : tile + (int)gridDim.x;
+            const int nu = u + 1 < nblk ? u + 1 : 0;
+            if (nt < p.tiles) {
+              load_block(nt, nu, nxt, nsc);
+              nxt_key = nt * nblk + nu;
+            }
+          }
+          const int si = (kk >> 1) - ((KPB * u) >> 1);  // 0..2
+          const uint32_t sc = si == 0 ? csc[0] : si == 1 ? csc[1] : csc[2];
+          const uint32_t s2 = sc * 0x10001u;  // rows past n carry scale 0
+          if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
           switch (kk % 5) {
-            case 0: dq_ternary<0>(wd, s2, lut, plut, dst, sw); break;
-            case 1: dq_ternary<1>(wd, s2, lut, plut, dst, sw); break;
-            case 2: dq_ternary<2>(wd, s2, lut, plut, dst, sw); break;
-            case 3: dq_ternary<3>(wd, s2, lut, plut, dst, sw); break;
-            default: dq_ternary<4>(wd, s2, lut, plut, dst, sw); break;
+            case 0: dq_ternary<0>(cur, s2, lut, plut, dst, sw); break;
+            case 1: dq_ternary<1>(cur, s2, lut, plut, dst, sw); break;
+            case 2: dq_ternary<2>(cur, s2, lut, plut, dst, sw); break;
+            case 3: dq_ternary<3>(cur, s2, lut, plut, dst, sw); break;
+            default: dq_ternary<4>(cur, s2, lut, plut, dst, sw); break;
           }
         }
         fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
         __syncwarp();
-        if (lane == 0) mbar_arrive(full_w + 8 * s);
+        if (lane == 0) mbar_arrive(full_a + 8 * s);
       }
     }
   }
@@ -405,7 +461,10 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
 
   const bool ter = w->format == BONSAI_FMT_TERNARY;
-  const int smem = STAGES * (A_BYTES + B_BYTES) + (ter ? LUT_BYTES + PLUT_BYTES : 0) + BAR_BYTES;
+  const int smem = ter ? Ring<BONSAI_FMT_TERNARY>::A * A_BYTES + Ring<BONSAI_FMT_TERNARY>::B * B_BYTES +
+                             LUT_BYTES + PLUT_BYTES + BAR_BYTES
+                       : Ring<BONSAI_FMT_BINARY>::A * A_BYTES + Ring<BONSAI_FMT_BINARY>::B * B_BYTES +
+                             BAR_BYTES;
   if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
   const void* fn = ter ? (const void*)gemm_kernel<BONSAI_FMT_TERNARY>
                        : (const void*)gemm_kernel<BONSAI_FMT_BINARY>;
