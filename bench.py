@@ -12,7 +12,7 @@ replicas that the working set exceeds L2.
 
 The line also carries `secondary` measurements of the other workloads:
 the binary decode product (K=N=1024), the 64-layer decode sweep (binary and
-ternary, tokens/s; one step = 448 products = one token), the prefill GEMM
+ternary, tokens/s; one step = 256 products = one token), the prefill GEMM
 M=512 (binary and ternary, TFLOP/s) and the XNOR product 512x4096x4096.
 Each can also be the headline with --workload.
 
@@ -162,6 +162,31 @@ def max_over_ranks(world, value):
     return float(t.item())
 
 
+def profiled_traffic(summary):
+    """DRAM bytes per launch from an ncu summary under profiles/, or None if
+    the kernel sources changed since the capture (the summary records a
+    sha256 over the source files it covers)."""
+    import hashlib
+    import re
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", summary)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"source sha256 \(([^)]*)\): ([0-9a-f]{64})", text)
+    t = re.search(r"DRAM bytes per launch: (\d+)", text)
+    if not m or not t:
+        return None
+    h = hashlib.sha256()
+    for f in m.group(1).split(" + "):
+        try:
+            h.update(open(os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                       "sub_bit_weight_binary_b300", "csrc", f.strip()), "rb").read())
+        except OSError:
+            return None
+    return int(t.group(1)) if h.hexdigest() == m.group(2) else None
+
+
 def make_weights(fmt, n, k, seed, tid_w, tid_s, flags):
     """Seeded weights generated on the device (codes -> pack for ternary)."""
     import torch
@@ -278,9 +303,11 @@ class GemvWorkload:
 
     def roofline(self, r, pk):
         a = self.unit_bytes() / (r["kernel_ms"] / 1e3) / 1e9
-        return {"bound": "hbm", "kernel": "gemv_kernel<%s>" % ("TERNARY" if self.fmt == 2 else "BINARY"),
+        prof = {(2, 17408, 5120): "gemv_ternary_k5120_n17408.md",
+                (1, 17408, 5120): "gemv_binary_k5120_n17408.md"}.get((self.fmt, self.n, self.k))
+        return {"bound": "hbm", "kernel": "gemv_%s_kernel" % ("ternary" if self.fmt == 2 else "binary"),
                 "achieved": round(a, 1), "peak": pk["hbm"], "unit": "GB/s",
-                "frac": round(a / pk["hbm"], 4), "traffic": None,
+                "frac": round(a / pk["hbm"], 4), "traffic": profiled_traffic(prof) if prof else None,
                 "peak_src": "%s HBM copy (burst)" % pk["src"],
                 "bytes_per_launch": self.unit_bytes()}
 
@@ -315,11 +342,16 @@ class GemvWorkload:
             passes, rows - 1, self.n, el)
 
 
-SWEEP_SHAPES = [(5120, 5120)] * 4 + [(17408, 5120)] * 2 + [(5120, 17408)]  # q k v o gate up down
+# One layer: q, k, v (5120 x 5120 each) stored stacked as one 15360 x 5120
+# matrix, o 5120 x 5120, gate and up (17408 x 5120 each) stacked as one
+# 34816 x 5120 matrix, down 5120 x 17408: four products, the same bytes as
+# seven separate ones.
+SWEEP_SHAPES = [(15360, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]  # qkv o gate_up down
 
 
 class SweepWorkload:
-    """64-layer decode: 7 products per layer, 448 per token, weights resident."""
+    """64-layer decode: 4 products per layer (q/k/v and gate/up stacked),
+    256 per token, weights resident."""
     kind = "sweep"
 
     def __init__(self, fmt, name, layers=64):
@@ -341,7 +373,7 @@ class SweepWorkload:
                                            sb.BONSAI_WEIGHTS_PREFETCH))
         self.x = {k: torch.from_numpy(synth.gen_x(seed + k, 1, k).view(np.float16)[0].copy()).cuda()
                   for k in (5120, 17408)}
-        self.y = {n: torch.empty(n, dtype=torch.float16, device="cuda") for n in (5120, 17408)}
+        self.y = {n: torch.empty(n, dtype=torch.float16, device="cuda") for n, _ in SWEEP_SHAPES}
         torch.cuda.synchronize()
         sb.check()
 
@@ -386,7 +418,9 @@ class SweepWorkload:
 
     def roofline(self, r, pk):
         a = self.unit_bytes() / (r["ms"] / r["steps"] / 1e3) / 1e9
-        return {"bound": "hbm", "kernel": "gemv_kernel (448 per token)", "achieved": round(a, 1),
+        return {"bound": "hbm", "kernel": "gemv_%s_kernel (%d per token)" % (
+                    "ternary" if self.fmt == 2 else "binary", self.layers * len(SWEEP_SHAPES)),
+                "achieved": round(a, 1),
                 "peak": pk["hbm"], "unit": "GB/s", "frac": round(a / pk["hbm"], 4),
                 "traffic": None, "peak_src": "%s HBM copy (burst)" % pk["src"],
                 "bytes_per_token": self.unit_bytes()}
@@ -394,7 +428,9 @@ class SweepWorkload:
     def config(self):
         return {"workload": self.name, "layers": self.layers,
                 "shapes_nk": SWEEP_SHAPES, "format": "ternary" if self.fmt == 2 else "binary",
-                "timing": "one CUDA graph per token (448 launches), replayed per step",
+                "stacked": "q/k/v and gate/up weights stored stacked, one product each",
+                "timing": "one CUDA graph per token (%d launches), replayed per step" % (
+                    self.layers * len(SWEEP_SHAPES)),
                 "l2": "inputs larger than L2: %.2f GB of weights per token" % (self.unit_bytes() / 1e9)}
 
 
@@ -452,9 +488,12 @@ class GemmWorkload:
 
     def roofline(self, r, pk):
         a = self.flops() / (r["kernel_ms"] / 1e3) / 1e12
-        return {"bound": "tensor", "kernel": "gemm_kernel<%s>" % ("TERNARY" if self.fmt == 2 else "BINARY"),
+        return {"bound": "tensor", "kernel": "gemm_kernel<%d> (%s)" % (
+                    self.fmt, "ternary" if self.fmt == 2 else "binary"),
                 "achieved": round(a, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": round(a / pk["bf16"], 4), "traffic": None,
+                "frac": round(a / pk["bf16"], 4),
+                "traffic": profiled_traffic("gemm_%s_m512_k5120_n17408.md" % (
+                    "ternary" if self.fmt == 2 else "binary")) if self.m == 512 else None,
                 "peak_src": "%s dense bf16 cuBLAS burst (fp16 has the same dense rate)" % pk["src"]}
 
     def config(self):
@@ -502,7 +541,8 @@ class XnorWorkload:
         peak = POPC_PER_CLK_SM * 148 * mhz * 1e6 / 1e12  # T popc/s
         a = self.words() / (r["kernel_ms"] / 1e3) / 1e12
         return {"bound": "alu", "kernel": "xnor_kernel", "achieved": round(a, 3), "peak": round(peak, 3),
-                "unit": "T word-popc/s", "frac": round(a / peak, 4), "traffic": None,
+                "unit": "T word-popc/s", "frac": round(a / peak, 4),
+                "traffic": profiled_traffic("xnor_m512_k4096_n4096.md"),
                 "peak_src": "16 popc/clk/SM x 148 SMs x %.0f MHz (popc rate measured by a probe)" % mhz}
 
     def config(self):

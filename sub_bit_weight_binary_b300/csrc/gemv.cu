@@ -4,9 +4,9 @@
 // re-streamed per token): each packed byte is read from HBM once.
 //
 // Structure (sm_103a):
-//  * A persistent grid, one CTA per SM: 16 consumer warps and one producer
-//    warp. The producer streams tiles of 16 rows (15 + a neutral row for
-//    ternary) in chunks of <= 1024 bytes per row into a shared-memory ring
+//  * A persistent grid, one CTA per SM: 16 consumer warps, a producer warp and
+//    a reducer warp. The producer streams tiles of 16 rows in chunks of
+//    <= 1024 bytes per row into a shared-memory ring
 //    with 2-D TMA boxes, one box for the weights and one for the chunk's
 //    group scales. A box is as wide as the padded row pitch (pitch/4 = 4
 //    mod 32 words), so the consumers' word loads are conflict-free; the
@@ -27,12 +27,13 @@
 // flip", 三值权重 page). The same 2^-10 step for every j gives, per group,
 //   acc = sum_k 2^-j(k) x_k + 2^-10 sum_k c_k x_k.
 //  * binary:  sum (2b-1) x = 2^11 acc - T,  T = sum (2^(11-j)+1) x, built
-//    once per CTA from x.
-//  * ternary: the tile's 16th row holds byte 121 (five zero codes); its MMA
-//    sum comes from the same instruction as every real row, so
-//    sum (c-1) x = 2^10 (acc_row - acc_neutral) and an all-zero group gives
-//    exactly 0. The correction is linear, so a group may be split across
-//    rounds and warps, each part subtracting its own neutral part.
+//    once per CTA from x. Every binary code is +-1, so the rounding of the
+//    offset sums stays small against the output's own sum |x s w|.
+//  * ternary: one packed FP16 subtraction of the digit-1 operand (same j)
+//    turns each operand into (c-1)*2^-10 exactly (both values share the
+//    exponent), so a zero code contributes an exact 0 product, an all-zero
+//    group gives exactly 0 and the accumulation only rounds the nonzero
+//    terms: sum (c-1) x = 2^10 acc.
 #include <type_traits>
 
 #include "common.cuh"
@@ -59,14 +60,13 @@ constexpr int kChunk = 1024;               // packed bytes per row per stage
 constexpr int kLutBytes = 256 * 256;       // ternary: 256 entries x (32 lanes x 4 B + pad)
 constexpr int kTerEntry = 48;              // ternary x-table bytes per (round, side, lane)
 constexpr int kTerMaxTokens = 4;           // two B columns (group parities) per token
-constexpr uint32_t kZeroTrits = 121;       // byte of five zero codes
 
 struct Params {
   const __half* scales;
   const __half* x;
   __half* y;
   int n, k, m, G;
-  int rows;         // real rows per tile: 16 binary, 15 ternary (row 15 = neutral)
+  int rows;         // rows per tile (16)
   int data_bytes;   // packed bytes per row that are streamed
   int chunks;       // stages per tile
   int pitch;        // smem row pitch, bytes = TMA box width
@@ -201,12 +201,19 @@ __host__ __device__ constexpr uint32_t exp_base(int j) {
 // one LOP3 with the mask as its immediate.
 struct ExpRegs {
   uint32_t e[10];
+  uint32_t one[5];  // ternary: digit-1 operand per digit position
   __device__ __forceinline__ ExpRegs() {
 #pragma unroll
     for (int j = 0; j < 10; ++j) {
       uint32_t v = exp_base(j);
       asm volatile("" : "+r"(v));  // keep the value in a register
       e[j] = v;
+    }
+#pragma unroll
+    for (int md = 0; md < 5; ++md) {
+      uint32_t v = (uint32_t(15 - 2 * md) << 10 | (1u << (2 * md))) * 0x10001u;
+      asm volatile("" : "+r"(v));
+      one[md] = v;
     }
   }
 };
@@ -392,9 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // bits j = 2i, 2i+1.
 __host__ __device__ constexpr uint32_t mant_mask2(int j) { return (3u << j) | (3u << (j + 16)); }
 
+// digit-1 operand of position MD in both halves: 2^-j + 2^-10, j = 2 MD
+__host__ __device__ constexpr uint32_t ter_one(int md) {
+  return exp_base(2 * md) | (1u << (2 * md)) | (1u << (2 * md + 16));
+}
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// (c-1) * 2^-10 for the two codes of digit position MD: the offset operand
+// 2^-j + d*2^-10 minus the digit-1 operand, exact (same exponent, Sterbenz)
 template <int MD>
 __device__ __forceinline__ uint32_t ter_operand(uint32_t f, const ExpRegs& E) {
-  return and_or<mant_mask2(2 * MD)>(f, E.e[2 * MD]);
+  return hsub2_u32(and_or<mant_mask2(2 * MD)>(f, E.e[2 * MD]), E.one[MD]);
 }
 
 // group (0..4) of the super-group that the first / last code of round r falls in
@@ -491,18 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
   const uint32_t red_full = bar_full + 16 * kMaxStages;
   init_barriers(bar_full, bar_empty, p.stages);
-  // Row 15 of every stage holds zero codes (and zero scales); the 15-row
-  // boxes never write it.
-  for (int i = threadIdx.x; i < p.stages * (p.pitch / 4); i += kThreads) {
-    const int s = i / (p.pitch / 4), wd = i - s * (p.pitch / 4);
-    reinterpret_cast<uint32_t*>(smem + p.off_stage + s * p.stage_bytes + 15 * p.pitch)[wd] =
-        kZeroTrits * 0x01010101u;
-  }
-  for (int i = threadIdx.x; i < p.stages * (p.sc_pitch / 4); i += kThreads) {
-    const int s = i / (p.sc_pitch / 4), wd = i - s * (p.sc_pitch / 4);
-    reinterpret_cast<uint32_t*>(smem + p.off_stage + s * p.stage_bytes + 16 * p.pitch +
-                                15 * p.sc_pitch)[wd] = 0u;
-  }
   __syncthreads();
   pdl_launch_dependents();
   if (warp == kProducer) {
@@ -533,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool alive = true;
   int tcount = 0;
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tcount) {
-    const int row0 = tile * 15;
+    const int row0 = tile * 16;
     float yacc[2] = {0.f, 0.f};  // token q, rows g and g+8
     for (int c = 0; c < p.chunks; ++c) {
       const int len = min(kChunk, p.data_bytes - c * kChunk);
@@ -553,12 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int gl = min(5 * sgw + grp, p.G - 1 - c * p.sc_chunk);  // group within the chunk
           const int gi = 5 * sg + grp;
           const float sa = scale_of<SC>(p, stage, g, row0 + g, gl, gi);
-          const float sb = scale_of<SC>(p, stage, g + 8, row0 + g + 8, gl, gi);  // row 15: unused
+          const float sb = scale_of<SC>(p, stage, g + 8, row0 + g + 8, gl, gi);
           const float va = side ? acc[1] : acc[0];
           const float vb = side ? acc[3] : acc[2];
-          const float t = __shfl_sync(0xFFFFFFFFu, vb, 28 + q);  // neutral row 15
-          yacc[0] = fmaf(sa, (va - t) * 1024.f, yacc[0]);
-          yacc[1] = fmaf(sb, (vb - t) * 1024.f, yacc[1]);
+          yacc[0] = fmaf(sa, va * 1024.f, yacc[0]);
+          yacc[1] = fmaf(sb, vb * 1024.f, yacc[1]);
           if (side) {
             acc[1] = 0.f;
             acc[3] = 0.f;
@@ -648,7 +655,7 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
     p.data_bytes = k / 8;
     p.xt_stride = p.G * 256 + 64;
   } else {
-    p.rows = 15;
+    p.rows = 16;
     p.data_bytes = (int)bonsai_packed_row_bytes(BONSAI_FMT_TERNARY, k);
     p.n_sg = (p.data_bytes + 127) / 128;
     p.xt_stride = p.n_sg * 64 * kTerEntry + 64;

@@ -161,6 +161,59 @@ def test_gemv_special_values():
     assert np.all(host(yz).view(np.float16) == 0)
 
 
+def _sparse_ternary_codes(seed, n, k, per_mille):
+    """Seeded ternary codes with `per_mille`/1000 of them nonzero (+-1 equally
+    likely), from the counter-based generator's raw words."""
+    w = synth.words(seed, 0x51, 0, n * k)
+    keep = (w >> np.uint64(54)) < np.uint64(per_mille * 1024 // 1000)
+    sign = np.where((w & np.uint64(1)) == 1, 1, -1)
+    return np.where(keep, sign, 0).astype(np.int8).reshape(n, k)
+
+
+def _ternary_from_codes(codes, seed):
+    t = torch()
+    n, k = codes.shape
+    rb = sb.bonsai_packed_row_bytes(TER, k)
+    packed_gpu = t.empty((n, rb), dtype=t.uint8, device="cuda")
+    sb.bonsai_pack_ternary(dev(codes), packed_gpu)
+    scales = synth.gen_scales(seed, n, k)
+    return sb.Weights(TER, n, k, packed_gpu, dev(scales)), oracle.pack_ternary(codes), scales
+
+
+@pytest.mark.parametrize("per_mille", [100, 20, 5])
+@pytest.mark.parametrize("m", [1, 3])
+def test_sparse_ternary(per_mille, m):
+    """Rows with few nonzero weights: every output must still meet the bound
+    against its own (small) norm, so zero codes may add nothing to the error."""
+    n, k = 300, 5120
+    codes = _sparse_ternary_codes(60 + per_mille, n, k, per_mille)
+    w, packed, scales = _ternary_from_codes(codes, 61)
+    x = synth.gen_x(62, m, k)
+    y = Guarded((m, n), torch().float16)
+    sb.bonsai_gemm(w, dev(x), y.t)
+    assert sb.bonsai_check_async() == 0
+    y_ref, nrm = oracle.linear(TER, packed, scales, x)
+    assert_close(host(y.t), y_ref, nrm, "sparse ternary %d/1000 m=%d" % (per_mille, m))
+    y.check()
+
+
+def test_one_nonzero_ternary_per_row():
+    """Each row holds a single nonzero code (at a seeded position and sign);
+    y must be s*x[k] to the bound, with all other codes contributing nothing."""
+    n, k = 512, 5120
+    r = synth.words(70, 0x52, 0, n)
+    pos = (r % np.uint64(k)).astype(np.int64)
+    codes = np.zeros((n, k), dtype=np.int8)
+    codes[np.arange(n), pos] = np.where((r >> np.uint64(63)) == 1, 1, -1)
+    w, packed, scales = _ternary_from_codes(codes, 71)
+    x = synth.gen_x(72, 1, k)
+    y = torch().empty(n, dtype=torch().float16, device="cuda")
+    sb.bonsai_gemv(w, dev(x[0]), y)
+    assert sb.bonsai_check_async() == 0
+    y_ref, nrm = oracle.linear(TER, packed, scales, x)
+    assert_close(host(y), y_ref[0], nrm[0], "one nonzero per row")
+
+
 # ------------------------------------------------------------ GEMM, small m
 @pytest.mark.parametrize("fmt", [BIN, TER])
 @pytest.mark.parametrize("m,n,k", [(2, 300, 1024), (5, 1024, 5120), (8, 129, 640), (3, 64, 17408)])
