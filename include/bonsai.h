@@ -50,9 +50,10 @@
  * Conventions:
  *   - Every pointer passed to a compute call is a DEVICE pointer owned by the
  *     caller. The library allocates no device memory and keeps no pointer
- *     after the call returns. Its only device state is one 32-bit status word
- *     per device, a file-scope __device__ variable, written by kernels that
- *     detect bad input codes or a bounded wait that ran out.
+ *     after the call returns. Its device state is one 32-bit status word per
+ *     device, a file-scope __device__ variable, written by kernels that
+ *     detect bad input codes or a bounded wait that ran out, plus the fixed
+ *     scratch array of bonsai_gemv_splitk_static (declared below).
  *   - Calls enqueue work on `stream` and return without synchronising (they
  *     can be captured in a CUDA graph). A non-OK return means nothing was
  *     launched. Kernel-side problems are reported by bonsai_check_async.
@@ -138,6 +139,30 @@ bonsai_status bonsai_pack_ternary(const int8_t* codes, int64_t rows, int64_t k,
  * ("第一の壁"): the kernel streams each packed byte once. */
 bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x,
                           uint16_t* y, bonsai_stream stream);
+
+/* Decode product with K split across thread blocks, for matrices with few
+ * rows (n <= 8192), computing the same y as bonsai_gemv (to the same error
+ * bound, not bit-identically: the sums are ordered differently). The pages
+ * have no counterpart of this call; it exists for callers that cannot
+ * allocate device memory at call time -- a serving loop that must not stall
+ * on cudaMalloc/cudaFree, which synchronise the device, or a process whose
+ * device memory is budgeted up front -- yet need per-call scratch for the
+ * split sums. The scratch is a fixed file-scope device array of 1 MiB of FP32
+ * partial sums (at most 32 splits x 8192 rows) and 512 arrival counters;
+ * nothing is allocated, ever.
+ *   w, x, y: as bonsai_gemv (device pointers, 16-byte aligned).
+ *   Returns BONSAI_ERR_UNSUPPORTED for n > 8192 (the scratch holds no more
+ *   rows), with nothing launched; BONSAI_ERR_CUDA if the scratch address
+ *   cannot be obtained.
+ * The first call on a device looks up the scratch address
+ * (cudaGetSymbolAddress) and enqueues a clear of the counters on `stream`;
+ * make that first call before starting any stream capture that is to contain
+ * later calls. Calls share the scratch: two calls that overlap in time
+ * (different streams, or different host threads on one device) corrupt each
+ * other's sums, so order them on one stream or synchronise between them.
+ * Results of two ordered calls with the same inputs are bit-identical. */
+bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t* x,
+                                        uint16_t* y, bonsai_stream stream);
 
 /* Multi-token product Y[m][n] = sum_k X[m][k] * s[n][k/128] * w[n][k],
  * X FP16 [m][k], Y FP16 [m][n]. m <= 8 runs the streaming decode kernel with

@@ -60,6 +60,8 @@ def lib():
             f.restype = S
         L.bonsai_gemv.argtypes = [W, P, P, P]
         L.bonsai_gemv.restype = S
+        L.bonsai_gemv_splitk_static.argtypes = [W, P, P, P]
+        L.bonsai_gemv_splitk_static.restype = S
         L.bonsai_gemm.argtypes = [W, P, I64, P, P]
         L.bonsai_gemm.restype = S
         L.bonsai_xnor_gemm.argtypes = [P, P, I64, W, P, P, P]
@@ -154,6 +156,16 @@ def bonsai_gemv(w: Weights, x, y, stream=None):
     ws = w.c_struct()
     _ok(lib().bonsai_gemv(C.byref(ws), _ptr(x, (torch.float16,), "x"),
                           _ptr(y, (torch.float16,), "y"), _stream(stream)), "bonsai_gemv")
+
+
+def bonsai_gemv_splitk_static(w: Weights, x, y, stream=None):
+    """bonsai_gemv with K split over thread blocks and a fixed device scratch
+    array (no allocation); n <= 8192, calls on one device must not overlap."""
+    import torch
+    ws = w.c_struct()
+    _ok(lib().bonsai_gemv_splitk_static(C.byref(ws), _ptr(x, (torch.float16,), "x"),
+                                        _ptr(y, (torch.float16,), "y"), _stream(stream)),
+        "bonsai_gemv_splitk_static")
 
 
 def bonsai_gemm(w: Weights, x, y, stream=None):

@@ -10,6 +10,7 @@ namespace bonsai {
 bonsai_status pack_binary_launch(const int8_t*, int64_t, int64_t, void*, int64_t, cudaStream_t);
 bonsai_status pack_ternary_launch(const int8_t*, int64_t, int64_t, void*, int64_t, cudaStream_t);
 bonsai_status gemv_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, cudaStream_t);
+bonsai_status splitk_launch(const bonsai_weights*, const uint16_t*, uint16_t*, cudaStream_t);
 bonsai_status gemm_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, cudaStream_t);
 bonsai_status xnor_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
                           int32_t*, uint16_t*, cudaStream_t);
@@ -179,6 +180,15 @@ bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x, uint16_t* 
   if (!x || !y) return BONSAI_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
   return gemv_launch(w, x, 1, y, stream);
+}
+
+bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
+                                        bonsai_stream stream) {
+  bonsai_status st = check_weights(w);
+  if (st != BONSAI_OK) return st;
+  if (!x || !y) return BONSAI_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
+  return splitk_launch(w, x, y, stream);
 }
 
 bonsai_status bonsai_gemm(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
