@@ -50,10 +50,11 @@ unsigned int read_clear_status_gemv() {
 
 namespace gemv {
 
-constexpr int kWarps = 16;                 // consumer warps
-constexpr int kProducer = kWarps;          // warp that issues the TMA copies
-constexpr int kReducer = kWarps + 1;       // warp that sums the warps' partials of a tile
-constexpr int kThreads = (kWarps + 2) * 32;
+// Consumer warps per CTA; warp W issues the TMA copies, warp W+1 sums the
+// warps' partials of a tile.
+constexpr int kBinWarps = 16;
+constexpr int kTerWarps = 16;
+__host__ __device__ constexpr int threads_for(int w) { return (w + 2) * 32; }
 constexpr int kMaxStages = 8;
 constexpr int kStageBudget = 96 * 1024;    // bytes in flight per CTA
 constexpr int kChunk = 1024;               // packed bytes per row per stage
@@ -85,15 +86,16 @@ struct Params {
 // ---------------------------------------------------------------------------
 // Barriers at off_bar: full[kMaxStages], empty[kMaxStages] of the weight
 // ring, then red_full[2], red_empty[2] of the two partial-sum slots.
+template <int W>
 __device__ __forceinline__ void init_barriers(uint32_t bar_full, uint32_t bar_empty, int stages) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kWarps);
+      mbar_init(bar_empty + 8 * s, W);
     }
     const uint32_t red_full = bar_full + 16 * kMaxStages;
     for (int s = 0; s < 2; ++s) {
-      mbar_init(red_full + 8 * s, kWarps);
+      mbar_init(red_full + 8 * s, W);
       mbar_init(red_full + 16 + 8 * s, 1);
     }
     fence_barrier_init();
@@ -104,6 +106,7 @@ __device__ __forceinline__ void init_barriers(uint32_t bar_full, uint32_t bar_em
 // turn. A consumer warp waits until its slot is free, stores its partials
 // and arrives on red_full; the reducer warp sums the 16 warps' partials,
 // writes y and frees the slot. The consumer warps never wait for each other.
+template <int W>
 __device__ __forceinline__ float* partial_slot(const Params& p, uint8_t* smem, uint32_t red_full,
                                                int tcount, bool& alive) {
   const int slot = tcount & 1;
@@ -112,7 +115,7 @@ __device__ __forceinline__ float* partial_slot(const Params& p, uint8_t* smem, u
     set_status(BONSAI_ERR_TIMEOUT);
     alive = false;
   }
-  return reinterpret_cast<float*>(smem + p.off_red) + slot * (kWarps * 16 * 8);
+  return reinterpret_cast<float*>(smem + p.off_red) + slot * (W * 16 * 8);
 }
 
 __device__ __forceinline__ void partial_done(uint32_t red_full, int tcount, int lane) {
@@ -120,6 +123,7 @@ __device__ __forceinline__ void partial_done(uint32_t red_full, int tcount, int 
   if (lane == 0) mbar_arrive(red_full + 8 * (tcount & 1));
 }
 
+template <int W>
 __device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int lane) {
   pdl_wait();  // y may be read by earlier work on the stream
   int tcount = 0;
@@ -129,14 +133,14 @@ __device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int l
       set_status(BONSAI_ERR_TIMEOUT);
       return;
     }
-    const float* red = reinterpret_cast<const float*>(smem + p.off_red) + slot * (kWarps * 16 * 8);
+    const float* red = reinterpret_cast<const float*>(smem + p.off_red) + slot * (W * 16 * 8);
     const int row0 = tile * p.rows;
     for (int o = lane; o < 16 * p.m; o += 32) {
       const int row = o & 15, col = o >> 4;
       if (row < p.rows && row0 + row < p.n) {
         float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) sum += red[(w * 16 + row) * 8 + col];
+        for (int w = 0; w < W; ++w) sum += red[(w * 16 + row) * 8 + col];
         p.y[(size_t)col * p.n + row0 + row] = __float2half_rn(sum);
       }
     }
@@ -244,8 +248,9 @@ __device__ __forceinline__ uint32_t bin_operand(uint32_t w, uint32_t wr, const E
 // (bits i, i+16 of word q of the group) and class i+8 (bits i+8, i+24).
 // T[gi][t] = sum over the group of (2^(11-j)+1) x. One thread per word of
 // x; the four words of a group sit in four neighbouring lanes.
+template <int W>
 __device__ void build_binary_tables(const Params& p, uint8_t* smem) {
-  const int lane = threadIdx.x & 31, nthr = kWarps * 32;
+  const int lane = threadIdx.x & 31, nthr = W * 32;
   float* T = reinterpret_cast<float*>(smem + p.off_t);
   const int words = p.k / 32, total = p.m * words;
   for (int base = threadIdx.x - lane; base < total; base += nthr) {
@@ -293,7 +298,7 @@ __device__ void build_binary_tables(const Params& p, uint8_t* smem) {
 }
 
 template <bool SC>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(kBinWarps), 1)
     gemv_binary_kernel(const __grid_constant__ CUtensorMap tmw,
                        const __grid_constant__ CUtensorMap tms, const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -301,20 +306,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
   const uint32_t red_full = bar_full + 16 * kMaxStages;
-  init_barriers(bar_full, bar_empty, p.stages);
+  init_barriers<kBinWarps>(bar_full, bar_empty, p.stages);
   __syncthreads();
   pdl_launch_dependents();
-  if (warp == kProducer) {
+  if (warp == kBinWarps) {
     if (lane == 0) produce(&tmw, &tms, p, sbase, bar_full, bar_empty);
     return;
   }
-  if (warp == kReducer) {
-    reducer(p, smem, red_full, lane);
+  if (warp == kBinWarps + 1) {
+    reducer<kBinWarps>(p, smem, red_full, lane);
     return;
   }
   pdl_wait();  // x is written by earlier work on the stream
-  build_binary_tables(p, smem);
-  named_bar_sync(1, kWarps * 32);
+  build_binary_tables<kBinWarps>(p, smem);
+  named_bar_sync(1, kBinWarps * 32);
 
   const int g = lane >> 2, q = lane & 3;
   const bool bcol = g < p.m;
@@ -336,13 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* stage = smem + p.off_stage + s * p.stage_bytes;
       const uint32_t* stg = reinterpret_cast<const uint32_t*>(stage);
       if (wait_full(bar_full + 8 * s, ph, alive)) {
-        // Groups gl = r, r + kWarps, ... of the chunk; r alternates between
+        // Groups gl = r, r + kBinWarps, ... of the chunk; r alternates between
         // the two halves of the warp range from tile to tile, so a warp's
         // share evens out over two tiles. x-table loads only in the lanes of
         // real columns (the others keep stale values, and their columns are
         // not stored).
-        const int r = (warp + (kWarps / 2) * (tcount & 1)) % kWarps;
-        for (int gl = r; gl < cg; gl += kWarps) {
+        const int r = (warp + (kBinWarps / 2) * (tcount & 1)) % kBinWarps;
+        for (int gl = r; gl < cg; gl += kBinWarps) {
           const int gi = c * (kChunk / 16) + gl;
           const uint32_t w0 = stg[g * pw + gl * 4 + q];
           const uint32_t w1 = stg[(g + 8) * pw + gl * 4 + q];
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
       if (++s == p.stages) { s = 0; ph ^= 1; }
     }
-    float* red = partial_slot(p, smem, red_full, tcount, alive);
+    float* red = partial_slot<kBinWarps>(p, smem, red_full, tcount, alive);
     red[(warp * 16 + g) * 8 + 2 * q] = yacc[0];
     red[(warp * 16 + g) * 8 + 2 * q + 1] = yacc[1];
     red[(warp * 16 + g + 8) * 8 + 2 * q] = yacc[2];
@@ -422,7 +427,7 @@ __host__ __device__ constexpr int round_first_group(int r) { return (80 * r) >> 
 __host__ __device__ constexpr int round_last_group(int r) { return (80 * r + 79) >> 7; }
 
 // the super-group's 8 rounds are split over kTerParts warps
-constexpr int kTerParts = kWarps / 8;
+constexpr int kTerParts = kTerWarps / 8;
 static_assert(kTerParts == 2 || kTerParts == 4, "8 rounds over 2 or 4 warps");
 
 struct TerDigits {
@@ -449,7 +454,7 @@ __device__ __forceinline__ void ter_range(Fetch& fetch, Round& round, Epi& epi) 
 // digit i at bits 2i..2i+1. Independent of x, so it is built before the
 // wait for the previous grid.
 __device__ void build_byte_table(uint8_t* smem) {
-  for (int e = threadIdx.x; e < 256; e += kWarps * 32) {
+  for (int e = threadIdx.x; e < 256; e += kTerWarps * 32) {
     uint32_t v = 0;
     if (e < 243) {
       int r = e;
@@ -468,7 +473,7 @@ __device__ void build_byte_table(uint8_t* smem) {
 // (bytes 4 (4 rnd + q) + 0..3), read from global memory as 5 x 8 bytes.
 __device__ void build_ternary_xtable(const Params& p, uint8_t* smem) {
   const int per_token = p.n_sg * 64;
-  for (int t = threadIdx.x; t < p.m * per_token; t += kWarps * 32) {
+  for (int t = threadIdx.x; t < p.m * per_token; t += kTerWarps * 32) {
     const int col = t / per_token, it = t - col * per_token;
     const int q = it & 3, side = (it >> 2) & 1, rnd = (it >> 3) & 7, sg = it >> 6;
     const int k0 = 640 * sg + 80 * rnd + 20 * q;
@@ -502,7 +507,7 @@ __device__ void build_ternary_xtable(const Params& p, uint8_t* smem) {
 }
 
 template <bool SC>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(kTerWarps), 1)
     gemv_ternary_kernel(const __grid_constant__ CUtensorMap tmw,
                         const __grid_constant__ CUtensorMap tms, const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -510,21 +515,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
   const uint32_t red_full = bar_full + 16 * kMaxStages;
-  init_barriers(bar_full, bar_empty, p.stages);
+  init_barriers<kTerWarps>(bar_full, bar_empty, p.stages);
   __syncthreads();
   pdl_launch_dependents();
-  if (warp == kProducer) {
+  if (warp == kTerWarps) {
     if (lane == 0) produce(&tmw, &tms, p, sbase, bar_full, bar_empty);
     return;
   }
-  if (warp == kReducer) {
-    reducer(p, smem, red_full, lane);
+  if (warp == kTerWarps + 1) {
+    reducer<kTerWarps>(p, smem, red_full, lane);
     return;
   }
   build_byte_table(smem);
   pdl_wait();  // x is written by earlier work on the stream
   build_ternary_xtable(p, smem);
-  named_bar_sync(1, kWarps * 32);
+  named_bar_sync(1, kTerWarps * 32);
 
   const int g = lane >> 2, q = lane & 3;
   const bool bcol = (g >> 1) < p.m;  // B column g = token g>>1, side g&1
@@ -624,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
       if (++s == p.stages) { s = 0; ph ^= 1; }
     }
-    float* red = partial_slot(p, smem, red_full, tcount, alive);
+    float* red = partial_slot<kTerWarps>(p, smem, red_full, tcount, alive);
     red[(warp * 16 + g) * 8 + q] = yacc[0];
     red[(warp * 16 + g + 8) * 8 + q] = yacc[1];
     partial_done(red_full, tcount, lane);
@@ -679,7 +684,8 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
   int off = 0;
   p.off_lut = off;   if (ter) off = up(off + kLutBytes, 128);  // at 0: the kernel relies on it
   p.off_bar = off;   off = up(off + 8 * (2 * kMaxStages + 4), 128);
-  p.off_red = off;   off = up(off + 2 * kWarps * 16 * 8 * 4, 128);
+  const int warps = ter ? kTerWarps : kBinWarps;
+  p.off_red = off;   off = up(off + 2 * warps * 16 * 8 * 4, 128);
   p.off_t = off;     if (!ter) off = up(off + p.G * 8 * 4, 128);
   p.off_xt = off;    off = up(off + p.m * p.xt_stride, 1024);
   p.off_stage = off;
@@ -715,7 +721,7 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
   const int sms = device_sm_count();
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.tiles < sms ? p.tiles : sms);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(warps));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -37,10 +37,13 @@ __global__ void pack_binary_kernel(const int8_t* __restrict__ codes, long long r
       const uint32_t u[8] = {(uint32_t)v0.x, (uint32_t)v0.y, (uint32_t)v0.z, (uint32_t)v0.w,
                              (uint32_t)v1.x, (uint32_t)v1.y, (uint32_t)v1.z, (uint32_t)v1.w};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t c = (u[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-        if (c == 0x01u) word |= 1u << i;
-        else if (c != 0xFFu) bad = true;
+      for (int i = 0; i < 8; ++i) {
+        // +1 is 0x01 and -1 is 0xFF: the code bit is the inverted sign bit of
+        // each byte; one multiply gathers the four sign bits into bits 28..31
+        const uint32_t sgn = ~u[i] & 0x80808080u;
+        word |= ((sgn * 0x00204081u) >> 28) << (4 * i);
+        const uint32_t expect = ((u[i] >> 7) & 0x01010101u) * 0xFEu + 0x01010101u;
+        bad |= u[i] != expect;
       }
     }
     out[t] = word;
@@ -48,27 +51,75 @@ __global__ void pack_binary_kernel(const int8_t* __restrict__ codes, long long r
   if (bad) set_status(BONSAI_ERR_BAD_CODE);
 }
 
-// One thread per output byte.
+// Digit bytes (code + 1) of four int8 codes, with a carry-free byte add;
+// a code outside {-1,0,+1} gives a digit above 2.
+__device__ __forceinline__ uint32_t digits4(uint32_t w) {
+  return ((w & 0x7F7F7F7Fu) + 0x01010101u) ^ (w & 0x80808080u);
+}
+
+// One thread per 16 output bytes (80 codes, five 16-byte loads). Output byte
+// b = d0 + 3 d1 + 9 d2 + 27 d3 + 81 d4 of its five digit bytes: a byte
+// permute gathers d0..d3 and one 4-way byte dot product weighs them.
 __global__ void pack_ternary_kernel(const int8_t* __restrict__ codes, long long rows, int k,
                                     uint8_t* __restrict__ out, int row_bytes) {
-  const long long total = rows * (long long)row_bytes;
+  const int chunks = row_bytes / 16;
+  const long long total = rows * (long long)chunks;
   bool bad = false;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
        t += (long long)gridDim.x * blockDim.x) {
-    const long long r = t / row_bytes;
-    const int b = (int)(t - r * row_bytes);
-    int value = 0;
+    const long long r = t / chunks;
+    const int j = (int)(t - r * chunks);
+    const int k0 = 80 * j;
+    uint32_t d[21];
+    if (k0 + 80 <= k) {
+      const int4* src = reinterpret_cast<const int4*>(codes + r * k + k0);
 #pragma unroll
-    for (int i = 4; i >= 0; --i) {
-      const int kk = 5 * b + i;
-      int c = 0;
-      if (kk < k) {
-        c = codes[r * k + kk];
-        if (c < -1 || c > 1) { bad = true; c = 0; }
+      for (int i = 0; i < 5; ++i) {
+        const int4 v = src[i];
+        d[4 * i] = digits4((uint32_t)v.x);
+        d[4 * i + 1] = digits4((uint32_t)v.y);
+        d[4 * i + 2] = digits4((uint32_t)v.z);
+        d[4 * i + 3] = digits4((uint32_t)v.w);
       }
-      value = 3 * value + (c + 1);
+#pragma unroll
+      for (int i = 0; i < 20; ++i)  // a digit byte above 2: bits above 1 set, or both low bits
+        bad |= ((d[i] & 0xFCFCFCFCu) | (d[i] & (d[i] >> 1) & 0x01010101u)) != 0u;
+    } else {  // row tail and padding: codes past k are zero codes (digit 1)
+#pragma unroll
+      for (int i = 0; i < 20; ++i) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kk = k0 + 4 * i + e;
+          int c = 0;
+          if (kk < k) {
+            c = codes[r * k + kk];
+            if (c < -1 || c > 1) { bad = true; c = 0; }
+          }
+          v |= uint32_t(c + 1) << (8 * e);
+        }
+        d[i] = v;
+      }
     }
-    out[t] = (uint8_t)value;
+    d[20] = 0;
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int b = 4 * q + e;      // output byte within the chunk
+        const int p = 5 * b;          // its first digit byte
+        const int w0 = p >> 2, o0 = p & 3;
+        const uint32_t lo4 = __byte_perm(d[w0], d[w0 + 1],
+                                         o0 | ((o0 + 1) << 4) | ((o0 + 2) << 8) | ((o0 + 3) << 12));
+        const uint32_t d4 = (d[(p + 4) >> 2] >> (8 * ((p + 4) & 3))) & 0xFFu;
+        const uint32_t value = (uint32_t)__dp4a(lo4, 0x1B090301u, 81u * d4);
+        word |= (value & 0xFFu) << (8 * e);
+      }
+      o[q] = word;
+    }
+    *reinterpret_cast<uint4*>(out + r * row_bytes + 16LL * j) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (bad) set_status(BONSAI_ERR_BAD_CODE);
 }
@@ -94,7 +145,7 @@ bonsai_status pack_binary_launch(const int8_t* codes, int64_t rows, int64_t k, v
 
 bonsai_status pack_ternary_launch(const int8_t* codes, int64_t rows, int64_t k, void* out,
                                   int64_t row_bytes, cudaStream_t stream) {
-  const long long items = rows * (long long)row_bytes;
+  const long long items = rows * (long long)(row_bytes / 16);
   if (items == 0) return BONSAI_OK;
   pack_ternary_kernel<<<grid_for(items, 256), 256, 0, stream>>>(
       codes, rows, (int)k, static_cast<uint8_t*>(out), (int)row_bytes);
