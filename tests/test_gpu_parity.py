@@ -100,6 +100,8 @@ GEMV_CASES = [
     (TER, 17408, 5120),   # ternary decode workload (M=1, K=5120, N=17408)
     (TER, 1, 128), (TER, 17, 640), (TER, 33, 5120), (TER, 40, 17408),
     (TER, 5120, 17408), (TER, 300, 1280), (TER, 129, 384),
+    # the decode sweep's stacked q/k/v and gate/up matrices
+    (BIN, 15360, 5120), (TER, 15360, 5120), (BIN, 34816, 5120), (TER, 34816, 5120),
 ]
 
 
