@@ -57,6 +57,8 @@ def configure(L):
     L.oracle_linear.argtypes = [C.c_int, P, I64, P, I64, I64, P, I64,
                                 P, I64, P, I64, P, P]
     L.oracle_linear.restype = C.c_int
+    L.oracle_binarize.argtypes = [P, I64, I64, P, P]
+    L.oracle_binarize.restype = C.c_int
     L.oracle_xnor.argtypes = [P, P, I64, P, I64, P, I64, I64,
                               P, I64, P, I64, P, P, P]
     L.oracle_xnor.restype = C.c_int
@@ -183,6 +185,17 @@ def xnor(a_bits: np.ndarray, a_scale: np.ndarray, w_packed: np.ndarray,
                              _p(scales), n, k, _p(n_sel), len(n_sel), _p(m_sel), len(m_sel),
                              _p(d), _p(y), _p(nrm)), "xnor")
     return d, y, nrm
+
+
+def binarize(x: np.ndarray):
+    """(bits uint32 [m][k/32], a_scale float64 [m]) of FP16 rows x [m][k]:
+    bit 1 where x >= 0, a_scale = mean |x| per row."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    m, k = x.shape
+    bits = np.zeros((m, k // 32), dtype=np.uint32)
+    a_s = np.empty(m, dtype=np.float64)
+    _check(lib().oracle_binarize(_p(x), m, k, _p(bits), _p(a_s)), "binarize")
+    return bits, a_s
 
 
 def compare_f16(y_gpu: np.ndarray, y_ref: np.ndarray, norm: np.ndarray,

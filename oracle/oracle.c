@@ -18,6 +18,8 @@
  *   integers (not from popcount), so the popcount identity used on the GPU
  *   is checked rather than assumed;
  *   Y[m][n] = a_s[m] * sum_g s[n][g] * d_g,  d_g = sum_{k in g} a*w.
+ * Activation binarisation (this library's reading; the pages give no rule):
+ *   a = sign(x) with sign(0) = +1, a_s = mean |x| over the row.
  *
  * Byte layout (this library's reading; the pages give none):
  *   binary : bit (k % 32) of little-endian uint32 word k/32, bit 1 = +1.
@@ -247,6 +249,38 @@ int oracle_xnor(const uint8_t* a_bits, const uint16_t* a_scale, int64_t m,
   }
   free(a);
   free(w);
+  return st;
+}
+
+/* Activation binarisation, the A side of the XNOR product ("1-bit 嘅數學":
+ * XOR + popcount needs both operands as +-1 bits). The pages say neither how
+ * an FP16 activation row becomes +-1 codes nor which scale goes with it; this
+ * library's reading:
+ *   a[m][k]  = +1 if x[m][k] >= 0 (so +0 and -0 give +1), else -1;
+ *              a NaN compares false and gives -1,
+ *   a_s[m]   = (1/K) * sum_k |x[m][k]|,
+ * the scale alpha that minimises sum_k (x[m][k] - alpha * a[m][k])^2 for these
+ * codes (setting the derivative to zero: alpha * K = sum_k a*x = sum_k |x|).
+ * bits is [m][k/8] bytes in the binary weight layout; a_scale is [m], exact
+ * up to one rounding of the double sum. */
+int oracle_binarize(const uint16_t* x, int64_t m, int64_t k, uint8_t* bits,
+                    double* a_scale) {
+  if (!x || !bits || !a_scale || m < 0 || k <= 0) return O_ERR_ARG;
+  if (k % 32) return O_ERR_SHAPE;
+  int8_t* a = (int8_t*)malloc((size_t)k);
+  if (!a) return O_ERR_ARG;
+  int st = O_OK;
+  for (int64_t r = 0; r < m && st == O_OK; ++r) {
+    double sum = 0.0;
+    for (int64_t kk = 0; kk < k; ++kk) {
+      const double v = oracle_half_to_double(x[r * k + kk]);
+      a[kk] = (v >= 0.0) ? 1 : -1;
+      sum += fabs(v);
+    }
+    a_scale[r] = sum / (double)k;
+    st = oracle_pack_binary(a, 1, k, bits + r * (k / 8), k / 8);
+  }
+  free(a);
   return st;
 }
 

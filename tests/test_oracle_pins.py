@@ -301,6 +301,60 @@ def pin_xnor():
     assert d3[0, 0] == -k and d3[1, 1] == -k
 
 
+def pin_binarize():
+    # closed form: the ramp x_k = (k - 63.5)/64 over one group is exact in
+    # FP16; its first 64 entries are negative and sum |x| = 4096/64 = 64.
+    k = 128
+    ramp = ((np.arange(k) - 63.5) / 64).astype(np.float16)
+    assert np.array_equal(ramp.astype(np.float64), (np.arange(k) - 63.5) / 64)
+    bits, a_s = oracle.binarize(ramp.view(np.uint16)[None])
+    assert bits.dtype == np.uint32 and bits.shape == (1, 4)
+    assert list(bits[0]) == [0, 0, 0xFFFFFFFF, 0xFFFFFFFF]
+    assert a_s[0] == 0.5
+    # constant rows, and both zeros counting as +1 with a zero scale
+    c = np.float16(0.3125)
+    rows = np.stack([np.full(256, c), np.full(256, -c), np.zeros(256, np.float16),
+                     np.full(256, np.float16(-0.0))]).astype(np.float16)
+    assert np.signbit(rows[3]).all()
+    bits, a_s = oracle.binarize(rows.view(np.uint16))
+    assert np.all(bits[0] == 0xFFFFFFFF) and np.all(bits[1] == 0)
+    assert np.all(bits[2] == 0xFFFFFFFF) and np.all(bits[3] == 0xFFFFFFFF)
+    assert list(a_s) == [0.3125, 0.3125, 0.0, 0.0]
+    # one negative entry clears exactly its own bit
+    for pos in (0, 31, 32, 200):
+        row = np.full((1, 256), np.float16(1.5))
+        row[0, pos] = -2.0
+        bits, a_s = oracle.binarize(row.astype(np.float16).view(np.uint16))
+        expect = np.full(8, 0xFFFFFFFF, dtype=np.uint32)
+        expect[pos // 32] ^= np.uint32(1) << np.uint32(pos % 32)
+        assert np.array_equal(bits[0], expect) and a_s[0] == (255 * 1.5 + 2.0) / 256
+    # a NaN compares false: code -1, and the scale is NaN
+    row = np.ones((1, 128), np.float16)
+    row[0, 5] = np.nan
+    bits, a_s = oracle.binarize(row.view(np.uint16))
+    assert bits[0, 0] == 0xFFFFFFFF ^ (1 << 5) and math.isnan(a_s[0])
+    # invariants on random rows: the codes agree in sign with x, and the scale
+    # is the least-squares one -- zero derivative of sum (x - alpha a)^2 and a
+    # larger error on either side of it
+    m, k = 5, 1024
+    x = rand_x(21, m, k)
+    bits, a_s = oracle.binarize(x)
+    a = np_decode_binary(bits.view(np.uint8).reshape(m, -1), k).astype(np.float64)
+    xv = f16(x)
+    assert np.all(a * xv >= 0) and np.all(a[xv == 0] == 1)
+    for i in range(m):
+        err = lambda al: float(((xv[i] - al * a[i]) ** 2).sum())
+        grad = float((a[i] * (xv[i] - a_s[i] * a[i])).sum())
+        assert abs(grad) <= 1e-9 * np.abs(xv[i]).sum()
+        assert err(a_s[i]) < err(a_s[i] * 1.001) and err(a_s[i]) < err(a_s[i] * 0.999)
+    # composed with the XNOR product: weights equal to the codes give D = K
+    s = synth.gen_scales(22, m, k)
+    one = np.full(m, np.float16(1.0).view(np.uint16), dtype=np.uint16)
+    d, y, _ = oracle.xnor(bits, one, bits, s, k)
+    assert np.all(np.diag(d) == k)
+    assert np.allclose(np.diag(y), 128 * f16(s).sum(axis=1), rtol=1e-12, atol=0)
+
+
 def pin_compare_rule():
     ref = np.array([1.0, 1.0, 0.0, 1.0, 1.0])
     nrm = np.array([10.0, 10.0, 0.0, 10.0, 10.0])
@@ -320,7 +374,7 @@ PINS = [pin_half_to_double, pin_row_bytes, pin_page_sizes, pin_binary_round_trip
         pin_ternary_round_trip_and_padding, pin_bad_codes,
         pin_all_plus_constant_scale, pin_group_scales, pin_zero_ternary,
         pin_flip_and_scale, pin_single_weight, pin_brute_force, pin_xnor,
-        pin_compare_rule]
+        pin_binarize, pin_compare_rule]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -348,6 +402,10 @@ MUTANTS = {
     "xnor_group_scale": ("acc += sg * (double)dg;", "acc += sg * (double)total;"),
     "xnor_sign": ("dg += (int64_t)a[kk] * (int64_t)w[kk];", "dg -= (int64_t)a[kk] * (int64_t)w[kk];"),
     "ter_pad_bytes": ("return 64 * ((data + 63) / 64);", "return 16 * ((data + 15) / 16);"),
+    "binarize_zero_sign": ("a[kk] = (v >= 0.0) ? 1 : -1;", "a[kk] = (v > 0.0) ? 1 : -1;"),
+    "binarize_no_abs": ("sum += fabs(v);", "sum += v;"),
+    "binarize_squares": ("sum += fabs(v);", "sum += v * v;"),
+    "binarize_divisor": ("a_scale[r] = sum / (double)k;", "a_scale[r] = sum / (double)(k - 1);"),
     "ter_bad_byte": ("if (value > 242) return O_ERR_BAD_CODE;", "if (value > 255) return O_ERR_BAD_CODE;"),
 }
 
