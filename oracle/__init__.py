@@ -57,6 +57,9 @@ def configure(L):
     L.oracle_linear.argtypes = [C.c_int, P, I64, P, I64, I64, P, I64,
                                 P, I64, P, I64, P, P]
     L.oracle_linear.restype = C.c_int
+    L.oracle_swiglu.argtypes = [C.c_int, P, I64, P, I64, I64, P, I64, P, I64, P, I64,
+                                P, P, P, P, P]
+    L.oracle_swiglu.restype = C.c_int
     L.oracle_binarize.argtypes = [P, I64, I64, P, P]
     L.oracle_binarize.restype = C.c_int
     L.oracle_xnor.argtypes = [P, P, I64, P, I64, P, I64, I64,
@@ -185,6 +188,29 @@ def xnor(a_bits: np.ndarray, a_scale: np.ndarray, w_packed: np.ndarray,
                              _p(scales), n, k, _p(n_sel), len(n_sel), _p(m_sel), len(m_sel),
                              _p(d), _p(y), _p(nrm)), "xnor")
     return d, y, nrm
+
+
+def swiglu(fmt: int, packed: np.ndarray, scales: np.ndarray, x: np.ndarray,
+           f_sel=None, m_sel=None):
+    """Gated feed-forward input h = silu(g) * u of the interleaved gate/up
+    matrix packed [2F][row_bytes] (16-row blocks: 8 gate rows, then the 8 up
+    rows of the same features). Returns (h, g, u, norm_g, norm_u), each
+    [len(m_sel)][len(f_sel)] float64."""
+    packed = np.ascontiguousarray(packed)
+    n = packed.shape[0]
+    pb = packed.view(np.uint8).reshape(n, -1)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    m, k = x.shape
+    f_sel = np.arange(n // 2, dtype=np.int64) if f_sel is None else np.ascontiguousarray(f_sel, dtype=np.int64)
+    m_sel = np.arange(m, dtype=np.int64) if m_sel is None else np.ascontiguousarray(m_sel, dtype=np.int64)
+    outs = [np.empty((len(m_sel), len(f_sel)), dtype=np.float64) for _ in range(5)]
+    _check(lib().oracle_swiglu(fmt, _p(pb), pb.shape[1], _p(scales), n, k, _p(x), m,
+                               _p(f_sel), len(f_sel), _p(m_sel), len(m_sel),
+                               *[_p(o) for o in outs]), "swiglu")
+    return tuple(outs)
 
 
 def binarize(x: np.ndarray):

@@ -205,6 +205,58 @@ int oracle_linear(int fmt, const uint8_t* packed, int64_t row_bytes,
   return O_OK;
 }
 
+/* Gated feed-forward input of a decode layer: the gate and up projections
+ * of the same x, stored as ONE weight matrix of n = 2F rows whose 16-row
+ * blocks hold 8 gate rows then the 8 up rows of the same features:
+ *   gate row f -> stored row 16*(f/8) + f%8,  up row f -> that row + 8.
+ * The pages run Qwen-family models (OpenBonsai page: Qwen3.5-9B) but do not
+ * write the feed-forward block out; this library takes the SwiGLU form of
+ * that family:
+ *   g = x . (s (.) W_gate)^T,  u = x . (s (.) W_up)^T,
+ *   h[m][f] = silu(g) * u,     silu(g) = g / (1 + exp(-g)).
+ * h, g, u, norm_g, norm_u are [m_cnt][f_cnt]; norm_* are sum |x*s*w| of the
+ * gate and up rows (the error scale of g and u). */
+int oracle_swiglu(int fmt, const uint8_t* packed, int64_t row_bytes,
+                  const uint16_t* scales, int64_t n, int64_t k,
+                  const uint16_t* x, int64_t m,
+                  const int64_t* f_sel, int64_t f_cnt,
+                  const int64_t* m_sel, int64_t m_cnt,
+                  double* h, double* g, double* u, double* norm_g, double* norm_u) {
+  if (!f_sel || !h || !g || !u || !norm_g || !norm_u) return O_ERR_ARG;
+  if (n <= 0 || n % 16) return O_ERR_SHAPE;
+  const int64_t F = n / 2;
+  int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(2 * f_cnt + 1));
+  double* y = (double*)malloc(sizeof(double) * (size_t)(2 * f_cnt * m_cnt + 1));
+  double* nr = (double*)malloc(sizeof(double) * (size_t)(2 * f_cnt * m_cnt + 1));
+  if (!rows || !y || !nr) { free(rows); free(y); free(nr); return O_ERR_ARG; }
+  int st = O_OK;
+  for (int64_t j = 0; j < f_cnt; ++j) {
+    const int64_t f = f_sel[j];
+    if (f < 0 || f >= F) { st = O_ERR_ARG; break; }
+    rows[j] = 16 * (f / 8) + f % 8;      /* gate */
+    rows[f_cnt + j] = rows[j] + 8;       /* up   */
+  }
+  if (st == O_OK)
+    st = oracle_linear(fmt, packed, row_bytes, scales, n, k, x, m, rows, 2 * f_cnt, m_sel,
+                       m_cnt, y, nr);
+  if (st == O_OK) {
+    for (int64_t i = 0; i < m_cnt; ++i)
+      for (int64_t j = 0; j < f_cnt; ++j) {
+        const double gv = y[i * 2 * f_cnt + j], uv = y[i * 2 * f_cnt + f_cnt + j];
+        const int64_t o = i * f_cnt + j;
+        g[o] = gv;
+        u[o] = uv;
+        norm_g[o] = nr[i * 2 * f_cnt + j];
+        norm_u[o] = nr[i * 2 * f_cnt + f_cnt + j];
+        h[o] = gv / (1.0 + exp(-gv)) * uv;
+      }
+  }
+  free(rows);
+  free(y);
+  free(nr);
+  return st;
+}
+
 /* d, y, norm are [m_cnt][n_cnt]. a_bits rows are BINARY-packed, k/8 bytes. */
 int oracle_xnor(const uint8_t* a_bits, const uint16_t* a_scale, int64_t m,
                 const uint8_t* w_packed, int64_t row_bytes,

@@ -355,6 +355,62 @@ def pin_binarize():
     assert np.allclose(np.diag(y), 128 * f16(s).sum(axis=1), rtol=1e-12, atol=0)
 
 
+def interleave_rows(gate, up):
+    """[F][...] gate and up rows -> [2F][...], 16-row blocks of 8 gate rows
+    followed by the 8 up rows of the same features (numpy reshapes only)."""
+    f = gate.shape[0]
+    g = gate.reshape(f // 8, 1, 8, *gate.shape[1:])
+    u = up.reshape(f // 8, 1, 8, *up.shape[1:])
+    return np.concatenate([g, u], axis=1).reshape(2 * f, *gate.shape[1:])
+
+
+def pin_swiglu():
+    # the stored-row mapping: g and u are the products of the separate matrices
+    f, k, m = 24, 256, 3
+    x = rand_x(31, m, k)
+    for fmt in (BIN, TER):
+        if fmt == BIN:
+            gp = synth.gen_binary_words(32, f, k).view(np.uint8).reshape(f, -1)
+            up = synth.gen_binary_words(33, f, k).view(np.uint8).reshape(f, -1)
+        else:
+            gp = oracle.pack_ternary(synth.gen_ternary_codes(32, f, k))
+            up = oracle.pack_ternary(synth.gen_ternary_codes(33, f, k))
+        gs, us = synth.gen_scales(34, f, k), synth.gen_scales(35, f, k)
+        h, g, u, ng, nu = oracle.swiglu(fmt, interleave_rows(gp, up), interleave_rows(gs, us), x)
+        g_ref, ng_ref = oracle.linear(fmt, gp, gs, x)
+        u_ref, nu_ref = oracle.linear(fmt, up, us, x)
+        assert np.array_equal(g, g_ref) and np.array_equal(u, u_ref)
+        assert np.array_equal(ng, ng_ref) and np.array_equal(nu, nu_ref)
+        # silu(g) - silu(-g) = g: flipping every gate weight changes h by g*u
+        if fmt == BIN:
+            h2, g2, _, _, _ = oracle.swiglu(fmt, interleave_rows(~gp, up), interleave_rows(gs, us), x)
+            assert np.array_equal(g2, -g)
+            assert np.allclose(h - h2, g * u, rtol=0, atol=1e-12 * np.abs(g * u).max())
+        sel_h, _, _, _, _ = oracle.swiglu(fmt, interleave_rows(gp, up), interleave_rows(gs, us), x,
+                                          f_sel=[f - 1, 0, 9], m_sel=[2, 0])
+        assert np.array_equal(sel_h, h[np.ix_([2, 0], [f - 1, 0, 9])])
+    # closed forms: x = 2^-7 everywhere and unit scales give g = +-1 over one
+    # group of +-1 weights; sigma(1) = 1/(1 + 1/e) = 0.7310585786300049
+    k, f = 128, 8
+    x = np.full((1, k), np.float16(2.0 ** -7).view(np.uint16), dtype=np.uint16)
+    ones = np.full((f, 1), np.float16(1.0).view(np.uint16), dtype=np.uint16)
+    plus = np.full((f, k // 8), 0xFF, dtype=np.uint8)
+    minus = np.zeros((f, k // 8), dtype=np.uint8)
+    h, g, u, _, _ = oracle.swiglu(BIN, interleave_rows(plus, minus), interleave_rows(ones, ones), x)
+    assert np.all(g == 1.0) and np.all(u == -1.0)
+    assert np.allclose(h, -0.7310585786300049, rtol=1e-15, atol=0)
+    h, g, u, _, _ = oracle.swiglu(BIN, interleave_rows(minus, plus), interleave_rows(ones, ones), x)
+    assert np.allclose(h, -1.0 * (1.0 - 0.7310585786300049), rtol=1e-14, atol=0)
+    # a large gate passes through (sigma = 1 in double), a zero gate gives 0
+    big = np.full((f, 1), np.float16(64.0).view(np.uint16), dtype=np.uint16)
+    h, g, u, _, _ = oracle.swiglu(BIN, interleave_rows(plus, plus), interleave_rows(big, ones), x)
+    assert np.all(g == 64.0) and np.all(u == 1.0) and np.all(h == 64.0)
+    zero = oracle.pack_ternary(np.zeros((f, k), dtype=np.int8))
+    tplus = oracle.pack_ternary(np.ones((f, k), dtype=np.int8))
+    h, g, u, ng, _ = oracle.swiglu(TER, interleave_rows(zero, tplus), interleave_rows(ones, ones), x)
+    assert np.all(h == 0.0) and np.all(ng == 0.0) and np.all(u == 1.0)
+
+
 def pin_compare_rule():
     ref = np.array([1.0, 1.0, 0.0, 1.0, 1.0])
     nrm = np.array([10.0, 10.0, 0.0, 10.0, 10.0])
@@ -374,7 +430,7 @@ PINS = [pin_half_to_double, pin_row_bytes, pin_page_sizes, pin_binary_round_trip
         pin_ternary_round_trip_and_padding, pin_bad_codes,
         pin_all_plus_constant_scale, pin_group_scales, pin_zero_ternary,
         pin_flip_and_scale, pin_single_weight, pin_brute_force, pin_xnor,
-        pin_binarize, pin_compare_rule]
+        pin_binarize, pin_swiglu, pin_compare_rule]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -406,6 +462,10 @@ MUTANTS = {
     "binarize_no_abs": ("sum += fabs(v);", "sum += v;"),
     "binarize_squares": ("sum += fabs(v);", "sum += v * v;"),
     "binarize_divisor": ("a_scale[r] = sum / (double)k;", "a_scale[r] = sum / (double)(k - 1);"),
+    "swiglu_sign": ("h[o] = gv / (1.0 + exp(-gv)) * uv;", "h[o] = gv / (1.0 + exp(gv)) * uv;"),
+    "swiglu_swapped": ("h[o] = gv / (1.0 + exp(-gv)) * uv;", "h[o] = uv / (1.0 + exp(-uv)) * gv;"),
+    "swiglu_block": ("rows[j] = 16 * (f / 8) + f % 8;", "rows[j] = 8 * (f / 8) + f % 8;"),
+    "swiglu_up_offset": ("rows[f_cnt + j] = rows[j] + 8;", "rows[f_cnt + j] = rows[j] + 1;"),
     "ter_bad_byte": ("if (value > 242) return O_ERR_BAD_CODE;", "if (value > 255) return O_ERR_BAD_CODE;"),
 }
 
