@@ -351,11 +351,14 @@ SWEEP_SHAPES = [(15360, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]  # qk
 
 class SweepWorkload:
     """64-layer decode: 4 products per layer (q/k/v and gate/up stacked),
-    256 per token, weights resident."""
+    256 per token, weights resident. With fused=True the gate/up product
+    applies silu(g)*u in its epilogue and the down product reads that h
+    (the feed-forward chain of a layer); otherwise every product reads a
+    fixed x of its K."""
     kind = "sweep"
 
-    def __init__(self, fmt, name, layers=64):
-        self.fmt, self.name, self.layers = fmt, name, layers
+    def __init__(self, fmt, name, layers=64, fused=False):
+        self.fmt, self.name, self.layers, self.fused = fmt, name, layers, fused
 
     def unit_bytes(self):
         return self.layers * sum(weight_bytes(self.fmt, n, k) for n, k in SWEEP_SHAPES)
@@ -374,13 +377,20 @@ class SweepWorkload:
         self.x = {k: torch.from_numpy(synth.gen_x(seed + k, 1, k).view(np.float16)[0].copy()).cuda()
                   for k in (5120, 17408)}
         self.y = {n: torch.empty(n, dtype=torch.float16, device="cuda") for n, _ in SWEEP_SHAPES}
+        self.h = torch.empty(SWEEP_SHAPES[2][0] // 2, dtype=torch.float16, device="cuda")
         torch.cuda.synchronize()
         sb.check()
 
     def token(self):
         import sub_bit_weight_binary_b300 as sb
-        for w in self.w:
-            sb.bonsai_gemv(w, self.x[w.k], self.y[w.n])
+        for i, w in enumerate(self.w):
+            j = i % len(SWEEP_SHAPES)
+            if self.fused and j == 2:
+                sb.bonsai_gemm_swiglu(w, self.x[w.k], self.h)
+            elif self.fused and j == 3:
+                sb.bonsai_gemv(w, self.h, self.y[w.n])
+            else:
+                sb.bonsai_gemv(w, self.x[w.k], self.y[w.n])
 
     def launches(self, start, count):
         for _ in range(count):
@@ -429,6 +439,8 @@ class SweepWorkload:
         return {"workload": self.name, "layers": self.layers,
                 "shapes_nk": SWEEP_SHAPES, "format": "ternary" if self.fmt == 2 else "binary",
                 "stacked": "q/k/v and gate/up weights stored stacked, one product each",
+                "ffn": ("gate/up product writes silu(g)*u; down product reads it" if self.fused
+                        else "every product reads a fixed x"),
                 "timing": "one CUDA graph per token (%d launches), replayed per step" % (
                     self.layers * len(SWEEP_SHAPES)),
                 "l2": "inputs larger than L2: %.2f GB of weights per token" % (self.unit_bytes() / 1e9)}
@@ -502,6 +514,63 @@ class GemmWorkload:
                 "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
 
 
+class LayerGemmWorkload(GemmWorkload):
+    """One decoder layer of prompt processing on the tensor cores: the 7
+    weight products (q, k, v, o, gate, up, down) as 4 launches -- q/k/v and
+    gate/up stacked, silu(g)*u applied in the gate/up epilogue, the down
+    product reading that h. The o product reads the prompt x in place of an
+    attention output (attention itself is not a weight product)."""
+
+    def __init__(self, fmt, m, name):
+        super().__init__(fmt, m, name)
+
+    def flops(self):
+        return 2.0 * self.m * sum(n * k for n, k in SWEEP_SHAPES)
+
+    def setup(self):
+        import torch
+        import sub_bit_weight_binary_b300 as sb
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(4)
+        self.ws = []
+        for j, (n, k) in enumerate(SWEEP_SHAPES):
+            tid = synth.sweep_tid(0, j)
+            self.ws.append(make_weights(self.fmt, n, k, seed, tid, tid + 8, 0))
+        self.x = torch.from_numpy(synth.gen_x(seed, self.m, 5120).view(np.float16)).cuda()
+        self.h = torch.empty((self.m, SWEEP_SHAPES[2][0] // 2), dtype=torch.float16, device="cuda")
+        self.ys = [torch.empty((self.m, n), dtype=torch.float16, device="cuda") for n, _ in SWEEP_SHAPES]
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        sb.check()
+
+    def call(self):
+        import sub_bit_weight_binary_b300 as sb
+        qkv, o, gu, down = self.ws
+        sb.bonsai_gemm(qkv, self.x, self.ys[0])
+        sb.bonsai_gemm(o, self.x, self.ys[1])
+        sb.bonsai_gemm_swiglu(gu, self.x, self.h)
+        sb.bonsai_gemm(down, self.h, self.ys[3])
+
+    def measure(self, steps, warmup, clocks=None):
+        r = GemmWorkload.measure(self, steps, warmup, clocks)
+        r["launches"] = 4 * steps
+        return r
+
+    def roofline(self, r, pk):
+        a = self.flops() / (r["kernel_ms"] / 1e3) / 1e12
+        return {"bound": "tensor", "kernel": "gemm_kernel<%d> x4 (one layer)" % self.fmt,
+                "achieved": round(a, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": round(a / pk["bf16"], 4), "traffic": None,
+                "note": "whole layer step: 4 launches, achieved over their sum",
+                "peak_src": "%s dense bf16 cuBLAS burst (fp16 has the same dense rate)" % pk["src"]}
+
+    def config(self):
+        return {"workload": self.name, "m": self.m, "shapes_nk": SWEEP_SHAPES,
+                "format": "ternary" if self.fmt == 2 else "binary",
+                "ffn": "gate/up product writes silu(g)*u; down product reads it",
+                "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
+
+
 class XnorWorkload:
     kind = "xnor"
 
@@ -550,6 +619,67 @@ class XnorWorkload:
                 "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
 
 
+class XnorFp16Workload(XnorWorkload):
+    """XNOR product fed by FP16 activations: each step binarises x [m][k]
+    (sign codes + mean-|x| row scales) and then runs the XNOR-popcount GEMM."""
+    kind = "xnor"
+
+    def setup(self):
+        import torch
+        import sub_bit_weight_binary_b300 as sb
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(5)
+        x = synth.gen_x(seed, self.m, self.k)
+        w_bits = synth.gen_binary_words(seed + 1, self.n, self.k)
+        s = synth.gen_scales(seed + 2, self.n, self.k)
+        self.x = torch.from_numpy(x.view(np.float16)).cuda()
+        self.a = torch.empty((self.m, self.k // 32), dtype=torch.int32, device="cuda")
+        self.a_s = torch.empty(self.m, dtype=torch.float16, device="cuda")
+        self.w = sb.Weights(1, self.n, self.k,
+                            torch.from_numpy(w_bits.view(np.uint8).reshape(self.n, -1)).cuda(),
+                            torch.from_numpy(s.view(np.float16)).cuda())
+        self.d = torch.empty((self.m, self.n), dtype=torch.int32, device="cuda")
+        self.y = torch.empty((self.m, self.n), dtype=torch.float16, device="cuda")
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+
+    def binarize(self):
+        import sub_bit_weight_binary_b300 as sb
+        sb.bonsai_binarize_activations(self.x, self.a, self.a_s)
+
+    def call(self):
+        import sub_bit_weight_binary_b300 as sb
+        self.binarize()
+        sb.bonsai_xnor_gemm(self.a, self.a_s, self.w, self.d, self.y)
+
+    def measure(self, steps, warmup, clocks=None):
+        import torch
+        r = XnorWorkload.measure(self, steps, warmup, clocks)
+        r["launches"] = 2 * steps
+        # the binarisation kernel alone, same flush discipline
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            self.flush.zero_()
+            a.record()
+            self.binarize()
+            b.record()
+        torch.cuda.synchronize()
+        r["binarize_ms"] = sum(a.elapsed_time(b) for a, b in ev) / steps
+        return r
+
+    def roofline(self, r, pk, mhz=None):
+        out = XnorWorkload.roofline(self, r, pk, mhz)
+        out["traffic"] = None
+        out["note"] = ("achieved uses the whole step (binarisation + XNOR), a lower bound "
+                       "for the XNOR kernel alone")
+        nbytes = self.m * self.k * 2 + self.m * self.k // 8 + self.m * 2
+        out["binarize"] = {"ms": round(r["binarize_ms"], 6), "bytes": nbytes,
+                           "achieved_gbs": round(nbytes / (r["binarize_ms"] / 1e3) / 1e9, 1),
+                           "peak_gbs": pk["hbm"]}
+        return out
+
+
 WORKLOADS = {
     "ter_gemv": lambda: GemvWorkload(2, 17408, 5120, 2,
                                      "ternary GEMV M=1 K=5120 N=17408 (decode)"),
@@ -561,11 +691,23 @@ WORKLOADS = {
     "gemm512_ter": lambda: GemmWorkload(2, 512, "prefill GEMM M=512 K=5120 N=17408, ternary"),
     "gemm4096_bin": lambda: GemmWorkload(1, 4096, "DiT GEMM M=4096 K=5120 N=17408, binary"),
     "gemm4096_ter": lambda: GemmWorkload(2, 4096, "DiT GEMM M=4096 K=5120 N=17408, ternary"),
+    "layer_bin": lambda: SweepWorkload(1, "64-layer decode, fused feed-forward, binary, batch 1",
+                                       fused=True),
+    "layer_ter": lambda: SweepWorkload(2, "64-layer decode, fused feed-forward, ternary, batch 1",
+                                       fused=True),
+    "pp512_layer_bin": lambda: LayerGemmWorkload(1, 512, "prefill M=512, one decoder layer "
+                                                 "(7 products, fused feed-forward), binary"),
+    "pp512_layer_ter": lambda: LayerGemmWorkload(2, 512, "prefill M=512, one decoder layer "
+                                                 "(7 products, fused feed-forward), ternary"),
     "xnor": lambda: XnorWorkload("XNOR-popcount GEMM M=512 K=4096 N=4096"),
+    "xnor_fp16": lambda: XnorFp16Workload(
+        "FP16 activations binarised, then XNOR-popcount GEMM M=512 K=4096 N=4096"),
 }
 SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("sweep_bin", 30, 3), ("sweep_ter", 30, 3),
              ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
-             ("gemm4096_ter", 5, 2), ("xnor", 20, 3)]
+             ("gemm4096_ter", 5, 2), ("layer_bin", 30, 3), ("layer_ter", 30, 3),
+             ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("xnor", 20, 3),
+             ("xnor_fp16", 20, 3)]
 
 
 # -------------------------------------------------------------------- runs

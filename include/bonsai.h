@@ -172,6 +172,25 @@ bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t*
 bonsai_status bonsai_gemm(const bonsai_weights* w, const uint16_t* x,
                           int64_t m, uint16_t* y, bonsai_stream stream);
 
+/* Gated feed-forward input of a decode layer, gate and up projections in
+ * one pass over one weight matrix, with the SwiGLU product applied before
+ * the store:
+ *   h[m][f] = silu(g) * u,  silu(g) = g / (1 + e^-g),
+ *   g = x[m] . (s (.) W_gate[f]),  u = x[m] . (s (.) W_up[f]).
+ * The pages (OpenBonsai page: Qwen3.5-9B) run Qwen-family models, whose
+ * feed-forward block has this form; they do not write it out.
+ *   w  BINARY or TERNARY weights with n = 2F rows, F a multiple of 8, stored
+ *      interleaved in 16-row blocks: rows 16t..16t+7 are gate rows
+ *      8t..8t+7 and rows 16t+8..16t+15 are up rows 8t..8t+7 (scales in the
+ *      same row order). A tile of the product then holds both factors of
+ *      its outputs, and g and u never leave the chip.
+ *   x  device FP16 [m][k];  h: device FP16 [m][F] (the down projection's x).
+ * g and u are FP32 sums (as in bonsai_gemm); silu and the product are FP32,
+ * and h is rounded once to FP16. m <= 8 runs the streaming decode kernel,
+ * larger m the tensor-core GEMM. Returns BONSAI_ERR_SHAPE if n % 16 != 0. */
+bonsai_status bonsai_gemm_swiglu(const bonsai_weights* w, const uint16_t* x,
+                                 int64_t m, uint16_t* h, bonsai_stream stream);
+
 /* XNOR-popcount product of +-1 activations with +-1 weights ("1-bit 嘅數學":
  * binary GEMM via XOR + popcount).
  *   a_bits  device uint32 [m][k/32], same bit layout as BINARY weights
@@ -187,6 +206,27 @@ bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale,
                                int64_t m, const bonsai_weights* w,
                                int32_t* d_out, uint16_t* y_out,
                                bonsai_stream stream);
+
+/* Activation binarisation: the +-1 A operand of bonsai_xnor_gemm, made from
+ * FP16 activation rows in one pass over x. The pages ("1-bit 嘅數學") use
+ * XOR + popcount for +-1 operands but give no rule for the activation side;
+ * this library's rule is
+ *   code a[r][k] = +1 where x[r][k] >= 0 (+0 and -0 included; NaN gives -1),
+ *   scale a_s[r] = (1/k) * sum_k |x[r][k]|,
+ * the least-squares scale for those codes: it minimises
+ * sum_k (x[r][k] - a_s * a[r][k])^2.
+ *   x       device FP16 [m][k], row-major, 16-byte aligned.
+ *   m       rows, >= 1.  k: multiple of 128.
+ *   a_bits  device uint32 [m][k/32], written in the BINARY weight layout
+ *           (bit (k%32) of word k/32, bit 1 = +1), 16-byte aligned.
+ *   a_scale device FP16 [m] (round to nearest even of the FP32 mean of |x|;
+ *           within 2^-11 + k*2^-24 of the exact mean, relative), 16-byte
+ *           aligned.
+ * Codes are exact (no arithmetic decides them). A row holding a NaN gets a
+ * NaN scale; an infinite entry gives an infinite scale. */
+bonsai_status bonsai_binarize_activations(const uint16_t* x, int64_t m, int64_t k,
+                                          uint32_t* a_bits, uint16_t* a_scale,
+                                          bonsai_stream stream);
 
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: BONSAI_OK, BONSAI_ERR_BAD_CODE or BONSAI_ERR_TIMEOUT.

@@ -64,8 +64,12 @@ def lib():
         L.bonsai_gemv_splitk_static.restype = S
         L.bonsai_gemm.argtypes = [W, P, I64, P, P]
         L.bonsai_gemm.restype = S
+        L.bonsai_gemm_swiglu.argtypes = [W, P, I64, P, P]
+        L.bonsai_gemm_swiglu.restype = S
         L.bonsai_xnor_gemm.argtypes = [P, P, I64, W, P, P, P]
         L.bonsai_xnor_gemm.restype = S
+        L.bonsai_binarize_activations.argtypes = [P, I64, I64, P, P, P]
+        L.bonsai_binarize_activations.restype = S
         L.bonsai_check_async.argtypes = [P]
         L.bonsai_check_async.restype = S
         L.bonsai_status_string.argtypes = [S]
@@ -176,6 +180,37 @@ def bonsai_gemm(w: Weights, x, y, stream=None):
                           _ptr(y, (torch.float16,), "y"), _stream(stream)), "bonsai_gemm")
 
 
+def bonsai_gemm_swiglu(w: Weights, x, h, stream=None):
+    """h [m][n/2] = silu(g) * u for the interleaved gate/up matrix w (16-row
+    blocks: 8 gate rows, then the 8 up rows of the same features)."""
+    import torch
+    ws = w.c_struct()
+    m = x.shape[0] if x.dim() == 2 else 1
+    _ok(lib().bonsai_gemm_swiglu(C.byref(ws), _ptr(x, (torch.float16,), "x"), m,
+                                 _ptr(h, (torch.float16,), "h"), _stream(stream)),
+        "bonsai_gemm_swiglu")
+
+
+def interleave_gate_up(gate, up):
+    """Stack gate and up rows [F][...] into the [2F][...] row order that
+    bonsai_gemm_swiglu reads: 8 gate rows, then the 8 up rows of the same
+    features, per 16-row block. Works on numpy arrays and torch tensors."""
+    f = gate.shape[0]
+    if f % 8 or up.shape != gate.shape:
+        raise ValueError("gate and up must have the same shape with a multiple of 8 rows")
+    rest = tuple(gate.shape[1:])
+    g = gate.reshape((f // 8, 1, 8) + rest)
+    u = up.reshape((f // 8, 1, 8) + rest)
+    try:
+        import torch
+        if isinstance(gate, torch.Tensor):
+            return torch.cat([g, u], dim=1).reshape((2 * f,) + rest)
+    except ImportError:
+        pass
+    import numpy as np
+    return np.concatenate([g, u], axis=1).reshape((2 * f,) + rest)
+
+
 def bonsai_xnor_gemm(a_bits, a_scale, w: Weights, d_out=None, y_out=None, stream=None):
     import torch
     ws = w.c_struct()
@@ -184,6 +219,19 @@ def bonsai_xnor_gemm(a_bits, a_scale, w: Weights, d_out=None, y_out=None, stream
                                C.byref(ws), _ptr(d_out, (torch.int32,), "d_out"),
                                _ptr(y_out, (torch.float16,), "y_out"), _stream(stream)),
         "bonsai_xnor_gemm")
+
+
+def bonsai_binarize_activations(x, a_bits, a_scale, stream=None):
+    """Sign codes (bit 1 where x >= 0) and mean-|x| scales of FP16 rows x [m][k],
+    written into a_bits (int32 [m][k/32]) and a_scale (float16 [m])."""
+    import torch
+    if x.dim() != 2:
+        raise ValueError("x must be [m][k]")
+    _ok(lib().bonsai_binarize_activations(_ptr(x, (torch.float16,), "x"), x.shape[0], x.shape[1],
+                                          _ptr(a_bits, (torch.int32, torch.uint8), "a_bits"),
+                                          _ptr(a_scale, (torch.float16,), "a_scale"),
+                                          _stream(stream)),
+        "bonsai_binarize_activations")
 
 
 def bonsai_check_async(stream=None) -> int:

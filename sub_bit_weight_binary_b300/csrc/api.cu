@@ -9,11 +9,15 @@ namespace bonsai {
 // Launchers and status readers of the other translation units.
 bonsai_status pack_binary_launch(const int8_t*, int64_t, int64_t, void*, int64_t, cudaStream_t);
 bonsai_status pack_ternary_launch(const int8_t*, int64_t, int64_t, void*, int64_t, cudaStream_t);
-bonsai_status gemv_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, cudaStream_t);
+bonsai_status gemv_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, bool,
+                          cudaStream_t);
 bonsai_status splitk_launch(const bonsai_weights*, const uint16_t*, uint16_t*, cudaStream_t);
-bonsai_status gemm_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, cudaStream_t);
+bonsai_status gemm_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, bool,
+                          cudaStream_t);
 bonsai_status xnor_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
                           int32_t*, uint16_t*, cudaStream_t);
+bonsai_status binarize_launch(const uint16_t*, int64_t, int64_t, uint32_t*, uint16_t*,
+                              cudaStream_t);
 unsigned int read_clear_status_pack();
 unsigned int read_clear_status_gemv();
 unsigned int read_clear_status_gemm();
@@ -179,7 +183,7 @@ bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x, uint16_t* 
   if (st != BONSAI_OK) return st;
   if (!x || !y) return BONSAI_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
-  return gemv_launch(w, x, 1, y, stream);
+  return gemv_launch(w, x, 1, y, false, stream);
 }
 
 bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
@@ -199,10 +203,25 @@ bonsai_status bonsai_gemm(const bonsai_weights* w, const uint16_t* x, int64_t m,
   if (m > kMaxM) return BONSAI_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
   if (m <= 8) {
-    st = gemv_launch(w, x, m, y, stream);
+    st = gemv_launch(w, x, m, y, false, stream);
     if (st != BONSAI_ERR_UNSUPPORTED) return st;
   }
-  return gemm_launch(w, x, m, y, stream);
+  return gemm_launch(w, x, m, y, false, stream);
+}
+
+bonsai_status bonsai_gemm_swiglu(const bonsai_weights* w, const uint16_t* x, int64_t m,
+                                 uint16_t* h, bonsai_stream stream) {
+  bonsai_status st = check_weights(w);
+  if (st != BONSAI_OK) return st;
+  if (!x || !h || m <= 0) return BONSAI_ERR_INVALID_ARG;
+  if (w->n % 16) return BONSAI_ERR_SHAPE;
+  if (m > kMaxM) return BONSAI_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(h)) return BONSAI_ERR_ALIGN;
+  if (m <= 8) {
+    st = gemv_launch(w, x, m, h, true, stream);
+    if (st != BONSAI_ERR_UNSUPPORTED) return st;
+  }
+  return gemm_launch(w, x, m, h, true, stream);
 }
 
 bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,
@@ -217,6 +236,16 @@ bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale, 
       (y_out && !aligned16(y_out)))
     return BONSAI_ERR_ALIGN;
   return xnor_launch(a_bits, a_scale, m, w, d_out, y_out, stream);
+}
+
+bonsai_status bonsai_binarize_activations(const uint16_t* x, int64_t m, int64_t k,
+                                          uint32_t* a_bits, uint16_t* a_scale,
+                                          bonsai_stream stream) {
+  if (!x || !a_bits || !a_scale || m <= 0) return BONSAI_ERR_INVALID_ARG;
+  if (k <= 0 || k % 128) return BONSAI_ERR_SHAPE;
+  if (m > kMaxM || k > kMaxK) return BONSAI_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(a_bits) || !aligned16(a_scale)) return BONSAI_ERR_ALIGN;
+  return binarize_launch(x, m, k, a_bits, a_scale, stream);
 }
 
 bonsai_status bonsai_check_async(bonsai_stream stream) {

@@ -131,6 +131,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// ---------------- gated feed-forward epilogue ----------------
+// silu(g) = g * sigmoid(g) = g / (1 + e^-g), in FP32 (expf, IEEE divide):
+// e^-g overflows to +inf below g ~ -88 and the quotient is then -0.
+__device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
+
 // ---------------- programmatic dependent launch ----------------
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -60,6 +60,8 @@ struct Params {
   int m, n, k, G, nk;
   int tiles, tok_tiles;
   int prefetch;
+  int swiglu;    // rows 16t..16t+7 gate, 16t+8..16t+15 up: write silu(g)*u
+  int y_stride;  // elements per token row of y: n, or n/2 with swiglu
 };
 
 // ---- tcgen05 / TMA wrappers ------------------------------------------------
@@ -326,11 +328,25 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + 8 * a);
         }
-        if (fok) {
+        if (p.swiglu) {
+          // lanes 0-7 / 16-23 hold gate features, lanes 8-15 / 24-31 the up
+          // features of the same outputs (n % 16 == 0, so fok is uniform
+          // over each 16-lane block)
+          const int hcol = (feat >> 4) * 8 + (feat & 7);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float g = __uint_as_float(v[j]);
+            const float u = __shfl_down_sync(0xFFFFFFFFu, g, 8);
+            const int tok = m0 + 32 * c + j;
+            if (fok && !(lane & 8) && tok < p.m)
+              p.y[(size_t)tok * p.y_stride + hcol] = __float2half_rn(silu(g) * u);
+          }
+        } else if (fok) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int tok = m0 + 32 * c + j;
-            if (tok < p.m) p.y[(size_t)tok * p.n + feat] = __float2half_rn(__uint_as_float(v[j]));
+            if (tok < p.m)
+              p.y[(size_t)tok * p.y_stride + feat] = __float2half_rn(__uint_as_float(v[j]));
           }
         }
       }
@@ -437,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace gemm
 
 bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
-                          cudaStream_t stream) {
+                          bool swiglu, cudaStream_t stream) {
   using namespace gemm;
   if (m > 0x7FFFFFFF / 2) return BONSAI_ERR_UNSUPPORTED;
   CUtensorMap tm;
@@ -459,6 +475,8 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   p.tok_tiles = (int)((m + BN - 1) / BN);
   p.tiles = ((p.n + BM - 1) / BM) * p.tok_tiles;
   p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
+  p.swiglu = swiglu ? 1 : 0;
+  p.y_stride = swiglu ? p.n / 2 : p.n;
 
   const bool ter = w->format == BONSAI_FMT_TERNARY;
   const int smem = ter ? Ring<BONSAI_FMT_TERNARY>::A * A_BYTES + Ring<BONSAI_FMT_TERNARY>::B * B_BYTES +

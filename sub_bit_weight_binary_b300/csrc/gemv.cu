@@ -75,6 +75,8 @@ struct Params {
   int n_sg;         // ternary: 640-code super-groups per row
   int xt_stride;    // bytes per token of the x table
   int prefetch;     // may read weights before the previous grid completes
+  int swiglu;       // rows 16t..16t+7 gate, 16t+8..16t+15 up: write silu(g)*u
+  int y_stride;     // elements per token row of y: n, or n/2 with swiglu
   int sc_tma;       // group scales streamed with the weights (G % 8 == 0)
   int sc_chunk;     // groups per chunk (64 binary, 40 ternary)
   int sc_pitch;     // smem bytes per row of streamed scales = TMA box width
@@ -135,13 +137,27 @@ __device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int l
     }
     const float* red = reinterpret_cast<const float*>(smem + p.off_red) + slot * (W * 16 * 8);
     const int row0 = tile * p.rows;
-    for (int o = lane; o < 16 * p.m; o += 32) {
-      const int row = o & 15, col = o >> 4;
-      if (row < p.rows && row0 + row < p.n) {
-        float sum = 0.f;
+    if (p.swiglu) {
+      // 8 gate rows then the 8 up rows of the same features (n % 16 == 0)
+      for (int o = lane; o < 8 * p.m; o += 32) {
+        const int r = o & 7, col = o >> 3;
+        float g = 0.f, u = 0.f;
 #pragma unroll
-        for (int w = 0; w < W; ++w) sum += red[(w * 16 + row) * 8 + col];
-        p.y[(size_t)col * p.n + row0 + row] = __float2half_rn(sum);
+        for (int w = 0; w < W; ++w) {
+          g += red[(w * 16 + r) * 8 + col];
+          u += red[(w * 16 + r + 8) * 8 + col];
+        }
+        p.y[(size_t)col * p.y_stride + tile * 8 + r] = __float2half_rn(silu(g) * u);
+      }
+    } else {
+      for (int o = lane; o < 16 * p.m; o += 32) {
+        const int row = o & 15, col = o >> 4;
+        if (row < p.rows && row0 + row < p.n) {
+          float sum = 0.f;
+#pragma unroll
+          for (int w = 0; w < W; ++w) sum += red[(w * 16 + row) * 8 + col];
+          p.y[(size_t)col * p.y_stride + row0 + row] = __float2half_rn(sum);
+        }
       }
     }
     __syncwarp();
@@ -641,7 +657,7 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
 // One launch for up to 8 binary / 4 ternary tokens. Returns UNSUPPORTED
 // when the per-CTA tables do not fit in shared memory.
 static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x, int m,
-                                     uint16_t* y, cudaStream_t stream) {
+                                     uint16_t* y, bool swiglu, cudaStream_t stream) {
   using namespace gemv;
   const bool ter = w->format == BONSAI_FMT_TERNARY;
   const int k = (int)w->k;
@@ -655,6 +671,8 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
   p.m = m;
   p.G = k / 128;
   p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
+  p.swiglu = swiglu ? 1 : 0;
+  p.y_stride = swiglu ? n / 2 : n;
   if (!ter) {
     p.rows = 16;
     p.data_bytes = k / 8;
@@ -735,14 +753,15 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
 
 // Up to 8 tokens; ternary products of more than 4 tokens take two launches.
 bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
-                          cudaStream_t stream) {
+                          bool swiglu, cudaStream_t stream) {
   if (m < 1 || m > 8) return BONSAI_ERR_UNSUPPORTED;
   if (w->format != BONSAI_FMT_TERNARY || m <= gemv::kTerMaxTokens)
-    return gemv_launch_one(w, x, (int)m, y, stream);
-  const bonsai_status st = gemv_launch_one(w, x, gemv::kTerMaxTokens, y, stream);
+    return gemv_launch_one(w, x, (int)m, y, swiglu, stream);
+  const bonsai_status st = gemv_launch_one(w, x, gemv::kTerMaxTokens, y, swiglu, stream);
   if (st != BONSAI_OK) return st;
+  const int64_t y_stride = swiglu ? w->n / 2 : w->n;
   return gemv_launch_one(w, x + gemv::kTerMaxTokens * w->k, (int)m - gemv::kTerMaxTokens,
-                         y + gemv::kTerMaxTokens * w->n, stream);
+                         y + gemv::kTerMaxTokens * y_stride, swiglu, stream);
 }
 
 }  // namespace bonsai

@@ -121,6 +121,78 @@ __global__ void __launch_bounds__(kThreads) xnor_kernel(
   }
 }
 
+// ---- activation binarisation (the A operand from FP16 rows) ----
+// The pages give XOR + popcount for +-1 operands but no rule for turning an
+// FP16 activation row into one. This library's reading: code +1 where
+// x >= 0 (both zeros included; a NaN compares false and gives -1), and the
+// row scale a_s = mean |x|, the least-squares scale for those codes
+// (d/dalpha sum (x - alpha*a)^2 = 0 gives alpha = sum |x| / K).
+// One pass over x: each thread reads 8 halves (16 B), forms one byte of the
+// code row, and 4 neighbouring lanes make one LE word; |x| is summed in FP32
+// and reduced over the CTA, which owns whole rows.
+constexpr int kBinThreads = 256;
+constexpr int kBinUnroll = 4;
+
+// bit = (x >= 0) on the FP16 pattern h: +0..+inf are 0x0000..0x7C00, -0 is
+// 0x8000; positive NaNs (0x7C01..0x7FFF) and every negative fall outside.
+__device__ __forceinline__ uint32_t nonneg2(uint32_t w) {
+  const uint32_t le = __vcmpleu2(w, 0x7C007C00u);  // 0xFFFF per half where h <= 0x7C00
+  const uint32_t z = __vcmpeq2(w, 0x80008000u);    // 0xFFFF per half where h == -0
+  const uint32_t m = le | z;
+  return (m & 1u) | ((m >> 15) & 2u);
+}
+
+__device__ __forceinline__ float abs_sum2(uint32_t w) {
+  const uint32_t a = w & 0x7FFF7FFFu;  // clear both sign bits
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&a));
+  return f.x + f.y;
+}
+
+__global__ void __launch_bounds__(kBinThreads) binarize_kernel(
+    const uint4* __restrict__ x, long long m, int k, uint32_t* __restrict__ a_bits,
+    __half* __restrict__ a_scale) {
+  __shared__ float red[kBinThreads / 32];
+  pdl_wait();  // x may be written by earlier work on the stream
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int chunks = k / 8;  // 16-byte chunks per row; a multiple of 16
+  for (long long row = blockIdx.x; row < m; row += gridDim.x) {
+    const uint4* xr = x + row * chunks;
+    uint32_t* br = a_bits + row * (k / 32);
+    float sum = 0.f;
+    for (int base = warp * 32; base < chunks; base += kBinThreads * kBinUnroll) {
+      uint4 v[kBinUnroll];
+#pragma unroll
+      for (int u = 0; u < kBinUnroll; ++u) {
+        const int c = base + u * kBinThreads + lane;
+        v[u] = c < chunks ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kBinUnroll; ++u) {
+        const int c = base + u * kBinThreads + lane;
+        uint32_t byte = nonneg2(v[u].x) | (nonneg2(v[u].y) << 2) | (nonneg2(v[u].z) << 4) |
+                        (nonneg2(v[u].w) << 6);
+        sum += (abs_sum2(v[u].x) + abs_sum2(v[u].y)) + (abs_sum2(v[u].z) + abs_sum2(v[u].w));
+        // lanes 4j..4j+3 hold consecutive chunks (bytes) of one word
+        byte |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
+        byte |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
+        if ((lane & 3) == 0 && c < chunks) br[c >> 2] = byte;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane == 0) red[warp] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < kBinThreads / 32; ++i) t += red[i];
+      a_scale[row] = __float2half_rn(t / float(k));
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace xnor
 
 bonsai_status xnor_launch(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,
@@ -143,6 +215,26 @@ bonsai_status xnor_launch(const uint32_t* a_bits, const uint16_t* a_scale, int64
       static_cast<const uint32_t*>(w->packed), (long long)(w->row_bytes / 4),
       reinterpret_cast<const __half*>(w->scales), (int)m, (int)w->n, (int)w->k, d_out,
       reinterpret_cast<__half*>(y_out));
+  return cuda_status(e);
+}
+
+bonsai_status binarize_launch(const uint16_t* x, int64_t m, int64_t k, uint32_t* a_bits,
+                              uint16_t* a_scale, cudaStream_t stream) {
+  using namespace xnor;
+  const long long cap = 8LL * device_sm_count();  // 8 CTAs of 256 threads fill an SM
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(m < cap ? m : cap));
+  cfg.blockDim = dim3(kBinThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, binarize_kernel, reinterpret_cast<const uint4*>(x),
+                                     (long long)m, (int)k, a_bits,
+                                     reinterpret_cast<__half*>(a_scale));
   return cuda_status(e);
 }
 

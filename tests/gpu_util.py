@@ -93,3 +93,18 @@ def assert_close(y_gpu_u16, y_ref, norm, what=""):
     assert bad == 0, "%s: %d outputs outside %g*norm (first flat index %d, worst %.3g)" % (
         what, bad, TOL, first, worst)
     return worst
+
+
+def assert_swiglu_close(h_gpu_u16, h, g, u, norm_g, norm_u, what=""):
+    """h = silu(g) * u from g and u that each carry the products' error
+    (<= TOL * norm). |silu'| <= 1.1 and |silu(g)| <= |g| give
+        |dh| <= 1.1 * Eg * (|u| + Eu) + |g| * Eu,   E* = TOL * norm_*,
+    and the single FP16 rounding of h adds 2^-11 of |h| + that (2^-10 kept).
+    A zero bound (no gate or no up weights) requires h = +-0 exactly."""
+    eg, eu = TOL * norm_g, TOL * norm_u
+    b = 1.1 * eg * (np.abs(u) + eu) + np.abs(g) * eu
+    b = b + 2.0 ** -10 * (np.abs(h) + b)
+    bad, first, worst = oracle.compare_f16(h_gpu_u16, h, b, 1.0)
+    assert bad == 0, "%s: %d outputs outside the bound (first flat index %d, worst %.3g)" % (
+        what, bad, first, worst)
+    return worst

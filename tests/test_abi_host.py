@@ -29,7 +29,8 @@ def declared(header):
 def test_headers_declare_the_boundary():
     names = declared("bonsai.h")
     for f in ("bonsai_packed_row_bytes", "bonsai_pack_binary", "bonsai_pack_ternary",
-              "bonsai_gemv", "bonsai_gemm", "bonsai_xnor_gemm", "bonsai_check_async",
+              "bonsai_gemv", "bonsai_gemm", "bonsai_xnor_gemm", "bonsai_binarize_activations",
+              "bonsai_gemm_swiglu", "bonsai_check_async",
               "bonsai_status_string"):
         assert f in names
 
@@ -107,6 +108,20 @@ def test_other_host_checks(libs):
         == "BONSAI_ERR_INVALID_ARG"
     assert sb.STATUS[L.bonsai_xnor_gemm(0x50004, 0x60000, 4, C.byref(w), 0x70000, None, None)] \
         == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[L.bonsai_gemm_swiglu(C.byref(w), None, 4, 0x40000, None)] \
+        == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[L.bonsai_gemm_swiglu(C.byref(w), 0x30000, 4, 0x40008, None)] \
+        == "BONSAI_ERR_ALIGN"
+    w24 = W(n=24)
+    assert sb.STATUS[L.bonsai_gemm_swiglu(C.byref(w24), 0x30000, 4, 0x40000, None)] \
+        == "BONSAI_ERR_SHAPE"
+    bz = L.bonsai_binarize_activations
+    assert sb.STATUS[bz(None, 4, 128, 0x50000, 0x60000, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[bz(0x40000, 0, 128, 0x50000, 0x60000, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[bz(0x40000, 4, 96, 0x50000, 0x60000, None)] == "BONSAI_ERR_SHAPE"
+    assert sb.STATUS[bz(0x40000, 4, 1 << 21, 0x50000, 0x60000, None)] == "BONSAI_ERR_UNSUPPORTED"
+    assert sb.STATUS[bz(0x40000, 4, 128, 0x50004, 0x60000, None)] == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[bz(0x40000, 4, 128, 0x50000, 0x60002, None)] == "BONSAI_ERR_ALIGN"
     for f in (L.bonsai_pack_binary, L.bonsai_pack_ternary):
         assert sb.STATUS[f(None, 2, 128, 0x10000, 64, None)] == "BONSAI_ERR_INVALID_ARG"
         assert sb.STATUS[f(0x10000, -1, 128, 0x20000, 64, None)] == "BONSAI_ERR_INVALID_ARG"
@@ -125,3 +140,21 @@ def test_binding_refuses_cpu_tensors(libs):
     with pytest.raises(ValueError):
         sb.bonsai_gemv(w, torch.zeros(128, dtype=torch.float16),
                        torch.zeros(4, dtype=torch.float16), stream=0)
+
+
+def test_interleave_gate_up_row_order():
+    """interleave_gate_up puts gate row f at 16*(f//8) + f%8 and up row f
+    8 rows below it, for numpy arrays and torch tensors."""
+    import numpy as np
+    import torch
+    f = 24
+    gate = np.arange(f * 3).reshape(f, 3)
+    up = 1000 + np.arange(f * 3).reshape(f, 3)
+    out = sb.interleave_gate_up(gate, up)
+    for r in range(f):
+        assert np.array_equal(out[16 * (r // 8) + r % 8], gate[r])
+        assert np.array_equal(out[16 * (r // 8) + r % 8 + 8], up[r])
+    tout = sb.interleave_gate_up(torch.from_numpy(gate), torch.from_numpy(up))
+    assert np.array_equal(tout.numpy(), out)
+    with pytest.raises(ValueError):
+        sb.interleave_gate_up(gate[:12], up[:12])

@@ -10,7 +10,7 @@ import pytest
 import oracle
 import sub_bit_weight_binary_b300 as sb
 from sub_bit_weight_binary_b300 import synth
-from gpu_util import Guarded, assert_close, dev, host, torch, weights
+from gpu_util import Guarded, assert_close, assert_swiglu_close, dev, host, torch, weights
 
 pytestmark = pytest.mark.gpu
 BIN, TER = sb.BONSAI_FMT_BINARY, sb.BONSAI_FMT_TERNARY
@@ -234,7 +234,7 @@ def test_gemm_few_tokens(fmt, m, n, k):
 # ------------------------------------------------------- GEMM, tensor cores
 @pytest.mark.parametrize("fmt", [BIN, TER])
 @pytest.mark.parametrize("m,n,k", [(9, 128, 128), (300, 200, 640), (512, 384, 1024),
-                                   (257, 130, 5120), (256, 256, 320 * 4)])
+                                   (257, 130, 5120), (256, 256, 320 * 4), (130, 96, 17408)])
 def test_gemm_tensor_core(fmt, m, n, k):
     t = torch()
     w, packed, scales = weights(fmt, 60 + m, n, k)
@@ -320,6 +320,178 @@ def test_xnor_workload():
         assert np.array_equal(dg[i:i + 64].astype(np.int64), ref)
     d.check()
     y.check()
+
+
+@pytest.mark.parametrize("fmt", [BIN, TER])
+def test_gemm_down_projection_sampled(fmt):
+    """The down projection of a prefill layer (M=512, K=17408, N=5120) at
+    full size, sampled outputs."""
+    t = torch()
+    m, n, k = 512, 5120, 17408
+    w, packed, scales = weights(fmt, 180 + fmt, n, k)
+    x = synth.gen_x(181, m, k)
+    y = Guarded((m, n), t.float16)
+    sb.bonsai_gemm(w, dev(x), y.t)
+    assert sb.bonsai_check_async() == 0
+    ms = sample_idx(m, [0, 255, 256, m - 1], 10, 9)
+    ns = sample_idx(n, [0, 127, 128, n - 1], 40, 10)
+    y_ref, nrm = oracle.linear(fmt, packed, scales, x, n_sel=ns, m_sel=ms)
+    assert_close(host(y.t)[np.ix_(ms, ns)], y_ref, nrm, "down projection")
+    y.check()
+
+
+# ------------------------------------------ gated feed-forward (SwiGLU)
+SWIGLU_CASES = [(BIN, 8, 128, 1), (TER, 8, 128, 1), (BIN, 24, 640, 3), (TER, 40, 640, 5),
+                (TER, 56, 1152, 8), (BIN, 200, 1024, 9), (TER, 136, 1024, 300),
+                (BIN, 64, 256, 257)]
+
+
+@pytest.mark.parametrize("fmt,f,k,m", SWIGLU_CASES)
+def test_swiglu_full(fmt, f, k, m):
+    """Every output of h = silu(g) * u for the interleaved gate/up matrix:
+    decode kernel (m <= 8, ternary m > 4 in two launches) and GEMM (m > 8,
+    ragged feature and token tiles)."""
+    t = torch()
+    w, packed, scales = weights(fmt, 150 + f, 2 * f, k)
+    x = synth.gen_x(151 + m, m, k)
+    h = Guarded((m, f), t.float16)
+    sb.bonsai_gemm_swiglu(w, dev(x), h.t)
+    assert sb.bonsai_check_async() == 0
+    href, g, u, ng, nu = oracle.swiglu(fmt, packed, scales, x)
+    assert_swiglu_close(host(h.t), href, g, u, ng, nu, "swiglu fmt=%d f=%d k=%d m=%d" % (fmt, f, k, m))
+    h.check()
+
+
+@pytest.mark.parametrize("fmt,m", [(BIN, 1), (TER, 1), (TER, 8), (BIN, 512), (TER, 512)])
+def test_swiglu_workload(fmt, m):
+    """Gate/up of the 64-layer model (F=17408, K=5120), sampled features."""
+    t = torch()
+    f, k = 17408, 5120
+    w, packed, scales = weights(fmt, 160 + fmt, 2 * f, k)
+    x = synth.gen_x(161 + m, m, k)
+    h = Guarded((m, f), t.float16)
+    sb.bonsai_gemm_swiglu(w, dev(x), h.t)
+    assert sb.bonsai_check_async() == 0
+    fs = sample_idx(f, [0, 7, 8, 63, 64, 127, 128, f - 9, f - 8, f - 1], 50, 7)
+    ms = sample_idx(m, [0, m - 1], 12, 8)
+    href, g, u, ng, nu = oracle.swiglu(fmt, packed, scales, x, f_sel=fs, m_sel=ms)
+    assert_swiglu_close(host(h.t)[np.ix_(ms, fs)], href, g, u, ng, nu, "swiglu workload m=%d" % m)
+    h.check()
+
+
+def test_swiglu_zero_gate_rows():
+    """Ternary gate rows that are all zero give h = +-0 exactly, whatever u."""
+    t = torch()
+    f, k = 16, 640
+    codes = synth.gen_ternary_codes(170, 2 * f, k)
+    codes[0:8] = 0          # gate rows of features 0..7
+    codes[24:32] = 0        # up rows of features 8..15
+    rb = sb.bonsai_packed_row_bytes(TER, k)
+    packed_gpu = t.empty((2 * f, rb), dtype=t.uint8, device="cuda")
+    sb.bonsai_pack_ternary(dev(codes), packed_gpu)
+    scales = synth.gen_scales(171, 2 * f, k)
+    w = sb.Weights(TER, 2 * f, k, packed_gpu, dev(scales))
+    for m in (1, 3, 20):
+        x = synth.gen_x(172 + m, m, k)
+        h = t.empty((m, f), dtype=t.float16, device="cuda")
+        sb.bonsai_gemm_swiglu(w, dev(x), h)
+        assert sb.bonsai_check_async() == 0
+        hv = host(h)
+        assert np.all((hv & 0x7FFF) == 0), m
+        href, g, u, ng, nu = oracle.swiglu(TER, oracle.pack_ternary(codes), scales, x)
+        assert np.all(href == 0.0)
+        assert_swiglu_close(hv, href, g, u, ng, nu, "zero rows m=%d" % m)
+
+
+# --------------------------------------------- activation binarisation
+def scale_tol(ref, k):
+    """Bound on |a_s_gpu - mean|x|| for the FP16 scale: the FP32 sum of k
+    non-negative terms and the division are within (k + 1) * 2^-24 of the
+    exact mean, relative; the FP16 rounding adds half an ulp (2^-11 relative,
+    2^-25 absolute in the subnormal range)."""
+    return (2.0 ** -11 + (k + 2) * 2.0 ** -24) * np.abs(ref) + 2.0 ** -25
+
+
+def check_binarized(bits_gpu, as_gpu, x, what):
+    k = x.shape[1]
+    bits_ref, as_ref = oracle.binarize(x)
+    assert np.array_equal(bits_gpu.view(np.uint32), bits_ref), what + ": codes"
+    got = as_gpu.view(np.float16).astype(np.float64)
+    nan = np.isnan(as_ref)
+    assert np.array_equal(np.isnan(got), nan), what + ": NaN scales"
+    g, r = got[~nan], as_ref[~nan]
+    inf = np.isinf(r)
+    assert np.array_equal(g[inf], r[inf]), what + ": infinite scales"
+    err = np.abs(g[~inf] - r[~inf])
+    assert np.all(err <= scale_tol(r[~inf], k)), (what, float(err.max(initial=0.0)))
+
+
+@pytest.mark.parametrize("m,k", [(1, 128), (3, 640), (5, 4096), (512, 4096), (1, 17408),
+                                 (7, 5120), (1300, 256), (2, 1152)])
+def test_binarize_rows(m, k):
+    t = torch()
+    x = synth.gen_x(130 + m, m, k)
+    bits = Guarded((m, k // 32), t.int32)
+    a_s = Guarded((m,), t.float16)
+    sb.bonsai_binarize_activations(dev(x), bits.t, a_s.t)
+    assert sb.bonsai_check_async() == 0
+    check_binarized(host(bits.t), host(a_s.t), x, "binarize m=%d k=%d" % (m, k))
+    bits.check()
+    a_s.check()
+
+
+def test_binarize_special_values():
+    """Both zeros give +1, a NaN gives -1 and a NaN scale, infinities keep
+    their sign and give an infinite scale, subnormals keep theirs."""
+    t = torch()
+    k = 256
+    f = np.float16
+    rows = np.zeros((8, k), dtype=np.float16)
+    rows[1] = f(-0.0)
+    rows[2] = np.where(np.arange(k) % 2, f(-0.0), f(0.0))
+    rows[3] = f(1.0)
+    rows[3, 77] = f(np.nan)
+    rows[4] = f(-1.0)
+    rows[4, 3] = -f(np.nan)
+    rows[5] = np.where(np.arange(k) % 3, f(np.inf), f(-np.inf))
+    rows[6] = np.where(np.arange(k) % 2, f(6e-8), f(-6e-8))  # smallest subnormal
+    rows[7] = np.where(np.arange(k) < 200, f(65504.0), f(-65504.0))  # largest finite
+    x = rows.view(np.uint16)
+    bits = t.empty((8, k // 32), dtype=t.int32, device="cuda")
+    a_s = t.empty(8, dtype=t.float16, device="cuda")
+    sb.bonsai_binarize_activations(dev(x), bits, a_s)
+    assert sb.bonsai_check_async() == 0
+    check_binarized(host(bits), host(a_s), x, "special values")
+
+
+def test_xnor_from_fp16_activations():
+    """FP16 activations -> bonsai_binarize_activations -> bonsai_xnor_gemm,
+    against the oracle's binarisation composed with its XNOR product (unit
+    activation scale, then times the exact mean |x|). D is exact; Y carries
+    the scale's FP16 rounding, inside 2e-3 of sum a_s*128*|s_g|."""
+    t = torch()
+    for (m, n, k) in ((37, 200, 1024), (512, 4096, 4096)):
+        x = synth.gen_x(140 + m, m, k)
+        w_bits = synth.gen_binary_words(141 + m, n, k)
+        s = synth.gen_scales(142 + m, n, k)
+        w = sb.Weights(BIN, n, k, dev(w_bits.view(np.uint8).reshape(n, -1)), dev(s))
+        bits = t.empty((m, k // 32), dtype=t.int32, device="cuda")
+        a_s = t.empty(m, dtype=t.float16, device="cuda")
+        d = Guarded((m, n), t.int32)
+        y = Guarded((m, n), t.float16)
+        sb.bonsai_binarize_activations(dev(x), bits, a_s)
+        sb.bonsai_xnor_gemm(bits, a_s, w, d.t, y.t)
+        assert sb.bonsai_check_async() == 0
+        bits_ref, as_ref = oracle.binarize(x)
+        ms = sample_idx(m, [0, m - 1], 20, 5)
+        ns = sample_idx(n, [0, 63, 64, n - 1], 30, 6)
+        unit = np.full(m, np.float16(1.0).view(np.uint16), dtype=np.uint16)
+        d_ref, y1, n1 = oracle.xnor(bits_ref, unit, w_bits, s, k, n_sel=ns, m_sel=ms)
+        assert np.array_equal(host(d.t)[np.ix_(ms, ns)].astype(np.int64), d_ref)
+        sc = as_ref[ms][:, None]
+        assert_close(host(y.t)[np.ix_(ms, ns)], sc * y1, sc * n1, "xnor from fp16 m=%d" % m)
+        d.check()
+        y.check()
 
 
 # ------------------------------------------------------------ graph capture
