@@ -60,6 +60,8 @@ def configure(L):
     L.oracle_swiglu.argtypes = [C.c_int, P, I64, P, I64, I64, P, I64, P, I64, P, I64,
                                 P, P, P, P, P]
     L.oracle_swiglu.restype = C.c_int
+    L.oracle_hadamard.argtypes = [P, I64, I64, I64, P, P]
+    L.oracle_hadamard.restype = C.c_int
     L.oracle_binarize.argtypes = [P, I64, I64, P, P]
     L.oracle_binarize.restype = C.c_int
     L.oracle_xnor.argtypes = [P, P, I64, P, I64, P, I64, I64,
@@ -211,6 +213,20 @@ def swiglu(fmt: int, packed: np.ndarray, scales: np.ndarray, x: np.ndarray,
                                _p(f_sel), len(f_sel), _p(m_sel), len(m_sel),
                                *[_p(o) for o in outs]), "swiglu")
     return tuple(outs)
+
+
+def hadamard(x: np.ndarray, block: int, sign_bits=None):
+    """Block-diagonal signed Hadamard rotation of FP16 rows x [m][k]
+    (float64 [m][k]); sign_bits: uint32 [k/32] (bit 1 = +1) or None."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    m, k = x.shape
+    out = np.empty((m, k), dtype=np.float64)
+    sb = None if sign_bits is None else np.ascontiguousarray(sign_bits, dtype=np.uint32)
+    _check(lib().oracle_hadamard(_p(x), m, k, block, None if sb is None else _p(sb), _p(out)),
+           "hadamard")
+    return out
 
 
 def binarize(x: np.ndarray):

@@ -336,6 +336,40 @@ int oracle_binarize(const uint16_t* x, int64_t m, int64_t k, uint8_t* bits,
   return st;
 }
 
+/* Signed Hadamard rotation of activation rows. The OpenBonsai page
+ * ("工作原理") lists a signed Hadamard rotation among its compression steps
+ * (to tame weight outliers) but states neither its size nor where the
+ * activation side is rotated. This library's reading: a block-diagonal
+ * rotation along K with power-of-two blocks b (b | k), one +-1 sign per
+ * input feature, orthonormal scaling:
+ *   out[r][b0 + i] = b^(-1/2) * sum_{j<b} H[i][j] * s[b0 + j] * x[r][b0 + j],
+ *   H[i][j] = (-1)^popcount(i & j)      (Sylvester's construction),
+ * for each block start b0 = 0, b, 2b, ... The signs are bits in the binary
+ * weight layout (bit (k%32) of word k/32, bit 1 = +1); NULL means all +1.
+ * Written straight from the definition: O(b) work per output. */
+int oracle_hadamard(const uint16_t* x, int64_t m, int64_t k, int64_t block,
+                    const uint8_t* sign_bits, double* out) {
+  if (!x || !out || m < 0 || k <= 0 || block <= 0) return O_ERR_ARG;
+  if (block & (block - 1)) return O_ERR_SHAPE;
+  if (k % block) return O_ERR_SHAPE;
+  const double scale = 1.0 / sqrt((double)block);
+  for (int64_t r = 0; r < m; ++r) {
+    for (int64_t b0 = 0; b0 < k; b0 += block) {
+      for (int64_t i = 0; i < block; ++i) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < block; ++j) {
+          const int64_t kk = b0 + j;
+          double v = oracle_half_to_double(x[r * k + kk]);
+          if (sign_bits && !((sign_bits[kk >> 3] >> (kk & 7)) & 1)) v = -v;
+          acc += (__builtin_popcountll((unsigned long long)(i & j)) & 1) ? -v : v;
+        }
+        out[r * k + b0 + i] = acc * scale;
+      }
+    }
+  }
+  return O_OK;
+}
+
 /* Acceptance: |y_gpu - y_ref| <= tol * norm; norm == 0 requires y_gpu = +-0;
  * a non-finite y_gpu always fails. Returns the number of failures; writes
  * the first failing index (or -1) and the largest |err|/norm seen. */

@@ -411,6 +411,54 @@ def pin_swiglu():
     assert np.all(h == 0.0) and np.all(ng == 0.0) and np.all(u == 1.0)
 
 
+def pin_hadamard():
+    import scipy.linalg
+    f = np.float16
+    # worked example by hand: H4 [1,2,3,4] / 2 = [5, -1, -2, 0]
+    x = np.array([[1, 2, 3, 4]], dtype=f).view(np.uint16)
+    assert list(oracle.hadamard(x, 4)[0]) == [5.0, -1.0, -2.0, 0.0]
+    assert np.allclose(oracle.hadamard(x, 2)[0], np.array([3, -1, 7, -1]) / np.sqrt(2),
+                       rtol=1e-15, atol=0)
+    # against scipy's Sylvester matrix (built by its own recursion), with signs
+    for b, k in ((2, 64), (16, 64), (128, 384), (1024, 2048)):
+        xr = rand_x(41 + b, 3, k)
+        bits = synth.gen_binary_words(42 + b, 1, k)[0]
+        sgn = np_decode_binary(bits.view(np.uint8)[None, :], k)[0].astype(np.float64)
+        hm = scipy.linalg.hadamard(b).astype(np.float64) / np.sqrt(b)
+        xs = (f16(xr) * sgn).reshape(3, k // b, b)
+        ref = np.einsum("ij,rbj->rbi", hm, xs).reshape(3, k)
+        got = oracle.hadamard(xr, b, bits)
+        assert np.allclose(got, ref, rtol=0, atol=1e-12 * np.abs(f16(xr)).max() * np.sqrt(b))
+        # orthonormal: the sum of squares of every block is kept
+        assert np.allclose((got.reshape(3, -1, b) ** 2).sum(axis=2),
+                           (f16(xr).reshape(3, -1, b) ** 2).sum(axis=2), rtol=1e-12, atol=0)
+        # no sign vector means all +1
+        assert np.array_equal(oracle.hadamard(xr, b), oracle.hadamard(xr, b, np.full(k // 32, 0xFFFFFFFF, np.uint32)))
+    # unit vectors give the columns of H (entries +-b^-1/2), blocks do not mix
+    b, k = 16, 48
+    for j in (0, 5, 16 + 9, 47):
+        e = np.zeros((1, k), dtype=f)
+        e[0, j] = 1.0
+        got = oracle.hadamard(e.view(np.uint16), b)[0]
+        blk = j // b
+        col = np.array([(-1) ** bin(i & (j % b)).count("1") for i in range(b)]) / 4.0
+        assert np.array_equal(got[blk * b:(blk + 1) * b], col)
+        assert np.all(np.delete(got, np.arange(blk * b, (blk + 1) * b)) == 0.0)
+    # the rotation is its own inverse when b is an even power of two (exact
+    # here: the first pass of these integer rows is again exact in FP16)
+    xr = np.array([[3, -1, 4, 1, -5, 9, 2, -6, 5, 3, -5, 8, 9, -7, 9, 3]], dtype=f)
+    once = oracle.hadamard(xr.view(np.uint16), 16)
+    assert np.array_equal(once.astype(f).astype(np.float64), once)
+    twice = oracle.hadamard(once.astype(f).view(np.uint16), 16)
+    assert np.array_equal(twice, xr.astype(np.float64))
+    # a cleared sign bit negates that input
+    bits = np.full(1, 0xFFFFFFFF ^ (1 << 3), dtype=np.uint32)
+    xr32 = rand_x(43, 1, 32)
+    neg = xr32.copy()
+    neg[0, 3] ^= 0x8000
+    assert np.array_equal(oracle.hadamard(xr32, 32, bits), oracle.hadamard(neg, 32))
+
+
 def pin_compare_rule():
     ref = np.array([1.0, 1.0, 0.0, 1.0, 1.0])
     nrm = np.array([10.0, 10.0, 0.0, 10.0, 10.0])
@@ -430,7 +478,7 @@ PINS = [pin_half_to_double, pin_row_bytes, pin_page_sizes, pin_binary_round_trip
         pin_ternary_round_trip_and_padding, pin_bad_codes,
         pin_all_plus_constant_scale, pin_group_scales, pin_zero_ternary,
         pin_flip_and_scale, pin_single_weight, pin_brute_force, pin_xnor,
-        pin_binarize, pin_swiglu, pin_compare_rule]
+        pin_binarize, pin_swiglu, pin_hadamard, pin_compare_rule]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -466,6 +514,11 @@ MUTANTS = {
     "swiglu_swapped": ("h[o] = gv / (1.0 + exp(-gv)) * uv;", "h[o] = uv / (1.0 + exp(-uv)) * gv;"),
     "swiglu_block": ("rows[j] = 16 * (f / 8) + f % 8;", "rows[j] = 8 * (f / 8) + f % 8;"),
     "swiglu_up_offset": ("rows[f_cnt + j] = rows[j] + 8;", "rows[f_cnt + j] = rows[j] + 1;"),
+    "hadamard_or": ("(unsigned long long)(i & j)", "(unsigned long long)(i | j)"),
+    "hadamard_norm": ("const double scale = 1.0 / sqrt((double)block);",
+                      "const double scale = 1.0 / (double)block;"),
+    "hadamard_sign_index": ("(sign_bits[kk >> 3] >> (kk & 7)) & 1", "(sign_bits[kk >> 3] >> (j & 7)) & 1"),
+    "hadamard_block_base": ("const int64_t kk = b0 + j;", "const int64_t kk = j;"),
     "ter_bad_byte": ("if (value > 242) return O_ERR_BAD_CODE;", "if (value > 255) return O_ERR_BAD_CODE;"),
 }
 
