@@ -571,6 +571,55 @@ class LayerGemmWorkload(GemmWorkload):
                 "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
 
 
+class HadamardWorkload:
+    """Signed Hadamard rotation of FP16 activation rows (block 128), over
+    rotating input replicas larger than L2, timed in a CUDA graph."""
+    kind = "rotate"
+
+    def __init__(self, name, m=512, k=5120, block=128):
+        self.name, self.m, self.k, self.block = name, m, k, block
+
+    def unit_bytes(self):
+        return 2 * self.m * self.k * 2 + self.k // 8  # x in, out written, signs
+
+    def setup(self):
+        import torch
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(6)
+        self.reps = max(1, math.ceil(2 * L2_BYTES / (2 * self.m * self.k * 2)) + 1)
+        x = torch.from_numpy(synth.gen_x(seed, self.m, self.k).view(np.float16)).cuda()
+        self.x = [x.clone() for _ in range(self.reps)]
+        self.out = [torch.empty_like(x) for _ in range(self.reps)]
+        bits = synth.gen_binary_words(seed + 1, 1, self.k)[0]
+        self.signs = torch.from_numpy(bits.view(np.int32)).cuda()
+        torch.cuda.synchronize()
+
+    def launches(self, start, count):
+        import sub_bit_weight_binary_b300 as sb
+        for i in range(start, start + count):
+            j = i % self.reps
+            sb.bonsai_hadamard(self.x[j], self.out[j], self.block, self.signs)
+
+    def measure(self, steps, warmup, clocks=None):
+        ms = graph_time(self.launches, steps, warmup, clocks)
+        return {"ms": ms, "steps": steps, "launches": steps, "kernel_ms": ms / steps}
+
+    def value(self, ms, steps):
+        return self.unit_bytes() * steps / (ms / 1e3) / 1e9, "GB/s"
+
+    def roofline(self, r, pk):
+        a = self.unit_bytes() / (r["kernel_ms"] / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "hadamard_kernel<7>", "achieved": round(a, 1),
+                "peak": pk["hbm"], "unit": "GB/s", "frac": round(a / pk["hbm"], 4),
+                "traffic": None, "peak_src": "%s HBM copy (burst)" % pk["src"],
+                "bytes_per_launch": self.unit_bytes()}
+
+    def config(self):
+        return {"workload": self.name, "m": self.m, "k": self.k, "block": self.block,
+                "timing": "CUDA graph of launches over %d rotating replicas" % self.reps,
+                "l2": "inputs larger than L2 (rotating replicas)"}
+
+
 class XnorWorkload:
     kind = "xnor"
 
@@ -699,6 +748,7 @@ WORKLOADS = {
                                                  "(7 products, fused feed-forward), binary"),
     "pp512_layer_ter": lambda: LayerGemmWorkload(2, 512, "prefill M=512, one decoder layer "
                                                  "(7 products, fused feed-forward), ternary"),
+    "hadamard": lambda: HadamardWorkload("signed Hadamard rotation of x, M=512 K=5120, block 128"),
     "xnor": lambda: XnorWorkload("XNOR-popcount GEMM M=512 K=4096 N=4096"),
     "xnor_fp16": lambda: XnorFp16Workload(
         "FP16 activations binarised, then XNOR-popcount GEMM M=512 K=4096 N=4096"),
@@ -706,7 +756,8 @@ WORKLOADS = {
 SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("sweep_bin", 30, 3), ("sweep_ter", 30, 3),
              ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
              ("gemm4096_ter", 5, 2), ("layer_bin", 30, 3), ("layer_ter", 30, 3),
-             ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("xnor", 20, 3),
+             ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("hadamard", 200, 10),
+             ("xnor", 20, 3),
              ("xnor_fp16", 20, 3)]
 
 

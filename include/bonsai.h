@@ -228,6 +228,25 @@ bonsai_status bonsai_binarize_activations(const uint16_t* x, int64_t m, int64_t 
                                           uint32_t* a_bits, uint16_t* a_scale,
                                           bonsai_stream stream);
 
+/* Signed Hadamard rotation of activation rows, for weights that were
+ * rotated offline (OpenBonsai page, "工作原理": a signed Hadamard rotation is
+ * one of its compression steps; the pages give neither its size nor where
+ * the activations are rotated). Block-diagonal along K with power-of-two
+ * blocks, orthonormal:
+ *   out[r][b0 + i] = block^(-1/2) * sum_{j<block} H[i][j] * s[b0+j] * x[r][b0+j],
+ *   H[i][j] = (-1)^popcount(i & j)   (Sylvester's Hadamard matrix),
+ * for b0 = 0, block, 2*block, ...
+ *   x      device FP16 [m][k], 16-byte aligned.
+ *   m      rows, >= 1.   k: multiple of 128 and of block.
+ *   block  8, 16, ..., 1024 (else BONSAI_ERR_UNSUPPORTED).
+ *   signs  device uint32 [k/32], bit (k%32) of word k/32 = 1 for s = +1,
+ *          0 for s = -1 (the BINARY weight layout); NULL for all +1.
+ *   out    device FP16 [m][k], 16-byte aligned; may equal x (in place) but
+ *          must not otherwise overlap it (BONSAI_ERR_INVALID_ARG).
+ * FP32 butterflies (log2(block) stages), one FP16 rounding of each output. */
+bonsai_status bonsai_hadamard(const uint16_t* x, int64_t m, int64_t k, int32_t block,
+                              const uint32_t* signs, uint16_t* out, bonsai_stream stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: BONSAI_OK, BONSAI_ERR_BAD_CODE or BONSAI_ERR_TIMEOUT.
  * Returns BONSAI_ERR_CUDA if the stream reported a CUDA error. */

@@ -70,6 +70,8 @@ def lib():
         L.bonsai_xnor_gemm.restype = S
         L.bonsai_binarize_activations.argtypes = [P, I64, I64, P, P, P]
         L.bonsai_binarize_activations.restype = S
+        L.bonsai_hadamard.argtypes = [P, I64, I64, C.c_int32, P, P, P]
+        L.bonsai_hadamard.restype = S
         L.bonsai_check_async.argtypes = [P]
         L.bonsai_check_async.restype = S
         L.bonsai_status_string.argtypes = [S]
@@ -232,6 +234,18 @@ def bonsai_binarize_activations(x, a_bits, a_scale, stream=None):
                                           _ptr(a_scale, (torch.float16,), "a_scale"),
                                           _stream(stream)),
         "bonsai_binarize_activations")
+
+
+def bonsai_hadamard(x, out, block=128, signs=None, stream=None):
+    """Block-diagonal signed Hadamard rotation of FP16 rows x [m][k] into out
+    (may be x itself); signs: int32 [k/32] bits (1 = +1) or None (all +1)."""
+    import torch
+    if x.dim() != 2:
+        raise ValueError("x must be [m][k]")
+    _ok(lib().bonsai_hadamard(_ptr(x, (torch.float16,), "x"), x.shape[0], x.shape[1], block,
+                              _ptr(signs, (torch.int32,), "signs"),
+                              _ptr(out, (torch.float16,), "out"), _stream(stream)),
+        "bonsai_hadamard")
 
 
 def bonsai_check_async(stream=None) -> int:

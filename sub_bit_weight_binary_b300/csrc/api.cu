@@ -18,6 +18,8 @@ bonsai_status xnor_launch(const uint32_t*, const uint16_t*, int64_t, const bonsa
                           int32_t*, uint16_t*, cudaStream_t);
 bonsai_status binarize_launch(const uint16_t*, int64_t, int64_t, uint32_t*, uint16_t*,
                               cudaStream_t);
+bonsai_status hadamard_launch(const uint16_t*, int64_t, int64_t, int32_t, const uint32_t*,
+                              uint16_t*, cudaStream_t);
 unsigned int read_clear_status_pack();
 unsigned int read_clear_status_gemv();
 unsigned int read_clear_status_gemm();
@@ -246,6 +248,22 @@ bonsai_status bonsai_binarize_activations(const uint16_t* x, int64_t m, int64_t 
   if (m > kMaxM || k > kMaxK) return BONSAI_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(a_bits) || !aligned16(a_scale)) return BONSAI_ERR_ALIGN;
   return binarize_launch(x, m, k, a_bits, a_scale, stream);
+}
+
+bonsai_status bonsai_hadamard(const uint16_t* x, int64_t m, int64_t k, int32_t block,
+                              const uint32_t* signs, uint16_t* out, bonsai_stream stream) {
+  if (!x || !out || m <= 0) return BONSAI_ERR_INVALID_ARG;
+  if (block < 8 || block > 1024 || (block & (block - 1))) return BONSAI_ERR_UNSUPPORTED;
+  if (k <= 0 || k % 128 || k % block) return BONSAI_ERR_SHAPE;
+  if (m > kMaxM || k > kMaxK) return BONSAI_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(signs) & 3u))
+    return BONSAI_ERR_ALIGN;
+  if (x != out) {  // distinct buffers must not overlap
+    const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(out);
+    const uintptr_t bytes = static_cast<uintptr_t>(m) * static_cast<uintptr_t>(k) * 2u;
+    if (a < b + bytes && b < a + bytes) return BONSAI_ERR_INVALID_ARG;
+  }
+  return hadamard_launch(x, m, k, block, signs, out, stream);
 }
 
 bonsai_status bonsai_check_async(bonsai_stream stream) {

@@ -128,10 +128,14 @@ __global__ void __launch_bounds__(kThreads) xnor_kernel(
 // row scale a_s = mean |x|, the least-squares scale for those codes
 // (d/dalpha sum (x - alpha*a)^2 = 0 gives alpha = sum |x| / K).
 // One pass over x: each thread reads 8 halves (16 B), forms one byte of the
-// code row, and 4 neighbouring lanes make one LE word; |x| is summed in FP32
-// and reduced over the CTA, which owns whole rows.
+// code row, and 4 neighbouring lanes make one LE word; |x| is summed in FP32.
+// Few rows: a CTA owns a row and reduces over its 8 warps. Many rows (at
+// least 16 per SM): a warp owns a row, keeps 8 loads per lane in flight and
+// needs no CTA barrier (measured about 1.8x faster at 4096 x 4096, slower at
+// 512 rows where it leaves SMs idle).
 constexpr int kBinThreads = 256;
 constexpr int kBinUnroll = 4;
+constexpr int kBinWarpUnroll = 8;
 
 // bit = (x >= 0) on the FP16 pattern h: +0..+inf are 0x0000..0x7C00, -0 is
 // 0x8000; positive NaNs (0x7C01..0x7FFF) and every negative fall outside.
@@ -146,6 +150,49 @@ __device__ __forceinline__ float abs_sum2(uint32_t w) {
   const uint32_t a = w & 0x7FFF7FFFu;  // clear both sign bits
   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&a));
   return f.x + f.y;
+}
+
+__device__ __forceinline__ uint32_t code_byte(const uint4& v) {
+  return nonneg2(v.x) | (nonneg2(v.y) << 2) | (nonneg2(v.z) << 4) | (nonneg2(v.w) << 6);
+}
+__device__ __forceinline__ float abs_sum8(const uint4& v) {
+  return (abs_sum2(v.x) + abs_sum2(v.y)) + (abs_sum2(v.z) + abs_sum2(v.w));
+}
+
+__global__ void __launch_bounds__(kBinThreads) binarize_rows_warp(
+    const uint4* __restrict__ x, long long m, int k, uint32_t* __restrict__ a_bits,
+    __half* __restrict__ a_scale) {
+  pdl_wait();  // x may be written by earlier work on the stream
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (kBinThreads / 32);
+  const int chunks = k / 8;  // a multiple of 16: 4-lane word groups are all in or all out
+  for (long long row = (long long)blockIdx.x * (kBinThreads / 32) + (threadIdx.x >> 5); row < m;
+       row += warps) {
+    const uint4* xr = x + row * chunks;
+    uint32_t* br = a_bits + row * (k / 32);
+    float sum = 0.f;
+    for (int base = 0; base < chunks; base += 32 * kBinWarpUnroll) {
+      uint4 v[kBinWarpUnroll];
+#pragma unroll
+      for (int u = 0; u < kBinWarpUnroll; ++u) {
+        const int c = base + 32 * u + lane;
+        v[u] = c < chunks ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kBinWarpUnroll; ++u) {
+        const int c = base + 32 * u + lane;
+        uint32_t byte = code_byte(v[u]);
+        sum += abs_sum8(v[u]);
+        byte |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
+        byte |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
+        if ((lane & 3) == 0 && c < chunks) br[c >> 2] = byte;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane == 0) a_scale[row] = __float2half_rn(sum / float(k));
+  }
 }
 
 __global__ void __launch_bounds__(kBinThreads) binarize_kernel(
@@ -170,9 +217,8 @@ __global__ void __launch_bounds__(kBinThreads) binarize_kernel(
 #pragma unroll
       for (int u = 0; u < kBinUnroll; ++u) {
         const int c = base + u * kBinThreads + lane;
-        uint32_t byte = nonneg2(v[u].x) | (nonneg2(v[u].y) << 2) | (nonneg2(v[u].z) << 4) |
-                        (nonneg2(v[u].w) << 6);
-        sum += (abs_sum2(v[u].x) + abs_sum2(v[u].y)) + (abs_sum2(v[u].z) + abs_sum2(v[u].w));
+        uint32_t byte = code_byte(v[u]);
+        sum += abs_sum8(v[u]);
         // lanes 4j..4j+3 hold consecutive chunks (bytes) of one word
         byte |= __shfl_down_sync(0xFFFFFFFFu, byte, 1) << 8;
         byte |= __shfl_down_sync(0xFFFFFFFFu, byte, 2) << 16;
@@ -222,8 +268,11 @@ bonsai_status binarize_launch(const uint16_t* x, int64_t m, int64_t k, uint32_t*
                               uint16_t* a_scale, cudaStream_t stream) {
   using namespace xnor;
   const long long cap = 8LL * device_sm_count();  // 8 CTAs of 256 threads fill an SM
+  const long long rows_per_cta = kBinThreads / 32;
+  const bool per_warp = m >= 2 * cap;  // 16 rows per SM
+  const long long want = per_warp ? (m + rows_per_cta - 1) / rows_per_cta : m;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)(m < cap ? m : cap));
+  cfg.gridDim = dim3((unsigned)(want < cap ? want : cap));
   cfg.blockDim = dim3(kBinThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -232,9 +281,9 @@ bonsai_status binarize_launch(const uint16_t* x, int64_t m, int64_t k, uint32_t*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, binarize_kernel, reinterpret_cast<const uint4*>(x),
-                                     (long long)m, (int)k, a_bits,
-                                     reinterpret_cast<__half*>(a_scale));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, per_warp ? binarize_rows_warp : binarize_kernel,
+                                     reinterpret_cast<const uint4*>(x), (long long)m, (int)k,
+                                     a_bits, reinterpret_cast<__half*>(a_scale));
   return cuda_status(e);
 }
 

@@ -30,7 +30,7 @@ def test_headers_declare_the_boundary():
     names = declared("bonsai.h")
     for f in ("bonsai_packed_row_bytes", "bonsai_pack_binary", "bonsai_pack_ternary",
               "bonsai_gemv", "bonsai_gemm", "bonsai_xnor_gemm", "bonsai_binarize_activations",
-              "bonsai_gemm_swiglu", "bonsai_check_async",
+              "bonsai_gemm_swiglu", "bonsai_hadamard", "bonsai_check_async",
               "bonsai_status_string"):
         assert f in names
 
@@ -115,6 +115,16 @@ def test_other_host_checks(libs):
     w24 = W(n=24)
     assert sb.STATUS[L.bonsai_gemm_swiglu(C.byref(w24), 0x30000, 4, 0x40000, None)] \
         == "BONSAI_ERR_SHAPE"
+    hd = L.bonsai_hadamard
+    assert sb.STATUS[hd(None, 2, 256, 128, None, 0x50000, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[hd(0x40000, 2, 256, 96, None, 0x50000, None)] == "BONSAI_ERR_UNSUPPORTED"
+    assert sb.STATUS[hd(0x40000, 2, 256, 2048, None, 0x50000, None)] == "BONSAI_ERR_UNSUPPORTED"
+    assert sb.STATUS[hd(0x40000, 2, 384, 256, None, 0x50000, None)] == "BONSAI_ERR_SHAPE"
+    assert sb.STATUS[hd(0x40000, 2, 200, 8, None, 0x50000, None)] == "BONSAI_ERR_SHAPE"
+    assert sb.STATUS[hd(0x40008, 2, 256, 128, None, 0x50000, None)] == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[hd(0x40000, 2, 256, 128, 0x60002, 0x50000, None)] == "BONSAI_ERR_ALIGN"
+    # overlapping but not identical buffers
+    assert sb.STATUS[hd(0x40000, 2, 256, 128, None, 0x40100, None)] == "BONSAI_ERR_INVALID_ARG"
     bz = L.bonsai_binarize_activations
     assert sb.STATUS[bz(None, 4, 128, 0x50000, 0x60000, None)] == "BONSAI_ERR_INVALID_ARG"
     assert sb.STATUS[bz(0x40000, 0, 128, 0x50000, 0x60000, None)] == "BONSAI_ERR_INVALID_ARG"

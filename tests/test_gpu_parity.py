@@ -427,7 +427,8 @@ def check_binarized(bits_gpu, as_gpu, x, what):
 
 
 @pytest.mark.parametrize("m,k", [(1, 128), (3, 640), (5, 4096), (512, 4096), (1, 17408),
-                                 (7, 5120), (1300, 256), (2, 1152)])
+                                 (7, 5120), (1300, 256), (2, 1152), (4096, 4096),
+                                 (2500, 640), (10000, 128)])
 def test_binarize_rows(m, k):
     t = torch()
     x = synth.gen_x(130 + m, m, k)
@@ -492,6 +493,60 @@ def test_xnor_from_fp16_activations():
         assert_close(host(y.t)[np.ix_(ms, ns)], sc * y1, sc * n1, "xnor from fp16 m=%d" % m)
         d.check()
         y.check()
+
+
+# ------------------------------------------------- signed Hadamard rotation
+def hadamard_bound(ref, x, block):
+    """FP32 butterflies: each of the log2(block) stages rounds a partial sum
+    bounded by the block's sum |x|, and the 1/sqrt(block) constant and product
+    round once more each; the FP16 store adds half an ulp of the result
+    (2^-11 relative, 2^-25 absolute for subnormals)."""
+    m, k = x.shape
+    s = np.abs(x.view(np.float16).astype(np.float64)).reshape(m, k // block, block).sum(axis=2)
+    s = np.repeat(s, block, axis=1) / np.sqrt(block)
+    e = (np.log2(block) + 3) * 2.0 ** -24 * s
+    return e + 2.0 ** -11 * (np.abs(ref) + e) + 2.0 ** -25
+
+
+HADAMARD_CASES = [(1, 128, 128, False), (3, 640, 128, True), (5, 5120, 128, True),
+                  (2, 5120, 1024, True), (4, 17408, 512, True), (7, 1024, 256, True),
+                  (3, 256, 8, True), (2, 384, 32, True), (1, 2048, 64, False),
+                  (512, 5120, 128, True), (33, 17408, 1024, False)]
+
+
+@pytest.mark.parametrize("m,k,block,signed", HADAMARD_CASES)
+def test_hadamard(m, k, block, signed):
+    t = torch()
+    x = synth.gen_x(190 + m, m, k)
+    bits = synth.gen_binary_words(191 + k, 1, k)[0] if signed else None
+    out = Guarded((m, k), t.float16)
+    sb.bonsai_hadamard(dev(x), out.t, block, None if bits is None else dev(bits.view(np.int32)))
+    assert sb.bonsai_check_async() == 0
+    ref = oracle.hadamard(x, block, bits)
+    bad, first, worst = oracle.compare_f16(host(out.t), ref, hadamard_bound(ref, x, block), 1.0)
+    assert bad == 0, ("hadamard", m, k, block, bad, first, worst)
+    out.check()
+
+
+def test_hadamard_in_place_and_involution():
+    """In place gives the same bits as out of place; with all signs +1 and an
+    even log2(block), rotating twice returns x up to the two roundings."""
+    t = torch()
+    m, k = 6, 4096
+    x = synth.gen_x(195, m, k)
+    for block in (256, 1024):
+        a = dev(x)
+        b = t.empty_like(a)
+        sb.bonsai_hadamard(a, b, block)
+        sb.bonsai_hadamard(a, a, block)
+        assert sb.bonsai_check_async() == 0
+        assert np.array_equal(host(a), host(b))
+        back = t.empty_like(a)
+        sb.bonsai_hadamard(a, back, block)
+        assert sb.bonsai_check_async() == 0
+        xv = x.view(np.float16).astype(np.float64)
+        err = np.abs(host(back).view(np.float16).astype(np.float64) - xv)
+        assert np.all(err <= 4 * 2.0 ** -11 * np.sqrt(np.mean(xv ** 2)) + 2.0 ** -11 * np.abs(xv))
 
 
 # ------------------------------------------------------------ graph capture
