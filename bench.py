@@ -240,6 +240,18 @@ def graph_time(fn_steps, steps, warmup, clocks=None):
     return e0.elapsed_time(e1)
 
 
+def step_graph(fn):
+    """A CUDA graph holding the launches of one call of fn (called eagerly
+    at least once before, so one-time setup stays outside the capture)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    return g
+
+
 # ---------------------------------------------------------------- workloads
 class GemvWorkload:
     """Decode product M=1 over rotating weight replicas."""
@@ -474,12 +486,15 @@ class GemmWorkload:
         sb.bonsai_gemm(self.w, self.x, self.y)
 
     def measure(self, steps, warmup, clocks=None):
-        """Per-step event pairs around the product; an L2 flush (a 512 MB
+        """Per-step event pairs around one replay of a CUDA graph that holds
+        the step's launches (so a step of several kernels runs back to back,
+        with no host gaps inside the timed pair); an L2 flush (a 512 MB
         write) runs between steps, outside the timed pairs."""
         import torch
         for _ in range(warmup):
             self.call()
         torch.cuda.synchronize()
+        g = step_graph(self.call)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
         if clocks:
@@ -487,7 +502,7 @@ class GemmWorkload:
         for a, b in ev:
             self.flush.zero_()
             a.record()
-            self.call()
+            g.replay()
             b.record()
         torch.cuda.synchronize()
         if clocks:
@@ -706,12 +721,13 @@ class XnorFp16Workload(XnorWorkload):
         r = XnorWorkload.measure(self, steps, warmup, clocks)
         r["launches"] = 2 * steps
         # the binarisation kernel alone, same flush discipline
+        g = step_graph(self.binarize)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
         for a, b in ev:
             self.flush.zero_()
             a.record()
-            self.binarize()
+            g.replay()
             b.record()
         torch.cuda.synchronize()
         r["binarize_ms"] = sum(a.elapsed_time(b) for a, b in ev) / steps

@@ -110,6 +110,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         "=r"(v[30]), "=r"(v[31])                                                           \
       : "r"(taddr))
 
+// Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
+// without waiting; issued in pieces of at most 32 KB.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, long long bytes) {
+  const char* p = static_cast<const char*>(ptr);
+  for (long long off = 0; off < bytes; off += 32768) {
+    const uint32_t len = (uint32_t)(bytes - off < 32768 ? bytes - off : 32768);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + off), "r"(len) : "memory");
+  }
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -261,10 +271,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------ X producer ------------------------------
     if (lane == 0) {
       pdl_wait();
+      // The dequantisers read packed weight rows straight from global memory
+      // one 64-byte block ahead; with the rows of this tile and of the next
+      // one already on their way to L2, those reads do not wait on DRAM. A
+      // tile's rows are contiguous (row_bytes apart).
+      auto prefetch_tile = [&](int tile) {
+        if (tile >= p.tiles) return;
+        const int n0 = (tile / p.tok_tiles) * BM;
+        const int rows = p.n - n0 < BM ? p.n - n0 : BM;
+        prefetch_l2(p.w + (long long)n0 * p.row_bytes, (long long)rows * p.row_bytes);
+      };
+      prefetch_tile(blockIdx.x);
       uint32_t g = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
         const int m0 = (tile % p.tok_tiles) * BN;
+        prefetch_tile(tile + gridDim.x);
         for (int kk = 0; kk < p.nk; ++kk, ++g) {
           const int s = g % B_STAGES;
           const uint32_t ph = (g / B_STAGES) & 1;
