@@ -49,7 +49,6 @@ constexpr int TMEM_COLS = 512;
 constexpr int THREADS = 512;
 constexpr int W_TMA = 0, W_MMA = 1, W_TMEM = 2, W_EPI = 4, W_DQ = 8;
 constexpr int LUT_BYTES = 256 * 128;    // byte -> five 2-bit digits, one copy per lane
-constexpr int PLUT_BYTES = 16 * 128;    // digit pair -> FP16 pair of -1/0/+1, per lane
 constexpr int BAR_BYTES = 256;
 
 struct Params {
@@ -169,11 +168,60 @@ __device__ __forceinline__ void dq_binary(uint2 wv, uint32_t s2, uint32_t dst_ro
   }
 }
 
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Ternary digit pairs without a table: a digit c (0..2) placed in mantissa
+// bits p, p+1 of a half whose exponent field is 25 - p is the value
+// 2^(10-p) + c; minus the same half with c = 1 it is c - 1 in {-1, 0, +1},
+// exactly (both operands lie within a factor of two). The product with the
+// FP16 scale is then exact as well. Five pair shapes occur: digits (d, d+1)
+// of one byte for d = 0..3 (p = 2d low, 2d+2 high, from the byte's digit
+// word in both halves) and digit 4 of a byte with digit 0 of the next.
+__host__ __device__ constexpr uint32_t ter_exp(int p) { return uint32_t(25 - p) << 10; }
+__host__ __device__ constexpr int ter_plo(int d) { return d < 4 ? 2 * d : 8; }
+__host__ __device__ constexpr int ter_phi(int d) { return d < 4 ? 2 * d + 2 : 0; }
+__host__ __device__ constexpr uint32_t ter_mask(int d) {
+  return (3u << ter_plo(d)) | (3u << (ter_phi(d) + 16));
+}
+__host__ __device__ constexpr uint32_t ter_e(int d) {
+  return ter_exp(ter_plo(d)) | (ter_exp(ter_phi(d)) << 16);
+}
+__host__ __device__ constexpr uint32_t ter_one(int d) {
+  return ter_e(d) | (1u << ter_plo(d)) | (1u << (ter_phi(d) + 16));
+}
+
+// Exponent fields and c = 1 operands of the five pair shapes, in registers
+// (LOP3 takes one immediate; HSUB2 subtracts a register).
+struct TerConsts {
+  uint32_t e[5], one[5];
+  __device__ __forceinline__ TerConsts() {
+#pragma unroll
+    for (int d = 0; d < 5; ++d) {
+      uint32_t a = ter_e(d), b = ter_one(d);
+      asm volatile("" : "+r"(a), "+r"(b));  // keep them in registers
+      e[d] = a;
+      one[d] = b;
+    }
+  }
+};
+
+template <int D>
+__device__ __forceinline__ uint32_t ter_pair(uint32_t w, uint32_t s2, const TerConsts& K) {
+  uint32_t u;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(u) : "r"(w), "n"(ter_mask(D)), "r"(K.e[D]));
+  return hmul2_u32(hsub2_u32(u, K.one[D]), s2);
+}
+
 // Ternary k-step kk = 5u + V covers codes 64V..64V+63 of the 64-byte block u
 // (320 codes): they start in byte 64V/5 at digit 64V%5, known at compile time.
+// The byte table gives a byte's five digits (digit i at bits 2i, 2i+1).
 template <int V>
 __device__ __forceinline__ void dq_ternary(const uint32_t (&wd)[16], uint32_t s2, uint32_t lut,
-                                           uint32_t plut, uint32_t dst_row, int sw) {
+                                           const TerConsts& K, uint32_t dst_row, int sw) {
   constexpr int T0 = 64 * V;
   constexpr int B0 = T0 / 5;
   constexpr int B1 = (T0 + 63) / 5;
@@ -183,20 +231,25 @@ __device__ __forceinline__ void dq_ternary(const uint32_t (&wd)[16], uint32_t s2
     const uint32_t byte = (wd[b >> 2] >> (8 * (b & 3))) & 0xFFu;
     F[b - B0] = lds32(lut + byte * 128u);
   }
-  // all 32 pair lookups first, so their latencies overlap
   uint32_t pv[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int T = T0 + 2 * j;
     const int b = T / 5 - B0, d = T % 5;
-    const uint32_t nib = d < 4 ? (F[b] >> (2 * d)) & 0xFu
-                               : ((F[b] >> 8) | ((F[b + 1] & 3u) << 2));
-    pv[j] = lds32(plut + nib * 128u);
+    // the pair's digit word: the byte's digits in both halves, or (d = 4)
+    // this byte's digits low and the next byte's high
+    const uint32_t w = d < 4 ? __byte_perm(F[b], 0u, 0x1010) : __byte_perm(F[b], F[b + 1], 0x5410);
+    switch (d) {
+      case 0: pv[j] = ter_pair<0>(w, s2, K); break;
+      case 1: pv[j] = ter_pair<1>(w, s2, K); break;
+      case 2: pv[j] = ter_pair<2>(w, s2, K); break;
+      case 3: pv[j] = ter_pair<3>(w, s2, K); break;
+      default: pv[j] = ter_pair<4>(w, s2, K); break;
+    }
   }
 #pragma unroll
   for (int c = 0; c < 8; ++c)
-    sts128(dst_row + ((c ^ sw) << 4), hmul2_u32(pv[4 * c], s2), hmul2_u32(pv[4 * c + 1], s2),
-           hmul2_u32(pv[4 * c + 2], s2), hmul2_u32(pv[4 * c + 3], s2));
+    sts128(dst_row + ((c ^ sw) << 4), pv[4 * c], pv[4 * c + 1], pv[4 * c + 2], pv[4 * c + 3]);
 }
 
 template <int FMT>
@@ -208,8 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + A_STAGES * A_BYTES;
   const uint32_t sLut = sB + B_STAGES * B_BYTES;
-  const uint32_t sPlut = sLut + LUT_BYTES;
-  const uint32_t sBar = FMT == BONSAI_FMT_TERNARY ? sPlut + PLUT_BYTES : sLut;
+  const uint32_t sBar = FMT == BONSAI_FMT_TERNARY ? sLut + LUT_BYTES : sLut;
   // full_a[s]: the 4 dequantiser warps of the k-step's parity group;
   // full_b[s]: the X copy (transaction bytes); empty_a / empty_b: the MMAs
   // that read the stage have completed.
@@ -249,12 +301,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int d = 0; d < 5; ++d) { v |= uint32_t(r % 3) << (2 * d); r /= 3; }
       }
       asm volatile("st.shared.b32 [%0], %1;" ::"r"(sLut + e * 128 + ln * 4), "r"(v) : "memory");
-    }
-    for (int i = t; i < 16 * 32; i += 256) {
-      const int e = i >> 5, ln = i & 31;
-      const uint16_t val[4] = {0xBC00, 0x0000, 0x3C00, 0x0000};  // digit -> -1, 0, +1
-      const uint32_t v = uint32_t(val[e & 3]) | (uint32_t(val[e >> 2]) << 16);
-      asm volatile("st.shared.b32 [%0], %1;" ::"r"(sPlut + e * 128 + ln * 4), "r"(v) : "memory");
     }
   }
   if (warp == W_TMEM) {
@@ -380,12 +426,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t h = dq >> 2;         // parity group: even / odd k-steps
     const int r = (dq & 3) * 32 + lane; // feature row within the tile
     const int sw = r & 7;
-    const uint32_t lut = sLut + lane * 4, plut = sPlut + lane * 4;
+    const uint32_t lut = sLut + lane * 4;
+    const TerConsts K;
     // Ternary: the packed row is read in 64-byte blocks (320 codes = 5
     // k-steps) one block ahead, so the load latency hides behind the
     // dequantisation of the current block; the block's group scales travel
-    // with it. Binary: 8 bytes and one scale per k-step, loaded directly
-    // (measured faster than the block scheme for this cheap expansion).
+    // with it.
     constexpr int KPB = 5;
     const int nblk = (p.nk + KPB - 1) / KPB;
     uint32_t cur[16], nxt[16];
@@ -407,22 +453,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         dst[4 * i] = q4.x; dst[4 * i + 1] = q4.y; dst[4 * i + 2] = q4.z; dst[4 * i + 3] = q4.w;
       }
     };
+    // Binary: 8 bytes and one scale per k-step, loaded one own k-step ahead
+    // (k % 128 == 0 makes nk even, so this warp's k-steps are kk = h, h+2,
+    // ... in every tile).
+    uint2 nwv = make_uint2(0u, 0u);
+    uint32_t ns2 = 0;
+    auto load_bin = [&](int tile, int kk) {
+      const int n = (tile / p.tok_tiles) * BM + r;
+      const bool nok = n < p.n;
+      nwv = *reinterpret_cast<const uint2*>(p.w + (long long)(nok ? n : 0) * p.row_bytes + 8 * kk);
+      const __half sc = p.scales[(size_t)(nok ? n : 0) * p.G + (kk >> 1)];
+      ns2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;  // rows past n: scale 0
+    };
+    if constexpr (FMT == BONSAI_FMT_BINARY)
+      if ((int)blockIdx.x < p.tiles) load_bin(blockIdx.x, (int)h);
     uint32_t g = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-      const int n = (tile / p.tok_tiles) * BM + r;
-      const bool nok = n < p.n;
-      const uint8_t* wrow = p.w + (long long)(nok ? n : 0) * p.row_bytes;
-      const __half* srow = p.scales + (size_t)(nok ? n : 0) * p.G;
       for (int kk = 0; kk < p.nk; ++kk, ++g) {
         if ((g & 1) != h) continue;
         const int s = g % A_STAGES;
         const uint32_t ph = (g / A_STAGES) & 1;
         const uint32_t dst = sA + s * A_BYTES + r * 128;
         if constexpr (FMT == BONSAI_FMT_BINARY) {
-          const uint2 wv = *reinterpret_cast<const uint2*>(wrow + 8 * kk);
-          const __half sc = srow[kk >> 1];
-          const uint32_t s2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;
+          const uint2 wv = nwv;
+          const uint32_t s2 = ns2;
+          const bool last = kk + 2 >= p.nk;
+          const int nt = last ? tile + (int)gridDim.x : tile;
+          if (nt < p.tiles) load_bin(nt, last ? (int)h : kk + 2);
           if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
           dq_binary(wv, s2, dst, sw);
         } else {
@@ -451,11 +509,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t s2 = sc * 0x10001u;  // rows past n carry scale 0
           if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
           switch (kk % 5) {
-            case 0: dq_ternary<0>(cur, s2, lut, plut, dst, sw); break;
-            case 1: dq_ternary<1>(cur, s2, lut, plut, dst, sw); break;
-            case 2: dq_ternary<2>(cur, s2, lut, plut, dst, sw); break;
-            case 3: dq_ternary<3>(cur, s2, lut, plut, dst, sw); break;
-            default: dq_ternary<4>(cur, s2, lut, plut, dst, sw); break;
+            case 0: dq_ternary<0>(cur, s2, lut, K, dst, sw); break;
+            case 1: dq_ternary<1>(cur, s2, lut, K, dst, sw); break;
+            case 2: dq_ternary<2>(cur, s2, lut, K, dst, sw); break;
+            case 3: dq_ternary<3>(cur, s2, lut, K, dst, sw); break;
+            default: dq_ternary<4>(cur, s2, lut, K, dst, sw); break;
           }
         }
         fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
@@ -502,7 +560,7 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
 
   const bool ter = w->format == BONSAI_FMT_TERNARY;
   const int smem = ter ? Ring<BONSAI_FMT_TERNARY>::A * A_BYTES + Ring<BONSAI_FMT_TERNARY>::B * B_BYTES +
-                             LUT_BYTES + PLUT_BYTES + BAR_BYTES
+                             LUT_BYTES + BAR_BYTES
                        : Ring<BONSAI_FMT_BINARY>::A * A_BYTES + Ring<BONSAI_FMT_BINARY>::B * B_BYTES +
                              BAR_BYTES;
   if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
