@@ -453,34 +453,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         dst[4 * i] = q4.x; dst[4 * i + 1] = q4.y; dst[4 * i + 2] = q4.z; dst[4 * i + 3] = q4.w;
       }
     };
-    // Binary: 8 bytes and one scale per k-step, loaded one own k-step ahead
-    // (k % 128 == 0 makes nk even, so this warp's k-steps are kk = h, h+2,
-    // ... in every tile).
-    uint2 nwv = make_uint2(0u, 0u);
-    uint32_t ns2 = 0;
-    auto load_bin = [&](int tile, int kk) {
-      const int n = (tile / p.tok_tiles) * BM + r;
-      const bool nok = n < p.n;
-      nwv = *reinterpret_cast<const uint2*>(p.w + (long long)(nok ? n : 0) * p.row_bytes + 8 * kk);
-      const __half sc = p.scales[(size_t)(nok ? n : 0) * p.G + (kk >> 1)];
-      ns2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;  // rows past n: scale 0
-    };
-    if constexpr (FMT == BONSAI_FMT_BINARY)
-      if ((int)blockIdx.x < p.tiles) load_bin(blockIdx.x, (int)h);
     uint32_t g = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      const int n = (tile / p.tok_tiles) * BM + r;
+      const bool nok = n < p.n;
+      const uint8_t* wrow = p.w + (long long)(nok ? n : 0) * p.row_bytes;
+      const __half* srow = p.scales + (size_t)(nok ? n : 0) * p.G;
       for (int kk = 0; kk < p.nk; ++kk, ++g) {
         if ((g & 1) != h) continue;
         const int s = g % A_STAGES;
         const uint32_t ph = (g / A_STAGES) & 1;
         const uint32_t dst = sA + s * A_BYTES + r * 128;
         if constexpr (FMT == BONSAI_FMT_BINARY) {
-          const uint2 wv = nwv;
-          const uint32_t s2 = ns2;
-          const bool last = kk + 2 >= p.nk;
-          const int nt = last ? tile + (int)gridDim.x : tile;
-          if (nt < p.tiles) load_bin(nt, last ? (int)h : kk + 2);
+          // 8 bytes and one scale per k-step, loaded directly (measured
+          // faster than loading one own k-step or one 64-byte block ahead)
+          const uint2 wv = *reinterpret_cast<const uint2*>(wrow + 8 * kk);
+          const __half sc = srow[kk >> 1];
+          const uint32_t s2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;
           if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
           dq_binary(wv, s2, dst, sw);
         } else {
