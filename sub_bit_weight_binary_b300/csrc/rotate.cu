@@ -83,11 +83,11 @@ __global__ void __launch_bounds__(kThreads) hadamard_kernel(
 #pragma unroll
     for (int s = 0; s < kLaneStages; ++s) {
       const int mask = 1 << s;
-      const bool upper = lane & mask;
+      const float sgn = (lane & mask) ? -1.f : 1.f;  // upper lane: p - v, lower: v + p
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float p = __shfl_xor_sync(0xFFFFFFFFu, v[i], mask);
-        v[i] = upper ? p - v[i] : v[i] + p;
+        v[i] = fmaf(sgn, v[i], p);  // one rounding, as the plain sum or difference
       }
     }
     if constexpr (LOGB > 8) {
