@@ -626,7 +626,8 @@ class HadamardWorkload:
         a = self.unit_bytes() / (r["kernel_ms"] / 1e3) / 1e9
         return {"bound": "hbm", "kernel": "hadamard_kernel<7>", "achieved": round(a, 1),
                 "peak": pk["hbm"], "unit": "GB/s", "frac": round(a / pk["hbm"], 4),
-                "traffic": None, "peak_src": "%s HBM copy (burst)" % pk["src"],
+                "traffic": profiled_traffic("hadamard_m512_k5120_b128.md"),
+                "peak_src": "%s HBM copy (burst)" % pk["src"],
                 "bytes_per_launch": self.unit_bytes()}
 
     def config(self):
@@ -741,7 +742,8 @@ class XnorFp16Workload(XnorWorkload):
         nbytes = self.m * self.k * 2 + self.m * self.k // 8 + self.m * 2
         out["binarize"] = {"ms": round(r["binarize_ms"], 6), "bytes": nbytes,
                            "achieved_gbs": round(nbytes / (r["binarize_ms"] / 1e3) / 1e9, 1),
-                           "peak_gbs": pk["hbm"]}
+                           "peak_gbs": pk["hbm"],
+                           "traffic": profiled_traffic("binarize_m512_k4096.md")}
         return out
 
 
