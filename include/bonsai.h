@@ -140,6 +140,21 @@ bonsai_status bonsai_pack_ternary(const int8_t* codes, int64_t rows, int64_t k,
 bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x,
                           uint16_t* y, bonsai_stream stream);
 
+/* bonsai_gemv with the activations and the result in host memory: enqueues
+ * on `stream` the copy x_host -> x_dev (k FP16 values), the decode product
+ * into y_dev, and the copy y_dev -> y_host (n FP16 values), then returns.
+ * For a decode loop that samples on the host: one call per token, no other
+ * API call in between. Synchronise the stream (or call bonsai_check_async)
+ * before reading y_host. x_host and y_host should be page-locked
+ * (cudaHostAlloc / pinned tensors); pageable memory works but each copy
+ * then waits for the host. x_dev, y_dev: device buffers of k and n FP16
+ * values, 16-byte aligned, owned by the caller (the library allocates
+ * nothing). Errors as bonsai_gemv; BONSAI_ERR_CUDA if a copy cannot be
+ * enqueued. */
+bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
+                               uint16_t* x_dev, uint16_t* y_dev, uint16_t* y_host,
+                               bonsai_stream stream);
+
 /* Decode product with K split across thread blocks, for matrices with few
  * rows (n <= 8192), computing the same y as bonsai_gemv (to the same error
  * bound, not bit-identically: the sums are ordered differently). The pages

@@ -60,6 +60,8 @@ def lib():
             f.restype = S
         L.bonsai_gemv.argtypes = [W, P, P, P]
         L.bonsai_gemv.restype = S
+        L.bonsai_gemv_host.argtypes = [W, P, P, P, P, P]
+        L.bonsai_gemv_host.restype = S
         L.bonsai_gemv_splitk_static.argtypes = [W, P, P, P]
         L.bonsai_gemv_splitk_static.restype = S
         L.bonsai_gemm.argtypes = [W, P, I64, P, P]
@@ -127,11 +129,21 @@ class Weights:
             int(self.packed.numel() // self.n)
 
     def c_struct(self) -> bonsai_weights_t:
-        import torch
-        return bonsai_weights_t(
-            self.format, self.flags, self.n, self.k, self.row_bytes,
-            _ptr(self.packed, (torch.uint8, torch.int32, torch.int8), "packed"),
-            _ptr(self.scales, (torch.float16, torch.int16), "scales"))
+        """The C struct, built and checked once; assigning any field rebuilds
+        it (the tensors' storage is assumed not to move while held here)."""
+        cs = self.__dict__.get("_cs")
+        if cs is None:
+            import torch
+            cs = bonsai_weights_t(
+                self.format, self.flags, self.n, self.k, self.row_bytes,
+                _ptr(self.packed, (torch.uint8, torch.int32, torch.int8), "packed"),
+                _ptr(self.scales, (torch.float16, torch.int16), "scales"))
+            self.__dict__["_cs"] = cs
+        return cs
+
+    def __setattr__(self, name, value):
+        self.__dict__.pop("_cs", None)
+        object.__setattr__(self, name, value)
 
 
 # ---------------------------------------------------------------------------
@@ -162,6 +174,27 @@ def bonsai_gemv(w: Weights, x, y, stream=None):
     ws = w.c_struct()
     _ok(lib().bonsai_gemv(C.byref(ws), _ptr(x, (torch.float16,), "x"),
                           _ptr(y, (torch.float16,), "y"), _stream(stream)), "bonsai_gemv")
+
+
+def _host_ptr(t, name):
+    import torch
+    if t.is_cuda:
+        raise ValueError("%s must be a host (preferably pinned) tensor" % name)
+    if t.dtype != torch.float16 or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous float16 tensor" % name)
+    return t.data_ptr()
+
+
+def bonsai_gemv_host(w: Weights, x_host, x_dev, y_dev, y_host, stream=None):
+    """Host x in, host y out: enqueue x_host -> x_dev, the decode product into
+    y_dev and y_dev -> y_host on the stream (synchronise before reading y_host)."""
+    import torch
+    if x_host.numel() != w.k or y_host.numel() != w.n:
+        raise ValueError("x_host must hold k and y_host n values")
+    _ok(lib().bonsai_gemv_host(C.byref(w.c_struct()), _host_ptr(x_host, "x_host"),
+                               _ptr(x_dev, (torch.float16,), "x_dev"),
+                               _ptr(y_dev, (torch.float16,), "y_dev"),
+                               _host_ptr(y_host, "y_host"), _stream(stream)), "bonsai_gemv_host")
 
 
 def bonsai_gemv_splitk_static(w: Weights, x, y, stream=None):

@@ -95,12 +95,45 @@ bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType type, void* base
     return reinterpret_cast<EncodeTiled>(f);
   }();
   if (!fn) return false;
+  // A map depends only on these arguments, so the maps of recent calls are
+  // kept (a decode loop encodes the same weights every token). A reused
+  // address with the same shape gets the same, still correct, map.
+  struct Key {
+    CUtensorMapDataType type;
+    void* base;
+    uint64_t dim0, dim1, stride1;
+    uint32_t box0, box1;
+    CUtensorMapSwizzle swizzle;
+    bool operator==(const Key& o) const {
+      return type == o.type && base == o.base && dim0 == o.dim0 && dim1 == o.dim1 &&
+             stride1 == o.stride1 && box0 == o.box0 && box1 == o.box1 && swizzle == o.swizzle;
+    }
+  };
+  struct Entry { Key key; CUtensorMap map; bool used; };
+  constexpr int kEntries = 64;
+  static Entry cache[kEntries];
+  static int next = 0;
+  static std::mutex mu;
+  const Key key{type, base, dim0, dim1, stride1_bytes, box0, box1, swizzle};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : cache)
+      if (e.used && e.key == key) {
+        *map = e.map;
+        return true;
+      }
+  }
   const cuuint64_t gdim[2] = {dim0, dim1};
   const cuuint64_t gstride[1] = {stride1_bytes};
   const cuuint32_t box[2] = {box0, box1};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, type, 2, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(map, type, 2, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[next] = Entry{key, *map, true};
+  next = (next + 1) % kEntries;
+  return true;
 }
 
 }  // namespace bonsai
@@ -186,6 +219,24 @@ bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x, uint16_t* 
   if (!x || !y) return BONSAI_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
   return gemv_launch(w, x, 1, y, false, stream);
+}
+
+bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
+                               uint16_t* x_dev, uint16_t* y_dev, uint16_t* y_host,
+                               bonsai_stream stream) {
+  bonsai_status st = check_weights(w);
+  if (st != BONSAI_OK) return st;
+  if (!x_host || !x_dev || !y_dev || !y_host) return BONSAI_ERR_INVALID_ARG;
+  if (!aligned16(x_dev) || !aligned16(y_dev)) return BONSAI_ERR_ALIGN;
+  if (cudaMemcpyAsync(x_dev, x_host, (size_t)w->k * 2, cudaMemcpyHostToDevice, stream) !=
+      cudaSuccess)
+    return BONSAI_ERR_CUDA;
+  st = gemv_launch(w, x_dev, 1, y_dev, false, stream);
+  if (st != BONSAI_OK) return st;
+  if (cudaMemcpyAsync(y_host, y_dev, (size_t)w->n * 2, cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return BONSAI_ERR_CUDA;
+  return BONSAI_OK;
 }
 
 bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t* x, uint16_t* y,

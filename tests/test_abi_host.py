@@ -30,7 +30,7 @@ def test_headers_declare_the_boundary():
     names = declared("bonsai.h")
     for f in ("bonsai_packed_row_bytes", "bonsai_pack_binary", "bonsai_pack_ternary",
               "bonsai_gemv", "bonsai_gemm", "bonsai_xnor_gemm", "bonsai_binarize_activations",
-              "bonsai_gemm_swiglu", "bonsai_hadamard", "bonsai_check_async",
+              "bonsai_gemm_swiglu", "bonsai_hadamard", "bonsai_gemv_host", "bonsai_check_async",
               "bonsai_status_string"):
         assert f in names
 
@@ -115,6 +115,11 @@ def test_other_host_checks(libs):
     w24 = W(n=24)
     assert sb.STATUS[L.bonsai_gemm_swiglu(C.byref(w24), 0x30000, 4, 0x40000, None)] \
         == "BONSAI_ERR_SHAPE"
+    gh = L.bonsai_gemv_host
+    assert sb.STATUS[gh(C.byref(w), None, 0x30000, 0x40000, 0x50000, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[gh(C.byref(w), 0x10000, 0x30008, 0x40000, 0x50000, None)] == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[gh(C.byref(W(fmt=3)), 0x10000, 0x30000, 0x40000, 0x50000, None)] \
+        == "BONSAI_ERR_INVALID_ARG"
     hd = L.bonsai_hadamard
     assert sb.STATUS[hd(None, 2, 256, 128, None, 0x50000, None)] == "BONSAI_ERR_INVALID_ARG"
     assert sb.STATUS[hd(0x40000, 2, 256, 96, None, 0x50000, None)] == "BONSAI_ERR_UNSUPPORTED"
@@ -168,3 +173,13 @@ def test_interleave_gate_up_row_order():
     assert np.array_equal(tout.numpy(), out)
     with pytest.raises(ValueError):
         sb.interleave_gate_up(gate[:12], up[:12])
+
+
+def test_weights_struct_is_cached_and_rebuilt_on_assignment():
+    import torch
+    w = sb.Weights(1, 4, 128, torch.zeros(4, 16, dtype=torch.uint8),
+                   torch.zeros(4, 1, dtype=torch.float16))
+    w.__dict__["_cs"] = "cached"           # stands for a built struct
+    assert w.c_struct() == "cached"
+    w.flags = 1                            # any assignment drops it
+    assert "_cs" not in w.__dict__

@@ -340,6 +340,31 @@ def test_gemm_down_projection_sampled(fmt):
     y.check()
 
 
+@pytest.mark.parametrize("fmt,n,k", [(TER, 17408, 5120), (BIN, 1024, 1024), (TER, 33, 640)])
+def test_gemv_host_buffers(fmt, n, k):
+    """bonsai_gemv_host (host x in, host y out, one call) gives the bits of
+    bonsai_gemv and meets the oracle's bound; pinned and pageable host memory."""
+    t = torch()
+    w, packed, scales = weights(fmt, 200 + n, n, k)
+    x = synth.gen_x(201, 1, k)[0]
+    y_ref_dev = t.empty(n, dtype=t.float16, device="cuda")
+    sb.bonsai_gemv(w, dev(x), y_ref_dev)
+    for pinned in (True, False):
+        x_host = t.from_numpy(x.view(np.float16).copy())
+        y_host = t.zeros(n, dtype=t.float16)
+        if pinned:
+            x_host, y_host = x_host.pin_memory(), y_host.pin_memory()
+        x_dev = t.empty(k, dtype=t.float16, device="cuda")
+        y_dev = t.empty(n, dtype=t.float16, device="cuda")
+        sb.bonsai_gemv_host(w, x_host, x_dev, y_dev, y_host)
+        assert sb.bonsai_check_async() == 0
+        yh = y_host.numpy().view(np.uint16)
+        assert np.array_equal(yh, host(y_ref_dev))
+        ns = sample_idx(n, [0, n - 1], 64, 11)
+        y_ref, nrm = oracle.linear(fmt, packed, scales, x, n_sel=ns)
+        assert_close(yh[ns][None, :], y_ref, nrm, "gemv host buffers")
+
+
 # ------------------------------------------ gated feed-forward (SwiGLU)
 SWIGLU_CASES = [(BIN, 8, 128, 1), (TER, 8, 128, 1), (BIN, 24, 640, 3), (TER, 40, 640, 5),
                 (TER, 56, 1152, 8), (BIN, 200, 1024, 9), (TER, 136, 1024, 300),
