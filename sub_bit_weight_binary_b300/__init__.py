@@ -197,6 +197,32 @@ def bonsai_gemv_host(w: Weights, x_host, x_dev, y_dev, y_host, stream=None):
                                _host_ptr(y_host, "y_host"), _stream(stream)), "bonsai_gemv_host")
 
 
+class GemvHostPlan:
+    """A decode step with host buffers, prepared once: the copies and the
+    product of bonsai_gemv_host are captured in a CUDA graph, and each call
+    replays it (one launch per token; the contents of x_host may change
+    between calls, the buffers themselves may not). Synchronise before
+    reading y_host. x_host and y_host must be pinned."""
+
+    def __init__(self, w: Weights, x_host, x_dev, y_dev, y_host):
+        import torch
+        if not (x_host.is_pinned() and y_host.is_pinned()):
+            raise ValueError("x_host and y_host must be pinned host tensors")
+        self._keep = (w, x_host, x_dev, y_dev, y_host)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):  # eager call first: one-time setup stays outside the capture
+            bonsai_gemv_host(w, x_host, x_dev, y_dev, y_host)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            bonsai_gemv_host(w, x_host, x_dev, y_dev, y_host)
+
+    def __call__(self):
+        self.graph.replay()
+
+
 def bonsai_gemv_splitk_static(w: Weights, x, y, stream=None):
     """bonsai_gemv with K split over thread blocks and a fixed device scratch
     array (no allocation); n <= 8192, calls on one device must not overlap."""

@@ -363,6 +363,17 @@ def test_gemv_host_buffers(fmt, n, k):
         ns = sample_idx(n, [0, n - 1], 64, 11)
         y_ref, nrm = oracle.linear(fmt, packed, scales, x, n_sel=ns)
         assert_close(yh[ns][None, :], y_ref, nrm, "gemv host buffers")
+        if pinned:  # the prepared (graph-replayed) form reads x_host anew per call
+            plan = sb.GemvHostPlan(w, x_host, x_dev, y_dev, y_host)
+            x2 = synth.gen_x(202, 1, k)[0]
+            x_host.copy_(t.from_numpy(x2.view(np.float16).copy()))
+            y_host.zero_()
+            plan()
+            t.cuda.synchronize()
+            y2_dev = t.empty(n, dtype=t.float16, device="cuda")
+            sb.bonsai_gemv(w, dev(x2), y2_dev)
+            assert sb.bonsai_check_async() == 0
+            assert np.array_equal(y_host.numpy().view(np.uint16), host(y2_dev))
 
 
 # ------------------------------------------ gated feed-forward (SwiGLU)
