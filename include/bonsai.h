@@ -145,12 +145,14 @@ bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x,
  * into y_dev, and the copy y_dev -> y_host (n FP16 values), then returns.
  * For a decode loop that samples on the host: one call per token, no other
  * API call in between. Synchronise the stream (or call bonsai_check_async)
- * before reading y_host. x_host and y_host should be page-locked
- * (cudaHostAlloc / pinned tensors); pageable memory works but each copy
- * then waits for the host. x_dev, y_dev: device buffers of k and n FP16
- * values, 16-byte aligned, owned by the caller (the library allocates
- * nothing). Errors as bonsai_gemv; BONSAI_ERR_CUDA if a copy cannot be
- * enqueued. */
+ * before reading y_host. With page-locked, 16-byte aligned host buffers
+ * (cudaHostAlloc / pinned tensors) no copy engine is used: a small kernel
+ * reads x_host through its device mapping into x_dev, and the product
+ * kernel writes y straight into y_host (y_dev is then left untouched).
+ * Other host memory is copied with cudaMemcpyAsync (each copy then waits
+ * for the host). x_dev, y_dev: device buffers of k and n FP16 values,
+ * 16-byte aligned, owned by the caller (the library allocates nothing).
+ * Errors as bonsai_gemv; BONSAI_ERR_CUDA if a copy cannot be enqueued. */
 bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
                                uint16_t* x_dev, uint16_t* y_dev, uint16_t* y_host,
                                bonsai_stream stream);

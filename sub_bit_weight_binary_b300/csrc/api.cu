@@ -12,6 +12,7 @@ bonsai_status pack_ternary_launch(const int8_t*, int64_t, int64_t, void*, int64_
 bonsai_status gemv_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, bool,
                           cudaStream_t);
 bonsai_status splitk_launch(const bonsai_weights*, const uint16_t*, uint16_t*, cudaStream_t);
+bonsai_status stage_x_launch(const uint16_t*, uint16_t*, int64_t, cudaStream_t);
 bonsai_status gemm_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, bool,
                           cudaStream_t);
 bonsai_status xnor_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
@@ -228,9 +229,29 @@ bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
   if (st != BONSAI_OK) return st;
   if (!x_host || !x_dev || !y_dev || !y_host) return BONSAI_ERR_INVALID_ARG;
   if (!aligned16(x_dev) || !aligned16(y_dev)) return BONSAI_ERR_ALIGN;
-  if (cudaMemcpyAsync(x_dev, x_host, (size_t)w->k * 2, cudaMemcpyHostToDevice, stream) !=
-      cudaSuccess)
-    return BONSAI_ERR_CUDA;
+  // Page-locked host buffers are mapped into the device address space: the
+  // activations are then read by a small kernel and the result is written by
+  // the product kernel itself, so no copy-engine transfer (with its fixed
+  // latency) sits between the launches. Other host memory goes through
+  // cudaMemcpyAsync.
+  auto mapped = [](const void* p) -> const void* {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      cudaGetLastError();  // an unknown pointer is not an error here
+      return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+  };
+  const void* xm = aligned16(x_host) ? mapped(x_host) : nullptr;
+  void* ym = aligned16(y_host) ? const_cast<void*>(mapped(y_host)) : nullptr;
+  if (xm) {
+    st = stage_x_launch(static_cast<const uint16_t*>(xm), x_dev, w->k, stream);
+  } else {
+    st = cudaMemcpyAsync(x_dev, x_host, (size_t)w->k * 2, cudaMemcpyHostToDevice, stream) ==
+                 cudaSuccess ? BONSAI_OK : BONSAI_ERR_CUDA;
+  }
+  if (st != BONSAI_OK) return st;
+  if (ym) return gemv_launch(w, x_dev, 1, static_cast<uint16_t*>(ym), false, stream);
   st = gemv_launch(w, x_dev, 1, y_dev, false, stream);
   if (st != BONSAI_OK) return st;
   if (cudaMemcpyAsync(y_host, y_dev, (size_t)w->n * 2, cudaMemcpyDeviceToHost, stream) !=
