@@ -27,6 +27,7 @@ constexpr int kBM = 64, kBN = 64;      // output tile
 constexpr int kThreads = 256;          // 16 x 16 threads, 4 x 4 outputs each
 constexpr int kCW = 32;                // words of K per smem chunk (8 groups)
 constexpr int kPitch = kCW + 4;        // padded row pitch (words)
+constexpr int kSPitch = kCW / 4 + 1;   // group scales per W row, padded: 16 rows -> 16 banks
 
 // popc(a XOR w) over one 128-code group (4 words) with 3 popcounts: a full
 // adder over words 0..2 and a half adder with word 3 give per-bit
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(kThreads) xnor_kernel(
     int m, int n, int k, int32_t* __restrict__ d_out, __half* __restrict__ y_out) {
   __shared__ __align__(16) uint32_t As[kBM * kPitch];
   __shared__ __align__(16) uint32_t Ws[kBN * kPitch];
-  __shared__ float Ss[kBN * (kCW / 4)];
+  __shared__ float Ss[kBN * kSPitch];
 
   pdl_wait();
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kThreads) xnor_kernel(
       const int r = t / (kCW / 4), gg = t - r * (kCW / 4);
       const int rw = min(n0 + r, n - 1);
       const int gi = min(c0 / 4 + gg, G - 1);
-      Ss[r * (kCW / 4) + gg] = __half2float(scales[(long long)rw * G + gi]);
+      Ss[r * kSPitch + gg] = __half2float(scales[(long long)rw * G + gi]);
     }
     __syncthreads();
     for (int gg = 0; gg < cw / 4; ++gg) {
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) xnor_kernel(
         wv[j] = *reinterpret_cast<const uint4*>(&Ws[(tx + 16 * j) * kPitch + 4 * gg]);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float sg = Ss[(tx + 16 * j) * (kCW / 4) + gg];
+        const float sg = Ss[(tx + 16 * j) * kSPitch + gg];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int pc = group_popc(av[i], wv[j]);
