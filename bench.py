@@ -259,6 +259,7 @@ class GemvWorkload:
 
     def __init__(self, fmt, n, k, cfg_id, name):
         self.fmt, self.n, self.k, self.cfg_id, self.name = fmt, n, k, cfg_id, name
+        self.reps = max(1, math.ceil(2 * L2_BYTES / self.unit_bytes()) + 1)
 
     def unit_bytes(self):
         return weight_bytes(self.fmt, self.n, self.k)
@@ -268,7 +269,6 @@ class GemvWorkload:
         import sub_bit_weight_binary_b300 as sb
         from sub_bit_weight_binary_b300 import synth
         seed = synth.config_seed(self.cfg_id)
-        self.reps = max(1, math.ceil(2 * L2_BYTES / self.unit_bytes()) + 1)
         tid = synth.TID_WTER if self.fmt == sb.BONSAI_FMT_TERNARY else synth.TID_WBIN
         self.w = [make_weights(self.fmt, self.n, self.k, seed, tid + 64 * r,
                                synth.TID_SCALES + 64 * r, sb.BONSAI_WEIGHTS_PREFETCH)
