@@ -34,17 +34,27 @@ unsigned int read_clear_status_gemm() {
 namespace gemm {
 
 constexpr int BM = 128;                 // features per tile  (MMA M)
-constexpr int BN = 256;                 // tokens per tile    (MMA N)
+constexpr int BN = 256;                 // tokens per MMA     (MMA N)
 constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of FP16
-// Separate rings: dequantised weight tiles (A) are produced on chip, X
-// tiles (B) arrive by TMA from L2. Ternary dequantisation has the longer
-// latency per stage, so it gets the deeper A ring.
-template <int FMT> struct Ring {
-  static constexpr int A = FMT == BONSAI_FMT_TERNARY ? 6 : 4;
-  static constexpr int B = FMT == BONSAI_FMT_TERNARY ? 3 : 4;
+// Two tile shapes. Narrow: 256 tokens per tile, two TMEM accumulators of 256
+// columns, so the epilogue of one tile overlaps the main loop of the next.
+// Wide (more than 256 tokens): 512 tokens per tile, one accumulator of 512
+// columns; every dequantised weight stage then feeds two N=256 MMAs, which
+// halves the dequantisation per FLOP (the dequantisers are the limiter) at
+// the price of an epilogue that no longer overlaps.
+// Separate rings: dequantised weight tiles (A) are produced on chip, X tiles
+// (B) arrive by TMA from L2. Narrow ternary dequantisation has the longer
+// latency per stage, so it gets the deeper A ring; wide X stages are 64 KB.
+template <int FMT, bool WIDE> struct Cfg {
+  static constexpr int TT = WIDE ? 512 : 256;    // tokens per tile
+  static constexpr int HALVES = TT / BN;         // N=256 MMAs per K=16 step
+  static constexpr int NACC = WIDE ? 1 : 2;      // TMEM accumulators
+  static constexpr int A = WIDE ? 4 : (FMT == BONSAI_FMT_TERNARY ? 6 : 4);
+  static constexpr int B = WIDE ? 2 : (FMT == BONSAI_FMT_TERNARY ? 3 : 4);
+  static constexpr int B_BYTES = TT * BK * 2;    // 32 or 64 KB
 };
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr int B_BYTES = BN * BK * 2;    // 32 KB
+constexpr int B_HALF = BN * BK * 2;     // 32 KB: one TMA box of X
 constexpr int TMEM_COLS = 512;
 constexpr int THREADS = 512;
 constexpr int W_TMA = 0, W_MMA = 1, W_TMEM = 2, W_EPI = 4, W_DQ = 8;
@@ -252,11 +262,12 @@ __device__ __forceinline__ void dq_ternary(const uint32_t (&wd)[16], uint32_t s2
     sts128(dst_row + ((c ^ sw) << 4), pv[4 * c], pv[4 * c + 1], pv[4 * c + 2], pv[4 * c + 3]);
 }
 
-template <int FMT>
+template <int FMT, bool WIDE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  constexpr int A_STAGES = Ring<FMT>::A, B_STAGES = Ring<FMT>::B;
+  using C = Cfg<FMT, WIDE>;
+  constexpr int A_STAGES = C::A, B_STAGES = C::B, B_BYTES = C::B_BYTES, TT = C::TT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + A_STAGES * A_BYTES;
@@ -331,14 +342,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t g = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % p.tok_tiles) * BN;
+        const int m0 = (tile % p.tok_tiles) * TT;
+        // token halves of a wide tile that hold tokens (rows past m read as 0)
+        const int halves = (p.m - m0 + BN - 1) / BN < C::HALVES ? (p.m - m0 + BN - 1) / BN : C::HALVES;
         prefetch_tile(tile + gridDim.x);
         for (int kk = 0; kk < p.nk; ++kk, ++g) {
           const int s = g % B_STAGES;
           const uint32_t ph = (g / B_STAGES) & 1;
           if (!mbar_wait(empty_b + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
-          mbar_arrive_expect_tx(full_b + 8 * s, B_BYTES);
-          tma_load_2d(sB + s * B_BYTES, &tmx, kk * BK, m0, full_b + 8 * s);
+          mbar_arrive_expect_tx(full_b + 8 * s, (uint32_t)(halves * B_HALF));
+          for (int h = 0; h < halves; ++h)
+            tma_load_2d(sB + s * B_BYTES + h * B_HALF, &tmx, kk * BK, m0 + h * BN, full_b + 8 * s);
         }
       }
     }
@@ -348,10 +362,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t g = 0, it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++it) {
-        const uint32_t a = it & 1, use = it >> 1;
+        const uint32_t a = it % C::NACC, use = it / C::NACC;
         if (!mbar_wait(acc_empty + 8 * a, (use & 1) ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + a * 256;
+        const int m0 = (tile % p.tok_tiles) * TT;
+        const int halves = (p.m - m0 + BN - 1) / BN < C::HALVES ? (p.m - m0 + BN - 1) / BN : C::HALVES;
         for (int kk = 0; kk < p.nk; ++kk, ++g) {
           const int sa = g % A_STAGES, sb = g % B_STAGES;
           if (!mbar_wait(full_b + 8 * sb, (g / B_STAGES) & 1) ||
@@ -362,10 +378,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint64_t ad = smem_desc_sw128(sA + sa * A_BYTES);
-          const uint64_t bd = smem_desc_sw128(sB + sb * B_BYTES);
+          const uint64_t bd0 = smem_desc_sw128(sB + sb * B_BYTES);
+          const uint64_t bd1 = smem_desc_sw128(sB + sb * B_BYTES + B_HALF);
 #pragma unroll
-          for (int k4 = 0; k4 < BK / 16; ++k4)  // +32 bytes per K=16 step inside the atom
-            mma_f16_ss(d_tmem, ad + 2 * k4, bd + 2 * k4, kIdesc, (kk | k4) != 0);
+          for (int k4 = 0; k4 < BK / 16; ++k4) {  // +32 bytes per K=16 step inside the atom
+            // half h: tokens m0 + 256h .., TMEM columns 256h ..
+            mma_f16_ss(d_tmem, ad + 2 * k4, bd0 + 2 * k4, kIdesc, (kk | k4) != 0);
+            if (C::HALVES > 1 && halves > 1)
+              mma_f16_ss(d_tmem + 256, ad + 2 * k4, bd1 + 2 * k4, kIdesc, (kk | k4) != 0);
+          }
           mma_commit(empty_a + 8 * sa);
           mma_commit(empty_b + 8 * sb);
         }
@@ -380,18 +401,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int e = warp - W_EPI;  // TMEM lanes 32e .. 32e+31
     uint32_t it = 0;
     for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
-      const uint32_t a = it & 1, use = it >> 1;
+      const uint32_t a = it % C::NACC, use = it / C::NACC;
       if (!mbar_wait(acc_full + 8 * a, use & 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
       tc_fence_after();
-      const int n0 = (tile / p.tok_tiles) * BM, m0 = (tile % p.tok_tiles) * BN;
+      const int n0 = (tile / p.tok_tiles) * BM, m0 = (tile % p.tok_tiles) * TT;
       const int feat = n0 + 32 * e + lane;
       const bool fok = feat < p.n;
+      // column chunks that hold tokens (the MMAs wrote only the used halves)
+      const int chunks = (p.m - m0 + 31) / 32 < TT / 32 ? (p.m - m0 + 31) / 32 : TT / 32;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < chunks; ++c) {
         uint32_t v[32];
         TMEM_LD_32(tmem_base + ((uint32_t)(32 * e) << 16) + a * 256 + 32 * c, v);
         tmem_ld_wait();
-        if (c == BN / 32 - 1) {
+        if (c == chunks - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + 8 * a);
@@ -531,6 +554,19 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
                             (uint64_t)w->k, (uint64_t)m, (uint64_t)w->k * 2, BK, BN,
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return BONSAI_ERR_CUDA;
+  const bool ter = w->format == BONSAI_FMT_TERNARY;
+  auto smem_of = [](int a, int b, int b_bytes, bool lut) {
+    return a * A_BYTES + b * b_bytes + (lut ? LUT_BYTES : 0) + BAR_BYTES;
+  };
+  using CTN = Cfg<BONSAI_FMT_TERNARY, false>;
+  using CTW = Cfg<BONSAI_FMT_TERNARY, true>;
+  using CBN = Cfg<BONSAI_FMT_BINARY, false>;
+  using CBW = Cfg<BONSAI_FMT_BINARY, true>;
+  const int smem_wide = ter ? smem_of(CTW::A, CTW::B, CTW::B_BYTES, true)
+                            : smem_of(CBW::A, CBW::B, CBW::B_BYTES, false);
+  // wide tiles when there are more tokens than one MMA takes and they fit
+  const bool wide = m > BN && smem_wide <= device_max_smem_optin();
+  const int tt = wide ? 512 : 256;
 
   Params p{};
   p.w = static_cast<const uint8_t*>(w->packed);
@@ -542,20 +578,20 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   p.k = (int)w->k;
   p.G = p.k / 128;
   p.nk = p.k / BK;
-  p.tok_tiles = (int)((m + BN - 1) / BN);
+  p.tok_tiles = (int)((m + tt - 1) / tt);
   p.tiles = ((p.n + BM - 1) / BM) * p.tok_tiles;
   p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.y_stride = swiglu ? p.n / 2 : p.n;
 
-  const bool ter = w->format == BONSAI_FMT_TERNARY;
-  const int smem = ter ? Ring<BONSAI_FMT_TERNARY>::A * A_BYTES + Ring<BONSAI_FMT_TERNARY>::B * B_BYTES +
-                             LUT_BYTES + BAR_BYTES
-                       : Ring<BONSAI_FMT_BINARY>::A * A_BYTES + Ring<BONSAI_FMT_BINARY>::B * B_BYTES +
-                             BAR_BYTES;
+  const int smem = wide ? smem_wide
+                       : (ter ? smem_of(CTN::A, CTN::B, CTN::B_BYTES, true)
+                              : smem_of(CBN::A, CBN::B, CBN::B_BYTES, false));
   if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
-  const void* fn = ter ? (const void*)gemm_kernel<BONSAI_FMT_TERNARY>
-                       : (const void*)gemm_kernel<BONSAI_FMT_BINARY>;
+  const void* fn = ter ? (wide ? (const void*)gemm_kernel<BONSAI_FMT_TERNARY, true>
+                               : (const void*)gemm_kernel<BONSAI_FMT_TERNARY, false>)
+                       : (wide ? (const void*)gemm_kernel<BONSAI_FMT_BINARY, true>
+                               : (const void*)gemm_kernel<BONSAI_FMT_BINARY, false>);
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess)
     return BONSAI_ERR_CUDA;
 
@@ -570,9 +606,8 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = ter ? cudaLaunchKernelEx(&cfg, gemm_kernel<BONSAI_FMT_TERNARY>, tm, p)
-                      : cudaLaunchKernelEx(&cfg, gemm_kernel<BONSAI_FMT_BINARY>, tm, p);
-  return cuda_status(e);
+  void* args[] = {&tm, &p};
+  return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
 }
 
 }  // namespace bonsai

@@ -234,7 +234,8 @@ def test_gemm_few_tokens(fmt, m, n, k):
 # ------------------------------------------------------- GEMM, tensor cores
 @pytest.mark.parametrize("fmt", [BIN, TER])
 @pytest.mark.parametrize("m,n,k", [(9, 128, 128), (300, 200, 640), (512, 384, 1024),
-                                   (257, 130, 5120), (256, 256, 320 * 4), (130, 96, 17408)])
+                                   (257, 130, 5120), (256, 256, 320 * 4), (130, 96, 17408),
+                                   (600, 136, 640), (1000, 130, 256), (1536, 272, 384)])
 def test_gemm_tensor_core(fmt, m, n, k):
     t = torch()
     w, packed, scales = weights(fmt, 60 + m, n, k)
