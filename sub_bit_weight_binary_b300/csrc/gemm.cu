@@ -38,10 +38,11 @@ constexpr int BN = 256;                 // tokens per MMA     (MMA N)
 constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of FP16
 // Two tile shapes. Narrow: 256 tokens per tile, two TMEM accumulators of 256
 // columns, so the epilogue of one tile overlaps the main loop of the next.
-// Wide (more than 256 tokens): 512 tokens per tile, one accumulator of 512
-// columns; every dequantised weight stage then feeds two N=256 MMAs, which
-// halves the dequantisation per FLOP (the dequantisers are the limiter) at
-// the price of an epilogue that no longer overlaps.
+// Wide (ternary, more than 256 tokens, enough tiles to fill the SMs): 512
+// tokens per tile, one accumulator of 512 columns; every dequantised weight
+// stage then feeds two N=256 MMAs, which halves the dequantisation per FLOP
+// (the ternary dequantisers are the limiter) at the price of an epilogue that
+// no longer overlaps.
 // Separate rings: dequantised weight tiles (A) are produced on chip, X tiles
 // (B) arrive by TMA from L2. Narrow ternary dequantisation has the longer
 // latency per stage, so it gets the deeper A ring; wide X stages are 64 KB.
@@ -564,8 +565,14 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   using CBW = Cfg<BONSAI_FMT_BINARY, true>;
   const int smem_wide = ter ? smem_of(CTW::A, CTW::B, CTW::B_BYTES, true)
                             : smem_of(CBW::A, CBW::B, CBW::B_BYTES, false);
-  // wide tiles when there are more tokens than one MMA takes and they fit
-  const bool wide = m > BN && smem_wide <= device_max_smem_optin();
+  // Wide tiles pay off where the dequantisers limit (ternary) and enough
+  // tiles remain to fill the SMs; measured at M=512, N=17408: ternary +7%,
+  // binary -9% (its cheap expansion gains nothing and it loses the epilogue
+  // overlap and two X stages), and a whole layer loses 13-28% if its
+  // N=5120 products drop to 40 tiles.
+  const long long ftiles = (w->n + BM - 1) / BM;
+  const bool wide = ter && m > BN && ftiles * ((m + 511) / 512) * 10 >= 9LL * device_sm_count() &&
+                    smem_wide <= device_max_smem_optin();
   const int tt = wide ? 512 : 256;
 
   Params p{};

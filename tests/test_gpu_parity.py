@@ -248,6 +248,25 @@ def test_gemm_tensor_core(fmt, m, n, k):
     y.check()
 
 
+@pytest.mark.parametrize("m", [300, 600, 1000])
+def test_gemm_wide_tiles(m):
+    """Ternary products with enough feature tiles to take 512-token tiles
+    (n = 17040: 134 tiles, the last one ragged), token counts that leave the
+    second 256-token half partly or wholly empty; sampled outputs."""
+    t = torch()
+    n, k = 17040, 256
+    w, packed, scales = weights(TER, 210 + m, n, k)
+    x = synth.gen_x(211 + m, m, k)
+    y = Guarded((m, n), t.float16)
+    sb.bonsai_gemm(w, dev(x), y.t)
+    assert sb.bonsai_check_async() == 0
+    ms = sample_idx(m, [0, 255, 256, 299, 511, 512, 767, 768, m - 1], 20, 12)
+    ns = sample_idx(n, [0, 127, 128, n - 17, n - 16, n - 1], 60, 13)
+    y_ref, nrm = oracle.linear(TER, packed, scales, x, n_sel=ns, m_sel=ms)
+    assert_close(host(y.t)[np.ix_(ms, ns)], y_ref, nrm, "wide tiles m=%d" % m)
+    y.check()
+
+
 def sample_idx(total, edges, count, seed):
     rng = np.random.default_rng(seed)
     idx = set(int(e) for e in edges if 0 <= e < total)
