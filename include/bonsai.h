@@ -136,7 +136,9 @@ bonsai_status bonsai_pack_ternary(const int8_t* codes, int64_t rows, int64_t k,
  * w: binary or ternary weights; x: device FP16 [k]; y: device FP16 [n].
  * Packed bytes must be valid codes (ternary bytes <= 242, padding 121):
  * kernels do not re-check them. Decode is memory-bandwidth bound
- * ("第一の壁"): the kernel streams each packed byte once. */
+ * ("第一の壁"): the kernel streams each packed byte once. Rows too long for
+ * the decode kernel's on-chip activation table (beyond roughly 30K codes
+ * ternary or 75K binary) run on the tensor-core kernel of bonsai_gemm. */
 bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x,
                           uint16_t* y, bonsai_stream stream);
 

@@ -219,7 +219,11 @@ bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x, uint16_t* 
   if (st != BONSAI_OK) return st;
   if (!x || !y) return BONSAI_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
-  return gemv_launch(w, x, 1, y, false, stream);
+  st = gemv_launch(w, x, 1, y, false, stream);
+  // very long rows: the decode kernel's per-CTA x table no longer fits in
+  // shared memory; the tensor-core kernel takes any K
+  if (st == BONSAI_ERR_UNSUPPORTED) st = gemm_launch(w, x, 1, y, false, stream);
+  return st;
 }
 
 bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
@@ -251,9 +255,10 @@ bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
                  cudaSuccess ? BONSAI_OK : BONSAI_ERR_CUDA;
   }
   if (st != BONSAI_OK) return st;
-  if (ym) return gemv_launch(w, x_dev, 1, static_cast<uint16_t*>(ym), false, stream);
-  st = gemv_launch(w, x_dev, 1, y_dev, false, stream);
-  if (st != BONSAI_OK) return st;
+  uint16_t* y_out = ym ? static_cast<uint16_t*>(ym) : y_dev;
+  st = gemv_launch(w, x_dev, 1, y_out, false, stream);
+  if (st == BONSAI_ERR_UNSUPPORTED) st = gemm_launch(w, x_dev, 1, y_out, false, stream);
+  if (st != BONSAI_OK || ym) return st;
   if (cudaMemcpyAsync(y_host, y_dev, (size_t)w->n * 2, cudaMemcpyDeviceToHost, stream) !=
       cudaSuccess)
     return BONSAI_ERR_CUDA;

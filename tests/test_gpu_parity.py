@@ -102,6 +102,8 @@ GEMV_CASES = [
     (TER, 5120, 17408), (TER, 300, 1280), (TER, 129, 384),
     # the decode sweep's stacked q/k/v and gate/up matrices
     (BIN, 15360, 5120), (TER, 15360, 5120), (BIN, 34816, 5120), (TER, 34816, 5120),
+    # rows too long for the decode kernel's x table: the tensor-core fallback
+    (TER, 20, 65536), (BIN, 20, 131072), (TER, 3, 1 << 20),
 ]
 
 
