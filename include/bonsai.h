@@ -266,6 +266,15 @@ bonsai_status bonsai_binarize_activations(const uint16_t* x, int64_t m, int64_t 
 bonsai_status bonsai_hadamard(const uint16_t* x, int64_t m, int64_t k, int32_t block,
                               const uint32_t* signs, uint16_t* out, bonsai_stream stream);
 
+/* Self-test of the failure path: launches one thread that waits on a
+ * barrier nothing completes, with the same bounded wait the product kernels
+ * use on their barriers but a limit of `limit_ns` nanoseconds of wall-clock
+ * time (1 us .. 100 ms, else BONSAI_ERR_INVALID_ARG). The wait gives up, the
+ * kernel records BONSAI_ERR_TIMEOUT and returns; the next
+ * bonsai_check_async on the stream reports it (and clears it), and the
+ * device stays usable. No fault or trap is involved. */
+bonsai_status bonsai_selftest_wait_timeout(uint64_t limit_ns, bonsai_stream stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: BONSAI_OK, BONSAI_ERR_BAD_CODE or BONSAI_ERR_TIMEOUT.
  * Returns BONSAI_ERR_CUDA if the stream reported a CUDA error. */

@@ -74,6 +74,8 @@ def lib():
         L.bonsai_binarize_activations.restype = S
         L.bonsai_hadamard.argtypes = [P, I64, I64, C.c_int32, P, P, P]
         L.bonsai_hadamard.restype = S
+        L.bonsai_selftest_wait_timeout.argtypes = [C.c_uint64, P]
+        L.bonsai_selftest_wait_timeout.restype = S
         L.bonsai_check_async.argtypes = [P]
         L.bonsai_check_async.restype = S
         L.bonsai_status_string.argtypes = [S]
@@ -305,6 +307,12 @@ def bonsai_hadamard(x, out, block=128, signs=None, stream=None):
                               _ptr(signs, (torch.int32,), "signs"),
                               _ptr(out, (torch.float16,), "out"), _stream(stream)),
         "bonsai_hadamard")
+
+
+def bonsai_selftest_wait_timeout(limit_ns: int, stream=None):
+    """Launch the bounded-wait self-test (a wait that must run out)."""
+    _ok(lib().bonsai_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+        "bonsai_selftest_wait_timeout")
 
 
 def bonsai_check_async(stream=None) -> int:

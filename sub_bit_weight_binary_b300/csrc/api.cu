@@ -21,6 +21,8 @@ bonsai_status binarize_launch(const uint16_t*, int64_t, int64_t, uint32_t*, uint
                               cudaStream_t);
 bonsai_status hadamard_launch(const uint16_t*, int64_t, int64_t, int32_t, const uint32_t*,
                               uint16_t*, cudaStream_t);
+bonsai_status selftest_wait_timeout_launch(uint64_t, cudaStream_t);
+unsigned int read_clear_status_selftest();
 unsigned int read_clear_status_pack();
 unsigned int read_clear_status_gemv();
 unsigned int read_clear_status_gemm();
@@ -343,10 +345,16 @@ bonsai_status bonsai_hadamard(const uint16_t* x, int64_t m, int64_t k, int32_t b
   return hadamard_launch(x, m, k, block, signs, out, stream);
 }
 
+bonsai_status bonsai_selftest_wait_timeout(uint64_t limit_ns, bonsai_stream stream) {
+  if (limit_ns < 1000 || limit_ns > 100000000) return BONSAI_ERR_INVALID_ARG;
+  return selftest_wait_timeout_launch(limit_ns, stream);
+}
+
 bonsai_status bonsai_check_async(bonsai_stream stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return BONSAI_ERR_CUDA;
-  const unsigned int codes[4] = {read_clear_status_pack(), read_clear_status_gemv(),
-                                 read_clear_status_gemm(), read_clear_status_xnor()};
+  const unsigned int codes[5] = {read_clear_status_pack(), read_clear_status_gemv(),
+                                 read_clear_status_gemm(), read_clear_status_xnor(),
+                                 read_clear_status_selftest()};
   if (cudaGetLastError() != cudaSuccess) return BONSAI_ERR_CUDA;
   for (unsigned int c : codes)
     if (c != 0) return static_cast<bonsai_status>(c);

@@ -1,15 +1,18 @@
 // gemm.cu -- multi-token product Y = X . (s (.) W)^T on the 5th-generation
 // tensor cores (tcgen05), for prompt processing (pp512) and
 // diffusion-transformer image tokens. This case is a dense contraction:
-// every dequantised weight tile is reused by 256 tokens.
+// every dequantised weight tile is reused by 256 (or 512) tokens.
 //
 // One persistent CTA per SM, 16 warps with fixed roles:
 //   warp 0      TMA producer: X tiles [256 tokens x 64 k] FP16, 128-byte
-//               swizzle, straight into the MMA's canonical K-major layout.
+//               swizzle, straight into the MMA's canonical K-major layout
+//               (two per stage for 512-token tiles); it also prefetches the
+//               packed weight rows of its tiles into L2.
 //   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, M=128
 //               features x N=256 tokens x K=16, FP32 accumulators in TMEM.
-//   warp 2      TMEM allocator (512 columns = two accumulators, so the
-//               epilogue of tile i overlaps the main loop of tile i+1).
+//   warp 2      TMEM allocator (512 columns: two 256-column accumulators, so
+//               the epilogue of tile i overlaps the main loop of tile i+1,
+//               or one 512-column accumulator for 512-token tiles).
 //   warps 4-7   epilogue: tcgen05.ld -> FP16 (round to nearest even) -> Y.
 //   warps 8-15  dequantisers: packed codes -> FP16 s*w written into the
 //               swizzled A stage. The value is exact: s*(+-1) only flips the

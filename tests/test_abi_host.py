@@ -30,7 +30,8 @@ def test_headers_declare_the_boundary():
     names = declared("bonsai.h")
     for f in ("bonsai_packed_row_bytes", "bonsai_pack_binary", "bonsai_pack_ternary",
               "bonsai_gemv", "bonsai_gemm", "bonsai_xnor_gemm", "bonsai_binarize_activations",
-              "bonsai_gemm_swiglu", "bonsai_hadamard", "bonsai_gemv_host", "bonsai_check_async",
+              "bonsai_gemm_swiglu", "bonsai_hadamard", "bonsai_gemv_host", "bonsai_selftest_wait_timeout",
+              "bonsai_check_async",
               "bonsai_status_string"):
         assert f in names
 
@@ -120,6 +121,8 @@ def test_other_host_checks(libs):
     assert sb.STATUS[gh(C.byref(w), 0x10000, 0x30008, 0x40000, 0x50000, None)] == "BONSAI_ERR_ALIGN"
     assert sb.STATUS[gh(C.byref(W(fmt=3)), 0x10000, 0x30000, 0x40000, 0x50000, None)] \
         == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[L.bonsai_selftest_wait_timeout(10, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[L.bonsai_selftest_wait_timeout(10 ** 9, None)] == "BONSAI_ERR_INVALID_ARG"
     hd = L.bonsai_hadamard
     assert sb.STATUS[hd(None, 2, 256, 128, None, 0x50000, None)] == "BONSAI_ERR_INVALID_ARG"
     assert sb.STATUS[hd(0x40000, 2, 256, 96, None, 0x50000, None)] == "BONSAI_ERR_UNSUPPORTED"

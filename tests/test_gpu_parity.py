@@ -607,6 +607,27 @@ def test_hadamard_in_place_and_involution():
         assert np.all(err <= 4 * 2.0 ** -11 * np.sqrt(np.mean(xv ** 2)) + 2.0 ** -11 * np.abs(xv))
 
 
+# ------------------------------------------------------- failure detection
+def test_bounded_wait_reports_timeout_and_device_stays_usable():
+    """A wait that nothing completes gives up after its limit: the status
+    word reads BONSAI_ERR_TIMEOUT once, then clears, and products still run."""
+    t = torch()
+    t0 = __import__("time").perf_counter()
+    sb.bonsai_selftest_wait_timeout(2_000_000)  # 2 ms
+    st = sb.bonsai_check_async()
+    elapsed = __import__("time").perf_counter() - t0
+    assert sb.STATUS[st] == "BONSAI_ERR_TIMEOUT"
+    assert elapsed < 5.0
+    assert sb.bonsai_check_async() == 0  # cleared
+    w, packed, scales = weights(TER, 5, 64, 640)
+    x = synth.gen_x(7, 1, 640)
+    y = t.empty(64, dtype=t.float16, device="cuda")
+    sb.bonsai_gemv(w, dev(x[0]), y)
+    assert sb.bonsai_check_async() == 0
+    y_ref, nrm = oracle.linear(TER, packed, scales, x)
+    assert_close(host(y), y_ref[0], nrm[0], "after a timeout")
+
+
 # ------------------------------------------------------------ graph capture
 def test_graph_capture_matches_eager():
     """Launches captured into a CUDA graph (programmatic dependent launch
