@@ -165,6 +165,40 @@ def test_gemv_special_values():
     assert np.all(host(yz).view(np.float16) == 0)
 
 
+@pytest.mark.parametrize("fmt", [BIN, TER])
+@pytest.mark.parametrize("m", [1, 3, 300])
+def test_degenerate_scales_and_inputs(fmt, m):
+    """Zero scales or zero activations give exactly +-0 (the norm is 0);
+    negating every scale negates every output bit-exactly (s*w is exact and
+    negation commutes with round-to-nearest), on the decode (m <= 8) and the
+    tensor-core (m = 300) paths."""
+    t = torch()
+    n, k = 200, 1280
+    w, packed, scales = weights(fmt, 230 + m, n, k)
+    x = synth.gen_x(231 + m, m, k)
+
+    def run(sc, xv):
+        ww = sb.Weights(fmt, n, k, w.packed, dev(sc))
+        y = t.empty((m, n), dtype=t.float16, device="cuda")
+        sb.bonsai_gemm(ww, dev(xv), y)
+        assert sb.bonsai_check_async() == 0
+        return host(y)
+
+    zero_s = np.zeros_like(scales)
+    assert np.all((run(zero_s, x) & 0x7FFF) == 0)
+    assert np.all((run(scales, np.zeros_like(x)) & 0x7FFF) == 0)
+    y = run(scales, x)
+    y_neg = run(scales ^ np.uint16(0x8000), x)
+    assert np.array_equal(y_neg & 0x7FFF, y & 0x7FFF)       # same magnitudes
+    nz = (y & 0x7FFF) != 0                                    # an exact 0 may keep its sign
+    assert np.array_equal(y_neg[nz], y[nz] ^ np.uint16(0x8000))
+    # one group's scales zeroed: that group contributes nothing
+    part = scales.copy()
+    part[:, 3] = 0
+    y_ref, nrm = oracle.linear(fmt, packed, part, x)
+    assert_close(run(part, x), y_ref, nrm, "one zero group")
+
+
 def _sparse_ternary_codes(seed, n, k, per_mille):
     """Seeded ternary codes with `per_mille`/1000 of them nonzero (+-1 equally
     likely), from the counter-based generator's raw words."""
