@@ -53,7 +53,6 @@ template <int FMT, bool WIDE> struct Cfg {
   static constexpr int TT = WIDE ? 512 : 256;    // tokens per tile
   static constexpr int HALVES = TT / BN;         // N=256 MMAs per K=16 step
   static constexpr int NACC = WIDE ? 1 : 2;      // TMEM accumulators
-  static constexpr int NG = WIDE ? 3 : 2;        // dequantiser groups of 4 warps
   static constexpr int A = WIDE ? 4 : (FMT == BONSAI_FMT_TERNARY ? 6 : 4);
   static constexpr int B = WIDE ? 2 : (FMT == BONSAI_FMT_TERNARY ? 3 : 4);
   static constexpr int B_BYTES = TT * BK * 2;    // 32 or 64 KB
@@ -400,25 +399,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       mma_commit(drain);
       if (!mbar_wait(drain, 0)) set_status(BONSAI_ERR_TIMEOUT);
     }
-  } else if (warp >= W_EPI) {
-    // ------------------- epilogue (warps 4-7), dequantisers -------------------
-    // Warps 8-15 dequantise: two groups of four, each group the k-steps of one
-    // residue of the global k-step counter. With 512-token tiles the epilogue
-    // cannot overlap the main loop (one accumulator), so warps 4-7 are a third
-    // dequantiser group during a tile and drain TMEM after it.
-    const int e = warp - W_EPI;  // epilogue: TMEM lanes 32e .. 32e+31
-    const bool epi = warp < W_EPI + 4;
-    const bool deq = !epi || C::NG == 3;
-    if (epi || !p.prefetch) pdl_wait();  // y, or weights, may be written by earlier work
-    const uint32_t h = epi ? 2u : (uint32_t)((warp - W_DQ) >> 2);  // k-step residue
-    const int r = (epi ? e : ((warp - W_DQ) & 3)) * 32 + lane;    // feature row in the tile
-    const int sw = r & 7;
-    const uint32_t lut = sLut + lane * 4;
-    const TerConsts K;
-
-    auto epilogue_tile = [&](int tile, uint32_t it) -> bool {
+  } else if (warp >= W_EPI && warp < W_EPI + 4) {
+    // ------------------------------- epilogue -------------------------------
+    pdl_wait();
+    const int e = warp - W_EPI;  // TMEM lanes 32e .. 32e+31
+    uint32_t it = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
       const uint32_t a = it % C::NACC, use = it / C::NACC;
-      if (!mbar_wait(acc_full + 8 * a, use & 1)) { set_status(BONSAI_ERR_TIMEOUT); return false; }
+      if (!mbar_wait(acc_full + 8 * a, use & 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
       tc_fence_after();
       const int n0 = (tile / p.tok_tiles) * BM, m0 = (tile % p.tok_tiles) * TT;
       const int feat = n0 + 32 * e + lane;
@@ -457,9 +445,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      return true;
-    };
-
+    }
+  } else if (warp >= W_DQ) {
+    // ------------------------------ dequantisers -----------------------------
+    if (!p.prefetch) pdl_wait();
+    const int dq = warp - W_DQ;         // 0..7
+    const uint32_t h = dq >> 2;         // parity group: even / odd k-steps
+    const int r = (dq & 3) * 32 + lane; // feature row within the tile
+    const int sw = r & 7;
+    const uint32_t lut = sLut + lane * 4;
+    const TerConsts K;
     // Ternary: the packed row is read in 64-byte blocks (320 codes = 5
     // k-steps) one block ahead, so the load latency hides behind the
     // dequantisation of the current block; the block's group scales travel
@@ -485,14 +480,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         dst[4 * i] = q4.x; dst[4 * i + 1] = q4.y; dst[4 * i + 2] = q4.z; dst[4 * i + 3] = q4.w;
       }
     };
-    uint32_t g = 0;  // global k-step counter: stage g % A_STAGES, owner group g % NG
-    auto dequant_tile = [&](int tile) -> bool {
+    uint32_t g = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const int n = (tile / p.tok_tiles) * BM + r;
       const bool nok = n < p.n;
       const uint8_t* wrow = p.w + (long long)(nok ? n : 0) * p.row_bytes;
       const __half* srow = p.scales + (size_t)(nok ? n : 0) * p.G;
       for (int kk = 0; kk < p.nk; ++kk, ++g) {
-        if (g % C::NG != h) continue;
+        if ((g & 1) != h) continue;
         const int s = g % A_STAGES;
         const uint32_t ph = (g / A_STAGES) & 1;
         const uint32_t dst = sA + s * A_BYTES + r * 128;
@@ -502,7 +498,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint2 wv = *reinterpret_cast<const uint2*>(wrow + 8 * kk);
           const __half sc = srow[kk >> 1];
           const uint32_t s2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;
-          if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); return false; }
+          if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
           dq_binary(wv, s2, dst, sw);
         } else {
           const int u = kk / KPB;
@@ -528,7 +524,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int si = (kk >> 1) - ((KPB * u) >> 1);  // 0..2
           const uint32_t sc = si == 0 ? csc[0] : si == 1 ? csc[1] : csc[2];
           const uint32_t s2 = sc * 0x10001u;  // rows past n carry scale 0
-          if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); return false; }
+          if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
           switch (kk % 5) {
             case 0: dq_ternary<0>(cur, s2, lut, K, dst, sw); break;
             case 1: dq_ternary<1>(cur, s2, lut, K, dst, sw); break;
@@ -541,13 +537,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(full_a + 8 * s);
       }
-      return true;
-    };
-
-    uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
-      if (deq && !dequant_tile(tile)) break;
-      if (epi && !epilogue_tile(tile, it)) break;
     }
   }
 
