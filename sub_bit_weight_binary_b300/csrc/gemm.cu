@@ -266,6 +266,19 @@ __device__ __forceinline__ void dq_ternary(const uint32_t (&wd)[16], uint32_t s2
     sts128(dst_row + ((c ^ sw) << 4), pv[4 * c], pv[4 * c + 1], pv[4 * c + 2], pv[4 * c + 3]);
 }
 
+// K order of a tile. All CTAs stream the same activation tiles; in the same
+// K order they would all ask L2 for the same X tile at the same moment (the
+// MMA thread measured 140-325 cycles per k-step waiting on the X ring). Each
+// tile therefore starts at its own block of 5 k-steps and wraps around:
+// k = (j + 5 * rot) mod nk, rot = tile mod (number of blocks). Blocks stay
+// whole (the ternary dequantisers read 64-byte blocks of 5 k-steps).
+__device__ __forceinline__ int k_blocks(const Params& p) { return (p.nk + 4) / 5; }
+__device__ __forceinline__ int k_rot(const Params& p, int tile) { return tile % k_blocks(p); }
+__device__ __forceinline__ int k_at(const Params& p, int tile, int j) {
+  const int k = j + 5 * k_rot(p, tile);
+  return k < p.nk ? k : k - p.nk;
+}
+
 template <int FMT, bool WIDE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ Params p) {
@@ -356,7 +369,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!mbar_wait(empty_b + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
           mbar_arrive_expect_tx(full_b + 8 * s, (uint32_t)(halves * B_HALF));
           for (int h = 0; h < halves; ++h)
-            tma_load_2d(sB + s * B_BYTES + h * B_HALF, &tmx, kk * BK, m0 + h * BN, full_b + 8 * s);
+            tma_load_2d(sB + s * B_BYTES + h * B_HALF, &tmx, k_at(p, tile, kk) * BK, m0 + h * BN,
+                        full_b + 8 * s);
         }
       }
     }
@@ -487,8 +501,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool nok = n < p.n;
       const uint8_t* wrow = p.w + (long long)(nok ? n : 0) * p.row_bytes;
       const __half* srow = p.scales + (size_t)(nok ? n : 0) * p.G;
-      for (int kk = 0; kk < p.nk; ++kk, ++g) {
+      for (int j = 0; j < p.nk; ++j, ++g) {
         if ((g & 1) != h) continue;
+        const int kk = k_at(p, tile, j);  // the k-step this stage holds
         const int s = g % A_STAGES;
         const uint32_t ph = (g / A_STAGES) & 1;
         const uint32_t dst = sA + s * A_BYTES + r * 128;
@@ -513,9 +528,12 @@ __global__ void __launch_bounds__(THREADS, 1)
               load_block(tile, u, cur, csc);
             }
             cur_key = key;
-            // prefetch the block that follows in this thread's order
-            const int nt = u + 1 < nblk ? tile : tile + (int)gridDim.x;
-            const int nu = u + 1 < nblk ? u + 1 : 0;
+            // prefetch the block that follows in this thread's order: the
+            // next one of the tile's rotated order, or the next tile's first
+            const int un = u + 1 < nblk ? u + 1 : 0;
+            const bool last = un == k_rot(p, tile);
+            const int nt = last ? tile + (int)gridDim.x : tile;
+            const int nu = last ? k_rot(p, nt) : un;
             if (nt < p.tiles) {
               load_block(nt, nu, nxt, nsc);
               nxt_key = nt * nblk + nu;
