@@ -115,7 +115,7 @@ def pin_page_sizes():
 
 
 def pin_binary_round_trip():
-    for k, rows in ((128, 3), (640, 1), (5120, 3), (17408, 1)):
+    for k, rows in ((128, 3), (640, 1), (5120, 3), (17408, 1), (128, 1024)):
         codes = synth.gen_binary_codes(11, rows, k)
         packed = oracle.pack_binary(codes)
         ref = np.packbits(((codes + 1) // 2).astype(np.uint8), axis=1, bitorder="little")
@@ -171,7 +171,7 @@ def pin_ternary_all_bytes():
 
 
 def pin_ternary_round_trip_and_padding():
-    for k, rows in ((128, 3), (640, 2), (5120, 1), (17408, 1)):
+    for k, rows in ((128, 3), (640, 2), (5120, 1), (17408, 1), (640, 1024)):
         codes = synth.gen_ternary_codes(5, rows, k)
         packed = oracle.pack_ternary(codes)
         assert packed.shape == (rows, oracle.row_bytes(TER, k))
