@@ -385,6 +385,78 @@ class GemvWorkload:
 SWEEP_SHAPES = [(15360, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]  # qkv o gate_up down
 
 
+class SmallMWorkload(GemvWorkload):
+    """Decode product for a few tokens at once (speculative verification of
+    4 drafted tokens: M=5) over rotating weight replicas; the weights stream
+    once per launch for all tokens (ternary takes 4 tokens per launch, so
+    M=5 is two launches)."""
+    kind = "gemv_m"
+
+    def __init__(self, fmt, n, k, m, cfg_id, name):
+        super().__init__(fmt, n, k, cfg_id, name)
+        self.m = m
+
+    def setup(self):
+        import torch
+        from sub_bit_weight_binary_b300 import synth
+        super().setup()
+        seed = synth.config_seed(self.cfg_id)
+        self.xm = torch.from_numpy(synth.gen_x(seed + 7, self.m, self.k).view(np.float16)).cuda()
+        self.ym = torch.empty((self.m, self.n), dtype=torch.float16, device="cuda")
+        torch.cuda.synchronize()
+
+    def launches(self, start, count):
+        import sub_bit_weight_binary_b300 as sb
+        for i in range(start, start + count):
+            sb.bonsai_gemm(self.w[i % self.reps], self.xm, self.ym)
+
+    def measure(self, steps, warmup, clocks=None):
+        r = GemvWorkload.measure(self, steps, warmup, clocks)
+        per = 2 if (self.fmt == 2 and self.m > 4) else 1
+        r["launches"] = steps * per
+        r["kernel_ms"] = r["ms"] / steps  # one step = the product for all m tokens
+        return r
+
+    def value(self, ms, steps):
+        return self.m * steps / (ms / 1e3), "tok/s"
+
+    def roofline(self, r, pk):
+        out = GemvWorkload.roofline(self, r, pk)
+        out["traffic"] = None
+        out["note"] = "weight bytes per step over the step time (all %d tokens)" % self.m
+        return out
+
+    def config(self):
+        c = GemvWorkload.config(self)
+        c["m"] = self.m
+        return c
+
+    def cpu_sample(self, min_seconds=10.0, max_rows=None):
+        """The oracle for all m tokens over a bounded row sample, scaled to
+        whole-product tokens per second."""
+        import oracle
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(self.cfg_id)
+        rows = min(self.n, max_rows or 512)
+        if self.fmt == 2:
+            packed = oracle.pack_ternary(synth.gen_ternary_codes(seed, rows, self.k))
+        else:
+            packed = synth.gen_binary_words(seed, rows, self.k).view(np.uint8).reshape(rows, -1)
+        scales = synth.gen_scales(seed, rows, self.k)
+        x = synth.gen_x(seed + 7, self.m, self.k)
+        t0 = time.perf_counter()
+        passes = 0
+        while True:
+            oracle.linear(self.fmt, packed, scales, x)
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds or el > 30:
+                break
+        products = passes * rows / self.n
+        return self.m * products / el, "tok/s", "%d pass(es) over rows 0..%d of %d, %d tokens, one thread (%.1f s)" % (
+            passes, rows - 1, self.n, self.m, el)
+
+
 class SweepWorkload:
     """64-layer decode: 4 products per layer (q/k/v and gate/up stacked),
     256 per token, weights resident. With fused=True the gate/up product
@@ -776,6 +848,12 @@ WORKLOADS = {
                                      "ternary GEMV M=1 K=5120 N=17408 (decode)"),
     "bin_gemv_1k": lambda: GemvWorkload(1, 1024, 1024, 1, "binary GEMV M=1 K=1024 N=1024 (decode)"),
     "bin_gemv": lambda: GemvWorkload(1, 17408, 5120, 2, "binary GEMV M=1 K=5120 N=17408 (decode)"),
+    "ter_gemv_m5": lambda: SmallMWorkload(2, 17408, 5120, 5, 2,
+                                          "ternary decode product M=5 K=5120 N=17408 "
+                                          "(speculative verification)"),
+    "bin_gemv_m5": lambda: SmallMWorkload(1, 17408, 5120, 5, 2,
+                                          "binary decode product M=5 K=5120 N=17408 "
+                                          "(speculative verification)"),
     "sweep_bin": lambda: SweepWorkload(1, "64-layer decode sweep, binary, batch 1"),
     "sweep_ter": lambda: SweepWorkload(2, "64-layer decode sweep, ternary, batch 1"),
     "gemm512_bin": lambda: GemmWorkload(1, 512, "prefill GEMM M=512 K=5120 N=17408, binary"),
@@ -795,7 +873,8 @@ WORKLOADS = {
     "xnor_fp16": lambda: XnorFp16Workload(
         "FP16 activations binarised, then XNOR-popcount GEMM M=512 K=4096 N=4096"),
 }
-SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("sweep_bin", 30, 3), ("sweep_ter", 30, 3),
+SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("ter_gemv_m5", 2000, 20),
+             ("bin_gemv_m5", 2000, 20), ("sweep_bin", 30, 3), ("sweep_ter", 30, 3),
              ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
              ("gemm4096_ter", 5, 2), ("layer_bin", 30, 3), ("layer_ter", 30, 3),
              ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("hadamard", 200, 10),
