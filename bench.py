@@ -378,6 +378,44 @@ class GemvWorkload:
             passes, rows - 1, self.n, el)
 
 
+def _oracle_rows_worker(args):
+    """One host process of the all-core oracle baseline: its own slice of
+    rows of the decode product, timed on its own (spawned: no GPU state)."""
+    fmt, k, seed, r0, rows, min_seconds = args
+    import oracle
+    from sub_bit_weight_binary_b300 import synth
+    if fmt == 2:
+        packed = oracle.pack_ternary(synth.gen_ternary_codes(seed + r0, rows, k))
+    else:
+        packed = synth.gen_binary_words(seed + r0, rows, k).view(np.uint8).reshape(rows, -1)
+    scales = synth.gen_scales(seed + r0, rows, k)
+    x = synth.gen_x(seed, 1, k)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oracle.linear(fmt, packed, scales, x)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or el > 30:
+            break
+    return passes * rows * (packed.shape[1] + 2 * (k // 128)), el
+
+
+def oracle_all_cores(fmt, n, k, seed, min_seconds=5.0):
+    """The oracle on every host core at once (one spawned process per core,
+    n/cores rows each): packed + scale bytes per second summed over them."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = max(1, min(cores or 1, 256))
+    rows = max(1, n // cores)
+    jobs = [(fmt, k, seed, i * rows, rows, min_seconds) for i in range(cores)]
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_oracle_rows_worker, jobs)
+    gbs = sum(b / el for b, el in res) / 1e9
+    return gbs, cores, "%d processes x rows %d..%d slices of %d, %.0f s each" % (
+        cores, 0, rows - 1, n, min_seconds)
+
+
 # One layer: q, k, v (5120 x 5120 each) stored stacked as one 15360 x 5120
 # matrix, o 5120 x 5120, gate and up (17408 x 5120 each) stacked as one
 # 34816 x 5120 matrix, down 5120 x 17408: four products, the same bytes as
@@ -921,6 +959,12 @@ def run_ours(args, world, rank):
         v, u, sample = wl.cpu_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(v, 5), "unit": u, "cores": 1, "kind": "oracle",
                                 "sample": sample}
+        if wl.kind == "gemv":
+            from sub_bit_weight_binary_b300 import synth
+            av, ac, asample = oracle_all_cores(wl.fmt, wl.n, wl.k, synth.config_seed(wl.cfg_id),
+                                               min(args.cpu_seconds, 10.0) / 2)
+            line["cpu_baseline"]["all_cores"] = {"value": round(av, 5), "unit": u, "cores": ac,
+                                                 "sample": asample}
     if rank == 0 and not args.no_secondary and world == 1:
         sec = []
         del wl
