@@ -586,13 +586,19 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   using CBW = Cfg<BONSAI_FMT_BINARY, true>;
   const int smem_wide = ter ? smem_of(CTW::A, CTW::B, CTW::B_BYTES, true)
                             : smem_of(CBW::A, CBW::B, CBW::B_BYTES, false);
-  // Wide tiles pay off where the dequantisers limit (ternary) and enough
-  // tiles remain to fill the SMs; measured at M=512, N=17408: ternary +7%,
-  // binary -9% (its cheap expansion gains nothing and it loses the epilogue
-  // overlap and two X stages), and a whole layer loses 13-28% if its
-  // N=5120 products drop to 40 tiles.
+  // Wide tiles pay off where the dequantisers limit (ternary) as long as the
+  // SMs stay about as busy: measured at M=512, N=17408 ternary +7%, binary
+  // -9% (its cheap expansion gains nothing and it loses the epilogue overlap
+  // and two X stages), and a layer loses 13-28% when its N=5120 products drop
+  // from 80 to 40 tiles. Busy fraction = tiles / (waves * SMs).
+  const long long sms_l = device_sm_count();
   const long long ftiles = (w->n + BM - 1) / BM;
-  const bool wide = ter && m > BN && ftiles * ((m + 511) / 512) * 10 >= 9LL * device_sm_count() &&
+  auto busy = [&](long long tiles) {
+    return (double)tiles / (double)(((tiles + sms_l - 1) / sms_l) * sms_l);
+  };
+  const double busy_narrow = busy(ftiles * ((m + 255) / 256));
+  const double busy_wide = busy(ftiles * ((m + 511) / 512));
+  const bool wide = ter && m > BN && busy_wide >= 0.85 * busy_narrow &&
                     smem_wide <= device_max_smem_optin();
   const int tt = wide ? 512 : 256;
 
