@@ -291,11 +291,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t sLut = sB + B_STAGES * B_BYTES;
   const uint32_t sBar = FMT == BONSAI_FMT_TERNARY ? sLut + LUT_BYTES : sLut;
   // full_a[s]: the 4 dequantiser warps of the k-step's parity group;
-  // full_b[s]: the X copy (transaction bytes); empty_a / empty_b: the MMAs
+  // full_b[s][h]: the X copy of half h of stage s (transaction bytes; one
+  // half per 256 tokens, so the MMAs of the first half of a 512-token stage
+  // start, and its refill begins, without waiting for the second);
+  // empty_a / empty_b: the MMAs
   // that read the stage have completed.
   const uint32_t full_a = sBar, empty_a = full_a + 8 * A_STAGES;
-  const uint32_t full_b = empty_a + 8 * A_STAGES, empty_b = full_b + 8 * B_STAGES;
-  const uint32_t acc_full = empty_b + 8 * B_STAGES, acc_empty = acc_full + 16;
+  constexpr int NB = B_STAGES * C::HALVES;  // X barriers: one per (stage, half)
+  const uint32_t full_b = empty_a + 8 * A_STAGES, empty_b = full_b + 8 * NB;
+  const uint32_t acc_full = empty_b + 8 * NB, acc_empty = acc_full + 16;
   const uint32_t drain = acc_empty + 16;
   const uint32_t tmem_slot = drain + 8;
 
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(full_a + 8 * s, 4);
       mbar_init(empty_a + 8 * s, 1);
     }
-    for (int s = 0; s < B_STAGES; ++s) {
+    for (int s = 0; s < NB; ++s) {
       mbar_init(full_b + 8 * s, 1);
       mbar_init(empty_b + 8 * s, 1);
     }
@@ -366,11 +370,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kk = 0; kk < p.nk; ++kk, ++g) {
           const int s = g % B_STAGES;
           const uint32_t ph = (g / B_STAGES) & 1;
-          if (!mbar_wait(empty_b + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
-          mbar_arrive_expect_tx(full_b + 8 * s, (uint32_t)(halves * B_HALF));
-          for (int h = 0; h < halves; ++h)
-            tma_load_2d(sB + s * B_BYTES + h * B_HALF, &tmx, k_at(p, tile, kk) * BK, m0 + h * BN,
-                        full_b + 8 * s);
+          for (int h = 0; h < C::HALVES && ok; ++h) {
+            const uint32_t bf = full_b + 8 * (s * C::HALVES + h);
+            if (!mbar_wait(empty_b + 8 * (s * C::HALVES + h), ph ^ 1)) {
+              set_status(BONSAI_ERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+            if (h < halves) {
+              mbar_arrive_expect_tx(bf, (uint32_t)B_HALF);
+              tma_load_2d(sB + s * B_BYTES + h * B_HALF, &tmx, k_at(p, tile, kk) * BK,
+                          m0 + h * BN, bf);
+            } else {
+              mbar_arrive(bf);  // a half without tokens: complete its phase, load nothing
+            }
+          }
+          if (!ok) break;
         }
       }
     }
@@ -388,25 +403,33 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int halves = (p.m - m0 + BN - 1) / BN < C::HALVES ? (p.m - m0 + BN - 1) / BN : C::HALVES;
         for (int kk = 0; kk < p.nk; ++kk, ++g) {
           const int sa = g % A_STAGES, sb = g % B_STAGES;
-          if (!mbar_wait(full_b + 8 * sb, (g / B_STAGES) & 1) ||
-              !mbar_wait(full_a + 8 * sa, (g / A_STAGES) & 1)) {
+          const uint32_t pb = (g / B_STAGES) & 1;
+          if (!mbar_wait(full_a + 8 * sa, (g / A_STAGES) & 1)) {
             set_status(BONSAI_ERR_TIMEOUT);
             ok = false;
             break;
           }
-          tc_fence_after();
           const uint64_t ad = smem_desc_sw128(sA + sa * A_BYTES);
-          const uint64_t bd0 = smem_desc_sw128(sB + sb * B_BYTES);
-          const uint64_t bd1 = smem_desc_sw128(sB + sb * B_BYTES + B_HALF);
+          for (int h = 0; h < C::HALVES; ++h) {  // half h: tokens m0 + 256h.., TMEM columns 256h..
+            const int ib = sb * C::HALVES + h;
+            if (!mbar_wait(full_b + 8 * ib, pb)) {
+              set_status(BONSAI_ERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+            if (h < halves) {
+              tc_fence_after();
+              const uint64_t bd = smem_desc_sw128(sB + sb * B_BYTES + h * B_HALF);
 #pragma unroll
-          for (int k4 = 0; k4 < BK / 16; ++k4) {  // +32 bytes per K=16 step inside the atom
-            // half h: tokens m0 + 256h .., TMEM columns 256h ..
-            mma_f16_ss(d_tmem, ad + 2 * k4, bd0 + 2 * k4, kIdesc, (kk | k4) != 0);
-            if (C::HALVES > 1 && halves > 1)
-              mma_f16_ss(d_tmem + 256, ad + 2 * k4, bd1 + 2 * k4, kIdesc, (kk | k4) != 0);
+              for (int k4 = 0; k4 < BK / 16; ++k4)  // +32 bytes per K=16 step inside the atom
+                mma_f16_ss(d_tmem + h * 256, ad + 2 * k4, bd + 2 * k4, kIdesc, (kk | k4) != 0);
+              mma_commit(empty_b + 8 * ib);
+            } else {
+              mbar_arrive(empty_b + 8 * ib);  // nothing read this half
+            }
           }
+          if (!ok) break;
           mma_commit(empty_a + 8 * sa);
-          mma_commit(empty_b + 8 * sb);
         }
         if (ok) mma_commit(acc_full + 8 * a);
       }
