@@ -39,25 +39,32 @@ namespace gemm {
 constexpr int BM = 128;                 // features per tile  (MMA M)
 constexpr int BN = 256;                 // tokens per MMA     (MMA N)
 constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row of FP16
-// Two tile shapes. Narrow: 256 tokens per tile, two TMEM accumulators of 256
-// columns, so the epilogue of one tile overlaps the main loop of the next.
-// Wide (ternary, more than 256 tokens, enough tiles to fill the SMs): 512
-// tokens per tile, one accumulator of 512 columns; every dequantised weight
-// stage then feeds two N=256 MMAs, which halves the dequantisation per FLOP
-// (the ternary dequantisers are the limiter) at the price of an epilogue that
-// no longer overlaps.
+// Three tile shapes. Narrow: 128 features x 256 tokens, two TMEM
+// accumulators of 256 columns, so the epilogue of one tile overlaps the main
+// loop of the next. Wide (ternary): 128 x 512, one accumulator of 512
+// columns; every dequantised weight stage feeds two N=256 MMAs, which halves
+// the dequantisation per FLOP (the ternary dequantisers limit). Tall
+// (binary): 256 x 256, one accumulator of 512 columns; every activation
+// stage feeds two M=128 MMAs, which halves the X traffic per FLOP (binary's
+// MMA thread waits on the X ring). Both larger tiles give up the overlapped
+// epilogue.
 // Separate rings: dequantised weight tiles (A) are produced on chip, X tiles
 // (B) arrive by TMA from L2. Narrow ternary dequantisation has the longer
-// latency per stage, so it gets the deeper A ring; wide X stages are 64 KB.
-template <int FMT, bool WIDE> struct Cfg {
-  static constexpr int TT = WIDE ? 512 : 256;    // tokens per tile
-  static constexpr int HALVES = TT / BN;         // N=256 MMAs per K=16 step
-  static constexpr int NACC = WIDE ? 1 : 2;      // TMEM accumulators
-  static constexpr int A = WIDE ? 4 : (FMT == BONSAI_FMT_TERNARY ? 6 : 4);
-  static constexpr int B = WIDE ? 2 : (FMT == BONSAI_FMT_TERNARY ? 3 : 4);
-  static constexpr int B_BYTES = TT * BK * 2;    // 32 or 64 KB
+// latency per stage, so it gets the deeper A ring; wide X stages are 64 KB,
+// tall A stages 32 KB.
+constexpr int NARROW = 0, WIDE = 1, TALL = 2;
+template <int FMT, int MODE> struct Cfg {
+  static constexpr int TT = MODE == WIDE ? 512 : 256;      // tokens per tile
+  static constexpr int FM = MODE == TALL ? 256 : BM;       // features per tile
+  static constexpr int HALVES = TT / BN;                   // token halves (N=256 MMAs)
+  static constexpr int FHALVES = FM / BM;                  // feature halves (M=128 MMAs)
+  static constexpr int NACC = MODE == NARROW ? 2 : 1;      // TMEM accumulators of 256 columns x halves
+  static constexpr int A = MODE == WIDE ? 4 : MODE == TALL ? 3 : (FMT == BONSAI_FMT_TERNARY ? 6 : 4);
+  static constexpr int B = MODE == WIDE ? 2 : (FMT == BONSAI_FMT_TERNARY ? 3 : 4);
+  static constexpr int A_BYTES = FM * BK * 2;              // 16 or 32 KB
+  static constexpr int B_BYTES = TT * BK * 2;              // 32 or 64 KB
 };
-constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int A_HALF = BM * BK * 2;     // 16 KB: one M=128 operand tile
 constexpr int B_HALF = BN * BK * 2;     // 32 KB: one TMA box of X
 constexpr int TMEM_COLS = 512;
 constexpr int THREADS = 512;
@@ -279,12 +286,14 @@ __device__ __forceinline__ int k_at(const Params& p, int tile, int j) {
   return k < p.nk ? k : k - p.nk;
 }
 
-template <int FMT, bool WIDE>
+template <int FMT, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  using C = Cfg<FMT, WIDE>;
-  constexpr int A_STAGES = C::A, B_STAGES = C::B, B_BYTES = C::B_BYTES, TT = C::TT;
+  using C = Cfg<FMT, MODE>;
+  static_assert(MODE != TALL || FMT == BONSAI_FMT_BINARY, "256-feature tiles are for binary");
+  constexpr int A_STAGES = C::A, B_STAGES = C::B, B_BYTES = C::B_BYTES, TT = C::TT, FM = C::FM;
+  constexpr int A_BYTES = C::A_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + A_STAGES * A_BYTES;
@@ -355,8 +364,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // tile's rows are contiguous (row_bytes apart).
       auto prefetch_tile = [&](int tile) {
         if (tile >= p.tiles) return;
-        const int n0 = (tile / p.tok_tiles) * BM;
-        const int rows = p.n - n0 < BM ? p.n - n0 : BM;
+        const int n0 = (tile / p.tok_tiles) * FM;
+        const int rows = p.n - n0 < FM ? p.n - n0 : FM;
         prefetch_l2(p.w + (long long)n0 * p.row_bytes, (long long)rows * p.row_bytes);
       };
       prefetch_tile(blockIdx.x);
@@ -409,8 +418,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          const uint64_t ad = smem_desc_sw128(sA + sa * A_BYTES);
-          for (int h = 0; h < C::HALVES; ++h) {  // half h: tokens m0 + 256h.., TMEM columns 256h..
+          for (int h = 0; h < C::HALVES; ++h) {  // token half h: tokens m0 + 256h ..
             const int ib = sb * C::HALVES + h;
             if (!mbar_wait(full_b + 8 * ib, pb)) {
               set_status(BONSAI_ERR_TIMEOUT);
@@ -421,8 +429,14 @@ __global__ void __launch_bounds__(THREADS, 1)
               tc_fence_after();
               const uint64_t bd = smem_desc_sw128(sB + sb * B_BYTES + h * B_HALF);
 #pragma unroll
-              for (int k4 = 0; k4 < BK / 16; ++k4)  // +32 bytes per K=16 step inside the atom
-                mma_f16_ss(d_tmem + h * 256, ad + 2 * k4, bd + 2 * k4, kIdesc, (kk | k4) != 0);
+              for (int f = 0; f < C::FHALVES; ++f) {  // feature half f: rows 128f .. of the stage
+                const uint64_t ad = smem_desc_sw128(sA + sa * A_BYTES + f * A_HALF);
+                // accumulator of (f, h): TMEM columns 256 (f + h) (one of them is 0)
+#pragma unroll
+                for (int k4 = 0; k4 < BK / 16; ++k4)  // +32 bytes per K=16 step inside the atom
+                  mma_f16_ss(d_tmem + (f + h) * 256, ad + 2 * k4, bd + 2 * k4, kIdesc,
+                             (kk | k4) != 0);
+              }
               mma_commit(empty_b + 8 * ib);
             } else {
               mbar_arrive(empty_b + 8 * ib);  // nothing read this half
@@ -445,17 +459,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t a = it % C::NACC, use = it / C::NACC;
       if (!mbar_wait(acc_full + 8 * a, use & 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
       tc_fence_after();
-      const int n0 = (tile / p.tok_tiles) * BM, m0 = (tile % p.tok_tiles) * TT;
-      const int feat = n0 + 32 * e + lane;
-      const bool fok = feat < p.n;
+      const int n0 = (tile / p.tok_tiles) * FM, m0 = (tile % p.tok_tiles) * TT;
       // column chunks that hold tokens (the MMAs wrote only the used halves)
       const int chunks = (p.m - m0 + 31) / 32 < TT / 32 ? (p.m - m0 + 31) / 32 : TT / 32;
 #pragma unroll 1
-      for (int c = 0; c < chunks; ++c) {
+      for (int cf = 0; cf < chunks * C::FHALVES; ++cf) {
+        const int f = cf / chunks, c = cf - f * chunks;  // feature half, token chunk
+        const int feat = n0 + BM * f + 32 * e + lane;
+        const bool fok = feat < p.n;
         uint32_t v[32];
-        TMEM_LD_32(tmem_base + ((uint32_t)(32 * e) << 16) + a * 256 + 32 * c, v);
+        TMEM_LD_32(tmem_base + ((uint32_t)(32 * e) << 16) + (a + f) * 256 + 32 * c, v);
         tmem_ld_wait();
-        if (c == chunks - 1) {
+        if (cf == chunks * C::FHALVES - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + 8 * a);
@@ -502,7 +517,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint16_t csc[3], nsc[3];
     int cur_key = -1, nxt_key = -1;
     auto load_block = [&](int tile, int u, uint32_t (&dst)[16], uint16_t (&sc)[3]) {
-      const int n = (tile / p.tok_tiles) * BM + r;
+      const int n = (tile / p.tok_tiles) * FM + r;
       const bool nok = n < p.n;
       const unsigned short* srow = reinterpret_cast<const unsigned short*>(p.scales) +
                                    (size_t)(nok ? n : 0) * p.G;
@@ -520,10 +535,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t g = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
-      const int n = (tile / p.tok_tiles) * BM + r;
+      const int n = (tile / p.tok_tiles) * FM + r;
       const bool nok = n < p.n;
       const uint8_t* wrow = p.w + (long long)(nok ? n : 0) * p.row_bytes;
       const __half* srow = p.scales + (size_t)(nok ? n : 0) * p.G;
+      // 256-feature tiles: this thread also expands row r + 128 into the
+      // stage's second M=128 operand tile
+      const bool nok2 = FM > BM && n + BM < p.n;
+      const uint8_t* wrow2 = p.w + (long long)(nok2 ? n + BM : 0) * p.row_bytes;
+      const __half* srow2 = p.scales + (size_t)(nok2 ? n + BM : 0) * p.G;
       for (int j = 0; j < p.nk; ++j, ++g) {
         if ((g & 1) != h) continue;
         const int kk = k_at(p, tile, j);  // the k-step this stage holds
@@ -536,8 +556,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint2 wv = *reinterpret_cast<const uint2*>(wrow + 8 * kk);
           const __half sc = srow[kk >> 1];
           const uint32_t s2 = nok ? (uint32_t(__half_as_ushort(sc)) * 0x10001u) : 0u;
+          uint2 wv2 = make_uint2(0u, 0u);
+          uint32_t s22 = 0u;
+          if constexpr (FM > BM) {
+            wv2 = *reinterpret_cast<const uint2*>(wrow2 + 8 * kk);
+            const __half sc2 = srow2[kk >> 1];
+            s22 = nok2 ? (uint32_t(__half_as_ushort(sc2)) * 0x10001u) : 0u;
+          }
           if (!mbar_wait(empty_a + 8 * s, ph ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); ok = false; break; }
           dq_binary(wv, s2, dst, sw);
+          if constexpr (FM > BM) dq_binary(wv2, s22, dst + A_HALF, sw);
         } else {
           const int u = kk / KPB;
           const int key = tile * nblk + u;
@@ -600,30 +628,38 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return BONSAI_ERR_CUDA;
   const bool ter = w->format == BONSAI_FMT_TERNARY;
-  auto smem_of = [](int a, int b, int b_bytes, bool lut) {
-    return a * A_BYTES + b * b_bytes + (lut ? LUT_BYTES : 0) + BAR_BYTES;
+  auto smem_of = [](int a, int a_bytes, int b, int b_bytes, bool lut) {
+    return a * a_bytes + b * b_bytes + (lut ? LUT_BYTES : 0) + BAR_BYTES;
   };
-  using CTN = Cfg<BONSAI_FMT_TERNARY, false>;
-  using CTW = Cfg<BONSAI_FMT_TERNARY, true>;
-  using CBN = Cfg<BONSAI_FMT_BINARY, false>;
-  using CBW = Cfg<BONSAI_FMT_BINARY, true>;
-  const int smem_wide = ter ? smem_of(CTW::A, CTW::B, CTW::B_BYTES, true)
-                            : smem_of(CBW::A, CBW::B, CBW::B_BYTES, false);
-  // Wide tiles pay off where the dequantisers limit (ternary) as long as the
-  // SMs stay about as busy: measured at M=512, N=17408 ternary +7%, binary
-  // -9% (its cheap expansion gains nothing and it loses the epilogue overlap
-  // and two X stages), and a layer loses 13-28% when its N=5120 products drop
-  // from 80 to 40 tiles. Busy fraction = tiles / (waves * SMs).
+  using CTN = Cfg<BONSAI_FMT_TERNARY, NARROW>;
+  using CTW = Cfg<BONSAI_FMT_TERNARY, WIDE>;
+  using CBN = Cfg<BONSAI_FMT_BINARY, NARROW>;
+  using CBT = Cfg<BONSAI_FMT_BINARY, TALL>;
+  const int smem_narrow = ter ? smem_of(CTN::A, CTN::A_BYTES, CTN::B, CTN::B_BYTES, true)
+                              : smem_of(CBN::A, CBN::A_BYTES, CBN::B, CBN::B_BYTES, false);
+  const int smem_big = ter ? smem_of(CTW::A, CTW::A_BYTES, CTW::B, CTW::B_BYTES, true)
+                           : smem_of(CBT::A, CBT::A_BYTES, CBT::B, CBT::B_BYTES, false);
+  // Besides the 128-feature x 256-token tiles (two TMEM accumulators, the
+  // epilogue overlapping the next tile), each format has a larger tile with
+  // one 512-column accumulator: ternary 512 tokens (halves the dequantisation
+  // per FLOP, the ternary limiter: +7% at M=512, N=17408), binary 256
+  // features (halves the activation-tile traffic per FLOP, where binary's MMA
+  // thread waits; 512-token tiles measured -9% for binary). The larger tile
+  // is taken when the SMs stay about as busy (busy = tiles / (waves * SMs)):
+  // a layer's N=5120 products would otherwise drop from 80 to 40 tiles.
   const long long sms_l = device_sm_count();
-  const long long ftiles = (w->n + BM - 1) / BM;
   auto busy = [&](long long tiles) {
     return (double)tiles / (double)(((tiles + sms_l - 1) / sms_l) * sms_l);
   };
-  const double busy_narrow = busy(ftiles * ((m + 255) / 256));
-  const double busy_wide = busy(ftiles * ((m + 511) / 512));
-  const bool wide = ter && m > BN && busy_wide >= 0.85 * busy_narrow &&
-                    smem_wide <= device_max_smem_optin();
-  const int tt = wide ? 512 : 256;
+  const long long ft = (w->n + BM - 1) / BM, ft2 = (w->n + 2 * BM - 1) / (2 * BM);
+  const long long tok = (m + 255) / 256, tok2 = (m + 511) / 512;
+  const double busy_narrow = busy(ft * tok);
+  const double busy_big = ter ? busy(ft * tok2) : busy(ft2 * tok);
+  const bool big = (ter ? m > BN : true) && busy_big >= 0.85 * busy_narrow &&
+                   smem_big <= device_max_smem_optin();
+  const int mode = !big ? NARROW : (ter ? WIDE : TALL);
+  const int tt = mode == WIDE ? 512 : 256;
+  const int fm = mode == TALL ? 256 : BM;
 
   Params p{};
   p.w = static_cast<const uint8_t*>(w->packed);
@@ -636,19 +672,17 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   p.G = p.k / 128;
   p.nk = p.k / BK;
   p.tok_tiles = (int)((m + tt - 1) / tt);
-  p.tiles = ((p.n + BM - 1) / BM) * p.tok_tiles;
+  p.tiles = ((p.n + fm - 1) / fm) * p.tok_tiles;
   p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.y_stride = swiglu ? p.n / 2 : p.n;
 
-  const int smem = wide ? smem_wide
-                       : (ter ? smem_of(CTN::A, CTN::B, CTN::B_BYTES, true)
-                              : smem_of(CBN::A, CBN::B, CBN::B_BYTES, false));
+  const int smem = big ? smem_big : smem_narrow;
   if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
-  const void* fn = ter ? (wide ? (const void*)gemm_kernel<BONSAI_FMT_TERNARY, true>
-                               : (const void*)gemm_kernel<BONSAI_FMT_TERNARY, false>)
-                       : (wide ? (const void*)gemm_kernel<BONSAI_FMT_BINARY, true>
-                               : (const void*)gemm_kernel<BONSAI_FMT_BINARY, false>);
+  const void* fn = ter ? (big ? (const void*)gemm_kernel<BONSAI_FMT_TERNARY, WIDE>
+                              : (const void*)gemm_kernel<BONSAI_FMT_TERNARY, NARROW>)
+                       : (big ? (const void*)gemm_kernel<BONSAI_FMT_BINARY, TALL>
+                              : (const void*)gemm_kernel<BONSAI_FMT_BINARY, NARROW>);
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess)
     return BONSAI_ERR_CUDA;
 

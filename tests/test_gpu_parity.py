@@ -303,6 +303,25 @@ def test_gemm_wide_tiles(m):
     y.check()
 
 
+@pytest.mark.parametrize("n,m", [(17040, 9), (17040, 300), (17040, 600), (16900, 257)])
+def test_gemm_tall_tiles(n, m):
+    """Binary products with enough feature tiles to take 256-feature tiles:
+    the last tile's second 128-row half partly (n = 17040) or wholly
+    (n = 16900) past n; ragged token tiles; sampled outputs."""
+    t = torch()
+    k = 384
+    w, packed, scales = weights(BIN, 220 + m, n, k)
+    x = synth.gen_x(221 + m, m, k)
+    y = Guarded((m, n), t.float16)
+    sb.bonsai_gemm(w, dev(x), y.t)
+    assert sb.bonsai_check_async() == 0
+    ms = sample_idx(m, [0, 8, 255, 256, m - 1], 16, 14)
+    ns = sample_idx(n, [0, 127, 128, 255, 256, 16895, 16896, 16900 - 1, n - 17, n - 16, n - 1], 60, 15)
+    y_ref, nrm = oracle.linear(BIN, packed, scales, x, n_sel=ns, m_sel=ms)
+    assert_close(host(y.t)[np.ix_(ms, ns)], y_ref, nrm, "tall tiles n=%d m=%d" % (n, m))
+    y.check()
+
+
 def sample_idx(total, edges, count, seed):
     rng = np.random.default_rng(seed)
     idx = set(int(e) for e in edges if 0 <= e < total)
