@@ -655,7 +655,12 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   const long long tok = (m + 255) / 256, tok2 = (m + 511) / 512;
   const double busy_narrow = busy(ft * tok);
   const double busy_big = ter ? busy(ft * tok2) : busy(ft2 * tok);
-  const bool big = (ter ? m > BN : true) && busy_big >= 0.85 * busy_narrow &&
+  // Binary takes 256-feature tiles only while every SM gets at most one: the
+  // gain is the halved X traffic, and with several tiles per SM the
+  // epilogue no longer overlapped cancels it (interleaved A/B on one GPU:
+  // M=512, N=17408 +13%, M=4096 even, a layer whose q/k/v and gate/up took
+  // them -4.5%).
+  const bool big = (ter ? m > BN : ft2 * tok <= sms_l) && busy_big >= 0.85 * busy_narrow &&
                    smem_big <= device_max_smem_optin();
   const int mode = !big ? NARROW : (ter ? WIDE : TALL);
   const int tt = mode == WIDE ? 512 : 256;
