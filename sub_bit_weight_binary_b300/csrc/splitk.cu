@@ -124,8 +124,11 @@ bonsai_status splitk_launch(const bonsai_weights* w, const uint16_t* x, uint16_t
   unsigned int* counters = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(base) +
                                                            kPartialBytes);
   if (first &&
-      cudaMemsetAsync(counters, 0, kMaxTiles * sizeof(unsigned int), stream) != cudaSuccess)
+      cudaMemsetAsync(counters, 0, kMaxTiles * sizeof(unsigned int), stream) != cudaSuccess) {
+    std::lock_guard<std::mutex> lock(mu);
+    cleared[dev] = false;  // not cleared after all: the next call tries again
     return BONSAI_ERR_CUDA;
+  }
 
   Params p{};
   p.packed = static_cast<const uint8_t*>(w->packed);
