@@ -649,8 +649,9 @@ class GemmWorkload:
 
     def roofline(self, r, pk):
         a = self.flops() / (r["kernel_ms"] / 1e3) / 1e12
-        return {"bound": "tensor", "kernel": "gemm_kernel<%d> (%s)" % (
-                    self.fmt, "ternary" if self.fmt == 2 else "binary"),
+        return {"bound": "tensor", "kernel": "gemm_kernel<%d, %s> (%s)" % (
+                    self.fmt, "wide or narrow tiles" if self.fmt == 2 else "tall or narrow tiles",
+                    "ternary" if self.fmt == 2 else "binary"),
                 "achieved": round(a, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": round(a / pk["bf16"], 4),
                 "traffic": profiled_traffic("gemm_%s_m512_k5120_n17408.md" % (
