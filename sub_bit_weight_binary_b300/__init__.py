@@ -6,6 +6,17 @@ of libbonsai.so. PyTorch supplies device memory and streams. If the library
 is missing the calls raise: there is no CPU path.
 
 Build the library with ``python -m sub_bit_weight_binary_b300.build``.
+
+Typical use (all tensors on the GPU, FP16 activations)::
+
+    import torch, sub_bit_weight_binary_b300 as sb
+    rb = sb.bonsai_packed_row_bytes(sb.BONSAI_FMT_TERNARY, k)
+    packed = torch.empty((n, rb), dtype=torch.uint8, device="cuda")
+    sb.bonsai_pack_ternary(codes_int8_n_by_k, packed)          # codes in {-1, 0, +1}
+    w = sb.Weights(sb.BONSAI_FMT_TERNARY, n, k, packed, scales_fp16_n_by_k128)
+    sb.bonsai_gemv(w, x_k, y_n)                                # one token
+    sb.bonsai_gemm(w, x_m_by_k, y_m_by_n)                      # m tokens
+    sb.check()                                                 # sync, raise on a device status
 """
 from __future__ import annotations
 
