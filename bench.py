@@ -728,6 +728,7 @@ class HadamardWorkload:
 
     def __init__(self, name, m=512, k=5120, block=128):
         self.name, self.m, self.k, self.block = name, m, k, block
+        self.reps = max(1, math.ceil(2 * L2_BYTES / (2 * self.m * self.k * 2)) + 1)
 
     def unit_bytes(self):
         return 2 * self.m * self.k * 2 + self.k // 8  # x in, out written, signs
@@ -736,7 +737,6 @@ class HadamardWorkload:
         import torch
         from sub_bit_weight_binary_b300 import synth
         seed = synth.config_seed(6)
-        self.reps = max(1, math.ceil(2 * L2_BYTES / (2 * self.m * self.k * 2)) + 1)
         x = torch.from_numpy(synth.gen_x(seed, self.m, self.k).view(np.float16)).cuda()
         self.x = [x.clone() for _ in range(self.reps)]
         self.out = [torch.empty_like(x) for _ in range(self.reps)]
