@@ -714,3 +714,62 @@ def test_graph_capture_matches_eager():
     assert sb.bonsai_check_async() == 0
     for a, b in zip(eager, graphed):
         assert t.equal(a.view(t.int16), b.view(t.int16))
+
+
+def test_graph_capture_chained_newer_entry_points():
+    """The later entry points captured into one CUDA graph, each consuming the
+    previous one's output (as in a decode layer): Hadamard rotation -> gated
+    feed-forward (decode and tensor-core paths) -> down product, and FP16
+    binarisation -> XNOR. Replays give the bits of eager calls."""
+    t = torch()
+    k, f = 1024, 256
+    wgu, _, _ = weights(TER, 40, 2 * f, k, flags=sb.BONSAI_WEIGHTS_PREFETCH)
+    wdown, _, _ = weights(BIN, 41, 320, f)
+    wx = sb.Weights(BIN, 384, k, dev(synth.gen_binary_words(42, 384, k).view(np.uint8).reshape(384, -1)),
+                    dev(synth.gen_scales(43, 384, k)))
+    signs = dev(synth.gen_binary_words(44, 1, k)[0].view(np.int32))
+    x1 = dev(synth.gen_x(45, 1, k))
+    xm = dev(synth.gen_x(46, 300, k))
+
+    def bufs():
+        return {"r1": t.empty((1, k), dtype=t.float16, device="cuda"),
+                "rm": t.empty((300, k), dtype=t.float16, device="cuda"),
+                "h1": t.empty((1, f), dtype=t.float16, device="cuda"),
+                "hm": t.empty((300, f), dtype=t.float16, device="cuda"),
+                "y1": t.empty((1, 320), dtype=t.float16, device="cuda"),
+                "ym": t.empty((300, 320), dtype=t.float16, device="cuda"),
+                "bits": t.empty((300, k // 32), dtype=t.int32, device="cuda"),
+                "as": t.empty(300, dtype=t.float16, device="cuda"),
+                "d": t.empty((300, 384), dtype=t.int32, device="cuda"),
+                "yx": t.empty((300, 384), dtype=t.float16, device="cuda")}
+
+    def run(b):
+        sb.bonsai_hadamard(x1, b["r1"], 128, signs)
+        sb.bonsai_hadamard(xm, b["rm"], 256, signs)
+        sb.bonsai_gemm_swiglu(wgu, b["r1"], b["h1"])
+        sb.bonsai_gemm_swiglu(wgu, b["rm"], b["hm"])
+        sb.bonsai_gemm(wdown, b["h1"], b["y1"])
+        sb.bonsai_gemm(wdown, b["hm"], b["ym"])
+        sb.bonsai_binarize_activations(b["rm"], b["bits"], b["as"])
+        sb.bonsai_xnor_gemm(b["bits"], b["as"], wx, b["d"], b["yx"])
+
+    eager, graphed = bufs(), bufs()
+    run(eager)
+    t.cuda.synchronize()
+    assert sb.bonsai_check_async() == 0
+    s = t.cuda.Stream()
+    s.wait_stream(t.cuda.current_stream())
+    with t.cuda.stream(s):
+        run(graphed)  # eager once on the capture stream: one-time set-up outside the capture
+    t.cuda.current_stream().wait_stream(s)
+    t.cuda.synchronize()
+    g = t.cuda.CUDAGraph()
+    with t.cuda.graph(g):
+        run(graphed)
+    for _ in range(3):
+        g.replay()
+    assert sb.bonsai_check_async() == 0
+    for name in eager:
+        a, b = eager[name], graphed[name]
+        assert t.equal(a.view(t.int16) if a.dtype == t.float16 else a,
+                       b.view(t.int16) if b.dtype == t.float16 else b), name
