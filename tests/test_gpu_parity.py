@@ -473,7 +473,7 @@ def test_swiglu_full(fmt, f, k, m):
     h.check()
 
 
-@pytest.mark.parametrize("fmt,m", [(BIN, 1), (TER, 1), (TER, 8), (BIN, 512), (TER, 512)])
+@pytest.mark.parametrize("fmt,m", [(BIN, 1), (TER, 1), (TER, 8), (BIN, 100), (BIN, 512), (TER, 512)])
 def test_swiglu_workload(fmt, m):
     """Gate/up of the 64-layer model (F=17408, K=5120), sampled features."""
     t = torch()
