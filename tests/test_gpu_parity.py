@@ -415,7 +415,8 @@ def test_gemm_down_projection_sampled(fmt):
     y.check()
 
 
-@pytest.mark.parametrize("fmt,n,k", [(TER, 17408, 5120), (BIN, 1024, 1024), (TER, 33, 640)])
+@pytest.mark.parametrize("fmt,n,k", [(TER, 17408, 5120), (BIN, 1024, 1024), (TER, 33, 640),
+                                     (TER, 20, 65536)])  # last: tensor-core fallback, y into host memory
 def test_gemv_host_buffers(fmt, n, k):
     """bonsai_gemv_host (host x in, host y out, one call) gives the bits of
     bonsai_gemv and meets the oracle's bound; pinned and pageable host memory."""
