@@ -188,6 +188,35 @@ def profiled_traffic(summary):
     return int(t.group(1)) if h.hexdigest() == m.group(2) else None
 
 
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def timed_passes(fn, min_seconds):
+    """Run fn() until min_seconds have passed (at least once, at most ~30 s);
+    returns (passes, elapsed seconds)."""
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        fn()
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or el > 30:
+            return passes, el
+
+
+def cpu_baseline_record(value, unit, sample, cores=1):
+    return {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
+            "cpu": cpu_model(), "sample": sample}
+
+
 def make_weights(fmt, n, k, seed, tid_w, tid_s, flags):
     """Seeded weights generated on the device (codes -> pack for ternary)."""
     import torch
@@ -207,9 +236,16 @@ def make_weights(fmt, n, k, seed, tid_w, tid_s, flags):
     return sb.Weights(fmt, n, k, packed, scales, flags)
 
 
-def weight_bytes(fmt, n, k):
-    import sub_bit_weight_binary_b300 as sb
-    return n * sb.bonsai_packed_row_bytes(fmt, k) + n * (k // 128) * 2
+def weight_bytes(fmt, n, k, ref=False):
+    """Packed + scale bytes of an n x k matrix. The reference (oracle) arm
+    takes the row size from the oracle, so it never loads libbonsai.so."""
+    if ref:
+        import oracle
+        rb = oracle.row_bytes(fmt, k)
+    else:
+        import sub_bit_weight_binary_b300 as sb
+        rb = sb.bonsai_packed_row_bytes(fmt, k)
+    return n * rb + n * (k // 128) * 2
 
 
 def upload_graph(g):
@@ -232,9 +268,20 @@ def upload_graph(g):
         return False
 
 
-def graph_time(fn_steps, steps, warmup, clocks=None):
+SPIN_CYCLES = 2_000_000  # ~1 ms device spin enqueued ahead of each timed replay
+TIMED_REPS = 5
+
+
+def graph_time(fn_steps, steps, warmup, clocks=None, reps=TIMED_REPS):
     """Capture `steps` launches in a CUDA graph (and `warmup` in another),
-    replay, return the elapsed milliseconds of the timed graph."""
+    then time `reps` replays of it and return the median elapsed
+    milliseconds of one replay.
+
+    Each timed replay is preceded by a ~1 ms spin kernel on the same stream,
+    so the host has enqueued the replay (and both events) before the device
+    reaches the first event: the event pair then brackets device time only,
+    whatever the step count (without it, a short replay also timed the host
+    submitting the graph to an idle device)."""
     import torch
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -249,17 +296,21 @@ def graph_time(fn_steps, steps, warmup, clocks=None):
         fn_steps(warmup, steps)
     gw.replay()
     upload_graph(gt)
+    gt.replay()  # one untimed replay: the graph is resident on the device
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
     if clocks:
         clocks.__enter__()
-    e0.record()
-    gt.replay()
-    e1.record()
+    for e0, e1 in ev:
+        torch.cuda._sleep(SPIN_CYCLES)
+        e0.record()
+        gt.replay()
+        e1.record()
     torch.cuda.synchronize()
     if clocks:
         clocks.__exit__()
-    return e0.elapsed_time(e1)
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
 
 
 def step_graph(fn):
@@ -279,12 +330,12 @@ class GemvWorkload:
     """Decode product M=1 over rotating weight replicas."""
     kind = "gemv"
 
-    def __init__(self, fmt, n, k, cfg_id, name):
-        self.fmt, self.n, self.k, self.cfg_id, self.name = fmt, n, k, cfg_id, name
+    def __init__(self, fmt, n, k, cfg_id, name, ref=False):
+        self.fmt, self.n, self.k, self.cfg_id, self.name, self.ref = fmt, n, k, cfg_id, name, ref
         self.reps = max(1, math.ceil(2 * L2_BYTES / self.unit_bytes()) + 1)
 
     def unit_bytes(self):
-        return weight_bytes(self.fmt, self.n, self.k)
+        return weight_bytes(self.fmt, self.n, self.k, self.ref)
 
     def setup(self):
         import torch
@@ -312,27 +363,41 @@ class GemvWorkload:
         ms = graph_time(self.launches, steps, warmup, clocks)
         return {"ms": ms, "steps": steps, "launches": steps, "kernel_ms": ms / steps}
 
-    def measure_e2e(self, steps, warmup):
-        """Per step one call of a prepared bonsai_gemv_host (GemvHostPlan:
-        the C call with host buffers captured once, replayed per token):
-        pinned host x copied in, the product, y copied out to pinned host
-        memory, all inside the timed region."""
+    def measure_e2e(self, steps, warmup, reps=TIMED_REPS):
+        """End to end through the public API, host buffers in and out: per
+        step, pinned host x copied in, the decode product, y copied out to
+        pinned host memory. Two forms, each the median over `reps` runs of
+        `steps` consecutive steps issued from the host (host submission
+        included; nothing is enqueued ahead of the timed region):
+          plan  -- a prepared GemvHostPlan (the C call with host buffers,
+                   captured once and replayed per token);
+          eager -- the plain bonsai_gemv_host C call per token."""
         import torch
         import sub_bit_weight_binary_b300 as sb
         plans = [sb.GemvHostPlan(w, self.x_host, self.x, self.y, self.y_host) for w in self.w]
 
-        def one(i):
+        def plan(i):
             plans[i % self.reps]()
-        for i in range(warmup):
-            one(i)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(steps):
-            one(i)
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1), self.k * 2, self.n * 2
+
+        def eager(i):
+            sb.bonsai_gemv_host(self.w[i % self.reps], self.x_host, self.x, self.y, self.y_host)
+
+        out = {}
+        for name, one in (("plan", plan), ("eager", eager)):
+            for i in range(warmup):
+                one(i)
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for i in range(steps):
+                    one(i)
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            out[name] = statistics.median(times)
+        return out, self.k * 2, self.n * 2
 
     def value(self, ms, steps):
         return self.unit_bytes() * steps / (ms / 1e3) / 1e9, "GB/s"
@@ -430,8 +495,8 @@ class SmallMWorkload(GemvWorkload):
     M=5 is two launches)."""
     kind = "gemv_m"
 
-    def __init__(self, fmt, n, k, m, cfg_id, name):
-        super().__init__(fmt, n, k, cfg_id, name)
+    def __init__(self, fmt, n, k, m, cfg_id, name, ref=False):
+        super().__init__(fmt, n, k, cfg_id, name, ref)
         self.m = m
 
     def setup(self):
@@ -558,6 +623,7 @@ class SweepWorkload:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if clocks:
             clocks.__enter__()
+        torch.cuda._sleep(SPIN_CYCLES)  # the first replay is enqueued before the device reaches e0
         e0.record()
         for _ in range(steps):
             g.replay()
@@ -590,6 +656,29 @@ class SweepWorkload:
                 "timing": "one CUDA graph per token (%d launches), replayed per step" % (
                     self.layers * len(SWEEP_SHAPES)),
                 "l2": "inputs larger than L2: %.2f GB of weights per token" % (self.unit_bytes() / 1e9)}
+
+
+    def cpu_sample(self, min_seconds=3.0, rows=64):
+        """The oracle over `rows` output rows of each of a layer's four
+        products (same shapes, seeded weights), scaled to whole-token time:
+        64 layers x sum over products of (time per row x rows of the product)."""
+        import oracle
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(3)
+        per_token = 0.0
+        for j, (n, k) in enumerate(SWEEP_SHAPES):
+            tid = synth.sweep_tid(0, j)
+            if self.fmt == 2:
+                packed = oracle.pack_ternary(synth.gen_ternary_codes(seed, rows, k, tid=tid))
+            else:
+                packed = synth.gen_binary_words(seed, rows, k, tid=tid).view(np.uint8).reshape(rows, -1)
+            scales = synth.gen_scales(seed, rows, k, tid=tid + 8)
+            x = synth.gen_x(seed + k, 1, k)
+            passes, el = timed_passes(lambda: oracle.linear(self.fmt, packed, scales, x),
+                                      min_seconds / len(SWEEP_SHAPES))
+            per_token += self.layers * (el / passes) * (n / rows)
+        return 1.0 / per_token, "tok/s", ("sampled: %d rows of each of the 4 products of a layer, "
+                                          "scaled to 64 layers x all rows, one thread" % rows)
 
 
 class GemmWorkload:
@@ -664,6 +753,26 @@ class GemmWorkload:
                 "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
 
 
+    def cpu_sample(self, min_seconds=3.0, rows=None):
+        """The oracle for all M tokens over a sample of output features,
+        scaled to the whole product's FLOP rate."""
+        import oracle
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(4)
+        rows = rows or (64 if self.m <= 512 else 8)
+        tid = synth.TID_WTER if self.fmt == 2 else synth.TID_WBIN
+        if self.fmt == 2:
+            packed = oracle.pack_ternary(synth.gen_ternary_codes(seed, rows, self.k, tid=tid))
+        else:
+            packed = synth.gen_binary_words(seed, rows, self.k, tid=tid).view(np.uint8).reshape(rows, -1)
+        scales = synth.gen_scales(seed, rows, self.k)
+        x = synth.gen_x(seed, self.m, self.k)
+        passes, el = timed_passes(lambda: oracle.linear(self.fmt, packed, scales, x), min_seconds)
+        flops = passes * 2.0 * self.m * rows * self.k
+        return flops / el / 1e12, "TFLOP/s", ("sampled: all %d tokens x %d of %d output features, "
+                                              "one thread" % (self.m, rows, self.n))
+
+
 class LayerGemmWorkload(GemmWorkload):
     """One decoder layer of prompt processing on the tensor cores: the 7
     weight products (q, k, v, o, gate, up, down) as 4 launches -- q/k/v and
@@ -721,6 +830,30 @@ class LayerGemmWorkload(GemmWorkload):
                 "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
 
 
+    def cpu_sample(self, min_seconds=3.0, rows=16):
+        """The oracle for all M tokens over `rows` features of each of the
+        layer's four products, scaled to the layer's FLOP rate."""
+        import oracle
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(4)
+        x = synth.gen_x(seed, self.m, 5120)
+        t_layer = 0.0
+        for j, (n, k) in enumerate(SWEEP_SHAPES):
+            tid = synth.sweep_tid(0, j)
+            if self.fmt == 2:
+                packed = oracle.pack_ternary(synth.gen_ternary_codes(seed, rows, k, tid=tid))
+            else:
+                packed = synth.gen_binary_words(seed, rows, k, tid=tid).view(np.uint8).reshape(rows, -1)
+            scales = synth.gen_scales(seed, rows, k, tid=tid + 8)
+            xx = x if k == 5120 else synth.gen_x(seed + 1, self.m, k)
+            passes, el = timed_passes(lambda: oracle.linear(self.fmt, packed, scales, xx),
+                                      min_seconds / len(SWEEP_SHAPES))
+            t_layer += (el / passes) * (n / rows)
+        return self.flops() / t_layer / 1e12, "TFLOP/s", (
+            "sampled: all %d tokens x %d features of each of the 4 products, scaled, one thread"
+            % (self.m, rows))
+
+
 class HadamardWorkload:
     """Signed Hadamard rotation of FP16 activation rows (block 128), over
     rotating input replicas larger than L2, timed in a CUDA graph."""
@@ -771,6 +904,19 @@ class HadamardWorkload:
                 "l2": "inputs larger than L2 (rotating replicas)"}
 
 
+    def cpu_sample(self, min_seconds=3.0, rows=64):
+        """The oracle over the first `rows` of the M rows, scaled to GB/s of
+        the whole workload's bytes."""
+        import oracle
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(6)
+        x = synth.gen_x(seed, self.m, self.k)[:rows]
+        bits = synth.gen_binary_words(seed + 1, 1, self.k)[0]
+        passes, el = timed_passes(lambda: oracle.hadamard(x, self.block, bits), min_seconds)
+        return (passes * self.unit_bytes() * rows / self.m / el / 1e9, "GB/s",
+                "sampled: %d of %d rows, one thread" % (rows, self.m))
+
+
 class XnorWorkload:
     kind = "xnor"
 
@@ -817,6 +963,20 @@ class XnorWorkload:
     def config(self):
         return {"workload": self.name, "m": self.m, "k": self.k, "n": self.n,
                 "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
+
+
+    def cpu_sample(self, min_seconds=3.0, rows=256):
+        """The oracle (integer dot from unpacked +-1 codes) for all M rows
+        over a sample of output features, scaled to bit-TOPS."""
+        import oracle
+        from sub_bit_weight_binary_b300 import synth
+        seed = synth.config_seed(5)
+        a_bits, a_s, w_bits, sc = synth.gen_xnor_inputs(seed, self.m, rows, self.k)
+        passes, el = timed_passes(lambda: oracle.xnor(a_bits, a_s, w_bits, sc, self.k),
+                                  min_seconds)
+        ops = passes * 2.0 * self.m * rows * self.k
+        return ops / el / 1e12, "bit-TOPS", ("sampled: all %d rows x %d of %d output features, "
+                                             "one thread" % (self.m, rows, self.n))
 
 
 class XnorFp16Workload(XnorWorkload):
@@ -883,42 +1043,49 @@ class XnorFp16Workload(XnorWorkload):
 
 
 WORKLOADS = {
-    "ter_gemv": lambda: GemvWorkload(2, 17408, 5120, 2,
-                                     "ternary GEMV M=1 K=5120 N=17408 (decode)"),
-    "bin_gemv_1k": lambda: GemvWorkload(1, 1024, 1024, 1, "binary GEMV M=1 K=1024 N=1024 (decode)"),
-    "bin_gemv": lambda: GemvWorkload(1, 17408, 5120, 2, "binary GEMV M=1 K=5120 N=17408 (decode)"),
-    "ter_gemv_m5": lambda: SmallMWorkload(2, 17408, 5120, 5, 2,
-                                          "ternary decode product M=5 K=5120 N=17408 "
-                                          "(speculative verification)"),
-    "bin_gemv_m5": lambda: SmallMWorkload(1, 17408, 5120, 5, 2,
-                                          "binary decode product M=5 K=5120 N=17408 "
-                                          "(speculative verification)"),
-    "sweep_bin": lambda: SweepWorkload(1, "64-layer decode sweep, binary, batch 1"),
-    "sweep_ter": lambda: SweepWorkload(2, "64-layer decode sweep, ternary, batch 1"),
-    "gemm512_bin": lambda: GemmWorkload(1, 512, "prefill GEMM M=512 K=5120 N=17408, binary"),
-    "gemm512_ter": lambda: GemmWorkload(2, 512, "prefill GEMM M=512 K=5120 N=17408, ternary"),
-    "gemm4096_bin": lambda: GemmWorkload(1, 4096, "DiT GEMM M=4096 K=5120 N=17408, binary"),
-    "gemm4096_ter": lambda: GemmWorkload(2, 4096, "DiT GEMM M=4096 K=5120 N=17408, ternary"),
-    "layer_bin": lambda: SweepWorkload(1, "64-layer decode, fused feed-forward, binary, batch 1",
+    "ter_gemv": lambda ref=False: GemvWorkload(2, 17408, 5120, 2,
+                                               "ternary GEMV M=1 K=5120 N=17408 (decode)", ref),
+    "bin_gemv_1k": lambda ref=False: GemvWorkload(1, 1024, 1024, 1,
+                                                  "binary GEMV M=1 K=1024 N=1024 (decode)", ref),
+    "bin_gemv": lambda ref=False: GemvWorkload(1, 17408, 5120, 2,
+                                               "binary GEMV M=1 K=5120 N=17408 (decode)", ref),
+    "ter_gemv_m5": lambda ref=False: SmallMWorkload(2, 17408, 5120, 5, 2,
+                                                    "ternary decode product M=5 K=5120 N=17408 "
+                                                    "(speculative verification)", ref),
+    "bin_gemv_m5": lambda ref=False: SmallMWorkload(1, 17408, 5120, 5, 2,
+                                                    "binary decode product M=5 K=5120 N=17408 "
+                                                    "(speculative verification)", ref),
+    "sweep_bin": lambda ref=False: SweepWorkload(1, "64-layer decode sweep, binary, batch 1"),
+    "sweep_ter": lambda ref=False: SweepWorkload(2, "64-layer decode sweep, ternary, batch 1"),
+    "gemm512_bin": lambda ref=False: GemmWorkload(1, 512, "prefill GEMM M=512 K=5120 N=17408, binary"),
+    "gemm512_ter": lambda ref=False: GemmWorkload(2, 512, "prefill GEMM M=512 K=5120 N=17408, ternary"),
+    "gemm4096_bin": lambda ref=False: GemmWorkload(1, 4096, "DiT GEMM M=4096 K=5120 N=17408, binary"),
+    "gemm4096_ter": lambda ref=False: GemmWorkload(2, 4096, "DiT GEMM M=4096 K=5120 N=17408, ternary"),
+    "layer_bin": lambda ref=False: SweepWorkload(1, "64-layer decode, fused feed-forward, binary, batch 1",
                                        fused=True),
-    "layer_ter": lambda: SweepWorkload(2, "64-layer decode, fused feed-forward, ternary, batch 1",
+    "layer_ter": lambda ref=False: SweepWorkload(2, "64-layer decode, fused feed-forward, ternary, batch 1",
                                        fused=True),
-    "pp512_layer_bin": lambda: LayerGemmWorkload(1, 512, "prefill M=512, one decoder layer "
+    "pp512_layer_bin": lambda ref=False: LayerGemmWorkload(1, 512, "prefill M=512, one decoder layer "
                                                  "(7 products, fused feed-forward), binary"),
-    "pp512_layer_ter": lambda: LayerGemmWorkload(2, 512, "prefill M=512, one decoder layer "
+    "pp512_layer_ter": lambda ref=False: LayerGemmWorkload(2, 512, "prefill M=512, one decoder layer "
                                                  "(7 products, fused feed-forward), ternary"),
-    "hadamard": lambda: HadamardWorkload("signed Hadamard rotation of x, M=512 K=5120, block 128"),
-    "xnor": lambda: XnorWorkload("XNOR-popcount GEMM M=512 K=4096 N=4096"),
-    "xnor_fp16": lambda: XnorFp16Workload(
+    "hadamard": lambda ref=False: HadamardWorkload("signed Hadamard rotation of x, M=512 K=5120, block 128"),
+    "xnor": lambda ref=False: XnorWorkload("XNOR-popcount GEMM M=512 K=4096 N=4096"),
+    "xnor_fp16": lambda ref=False: XnorFp16Workload(
         "FP16 activations binarised, then XNOR-popcount GEMM M=512 K=4096 N=4096"),
 }
 SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("ter_gemv_m5", 2000, 20),
-             ("bin_gemv_m5", 2000, 20), ("sweep_bin", 30, 3), ("sweep_ter", 30, 3),
+             ("bin_gemv_m5", 2000, 20), ("sweep_bin", 128, 3), ("sweep_ter", 128, 3),
              ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
-             ("gemm4096_ter", 5, 2), ("layer_bin", 30, 3), ("layer_ter", 30, 3),
+             ("gemm4096_ter", 5, 2), ("layer_bin", 128, 3), ("layer_ter", 128, 3),
              ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("hadamard", 200, 10),
              ("xnor", 20, 3),
              ("xnor_fp16", 20, 3)]
+ROOFLINE_KEYS = ("bound", "achieved", "peak", "unit", "frac", "traffic")
+
+
+def short_roofline(rf):
+    return {k: rf.get(k) for k in ROOFLINE_KEYS}
 
 
 # -------------------------------------------------------------------- runs
@@ -947,19 +1114,23 @@ def run_ours(args, world, rank):
         "clocks": clk.report(),
     }
     if wl.kind == "gemv":
-        ms_e, bi, bo = wl.measure_e2e(min(args.steps, 2000), args.warmup)
-        ms_e = max_over_ranks(world, ms_e)
-        ev, _ = wl.value(ms_e, min(args.steps, 2000))
+        e2e_steps = min(args.steps, 2000)
+        times, bi, bo = wl.measure_e2e(e2e_steps, args.warmup)
+        ms_plan = max_over_ranks(world, times["plan"])
+        ms_eager = max_over_ranks(world, times["eager"])
+        ev, _ = wl.value(ms_plan, e2e_steps)
+        ee, _ = wl.value(ms_eager, e2e_steps)
         line["e2e"] = {"value": round(ev * world, 3), "unit": unit, "h2d_bytes_per_step": bi,
-                       "d2h_bytes_per_step": bo,
-                       "how": "per step one GemvHostPlan call (bonsai_gemv_host, the C ABI call with "
-                              "host buffers, captured once and replayed): pinned host x copied in, the "
-                              "product, y copied out to pinned host memory"}
+                       "d2h_bytes_per_step": bo, "steps": e2e_steps,
+                       "how": "median of %d runs of %d host-issued steps; per step one GemvHostPlan "
+                              "call (bonsai_gemv_host captured once, replayed): pinned host x in, the "
+                              "product, y out to pinned host memory" % (TIMED_REPS, e2e_steps),
+                       "eager": {"value": round(ee * world, 3), "unit": unit,
+                                 "how": "the plain bonsai_gemv_host C call per step"}}
     sb.check()
     if rank == 0 and not args.no_cpu_baseline and world == 1 and hasattr(wl, "cpu_sample"):
         v, u, sample = wl.cpu_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(v, 5), "unit": u, "cores": 1, "kind": "oracle",
-                                "sample": sample}
+        line["cpu_baseline"] = cpu_baseline_record(v, u, sample)
         if wl.kind == "gemv":
             from sub_bit_weight_binary_b300 import synth
             av, ac, asample = oracle_all_cores(wl.fmt, wl.n, wl.k, synth.config_seed(wl.cfg_id),
@@ -978,15 +1149,23 @@ def run_ours(args, world, rank):
             c2 = ClockSampler(torch.cuda.current_device())
             r2 = w2.measure(steps, warm, c2)
             v2, u2 = w2.value(r2["ms"], r2["steps"])
-            sec.append({"workload": w2.name, "value": round(v2, 3), "unit": u2,
-                        "steps": r2["steps"], "ms_per_step": round(r2["ms"] / r2["steps"], 6),
-                        "roofline": w2.roofline(r2, pk) if w2.kind != "xnor" else
-                        w2.roofline(r2, pk, c2.report().get("sm_mhz")),
-                        "gpu_launches": r2["launches"],
-                        "clocks": c2.report()})
+            rf = w2.roofline(r2, pk) if w2.kind != "xnor" else \
+                w2.roofline(r2, pk, c2.report().get("sm_mhz"))
+            cr = c2.report()
+            ent = {"workload": name, "value": round(v2, 3), "unit": u2, "steps": r2["steps"],
+                   "ms_per_step": round(r2["ms"] / r2["steps"], 6),
+                   "roofline": short_roofline(rf), "gpu_launches": r2["launches"],
+                   "clocks": {"sm_mhz": cr.get("sm_mhz"), "reasons": cr.get("reasons")}}
             sb.check()
             del w2
             torch.cuda.empty_cache()
+            if not args.no_cpu_baseline:
+                w3 = WORKLOADS[name]()
+                if hasattr(w3, "cpu_sample"):
+                    cv, cu, csample = w3.cpu_sample(args.secondary_cpu_seconds)
+                    ent["cpu_baseline"] = {"value": round(cv, 6), "unit": cu, "cores": 1,
+                                           "sample": csample}
+            sec.append(ent)
         line["secondary"] = sec
     return line if rank == 0 else None
 
@@ -994,7 +1173,7 @@ def run_ours(args, world, rank):
 def run_reference(args, world, rank):
     if rank != 0:
         return None
-    wl = WORKLOADS[args.workload]()
+    wl = WORKLOADS[args.workload](ref=True)
     if not hasattr(wl, "cpu_sample"):
         return {"impl": "reference", "unavailable": "the CPU oracle arm is defined for the "
                 "decode workloads only"}
@@ -1011,8 +1190,7 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded counter-based generator)", "config": wl.config(),
-        "cpu_baseline": {"value": round(val, 5), "unit": unit, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": cpu_baseline_record(val, unit, sample),
         "e2e": {"value": round(val, 5), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -1028,6 +1206,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--secondary-cpu-seconds", type=float, default=2.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

@@ -103,12 +103,14 @@ enum {
 /* A packed weight matrix W[n][k] with its FP16 group scales. */
 typedef struct {
   int32_t format;          /* BONSAI_FMT_BINARY or BONSAI_FMT_TERNARY        */
-  int32_t flags;           /* BONSAI_WEIGHTS_* bits, 0 if none               */
   int64_t n;               /* output features (rows of W)                    */
   int64_t k;               /* input features, multiple of 128                */
   int64_t row_bytes;       /* bytes per packed row (see layout above)        */
   const void* packed;      /* device, n * row_bytes bytes                    */
   const uint16_t* scales;  /* device, FP16 bits [n][k/128]                   */
+  int32_t flags;           /* BONSAI_WEIGHTS_* bits, 0 if none. Last, so a
+                              caller that fills only the six fields above
+                              (zero-initialised struct) gets flags = 0      */
 } bonsai_weights;
 
 /* Canonical packed row size: BINARY k/8; TERNARY 64*ceil(ceil(k/5)/64).
@@ -179,7 +181,10 @@ bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
  * later calls. Calls share the scratch: two calls that overlap in time
  * (different streams, or different host threads on one device) corrupt each
  * other's sums, so order them on one stream or synchronise between them.
- * Results of two ordered calls with the same inputs are bit-identical. */
+ * Results of two ordered calls with the same inputs are bit-identical.
+ * Unlike the other compute calls, this one uses neither programmatic
+ * dependent launch nor BONSAI_WEIGHTS_PREFETCH: its kernel is an ordinary
+ * launch that starts after the previous work on the stream has finished. */
 bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t* x,
                                         uint16_t* y, bonsai_stream stream);
 

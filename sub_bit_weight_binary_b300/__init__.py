@@ -46,9 +46,9 @@ class BonsaiError(RuntimeError):
 
 
 class bonsai_weights_t(C.Structure):
-    _fields_ = [("format", C.c_int32), ("flags", C.c_int32), ("n", C.c_int64),
-                ("k", C.c_int64), ("row_bytes", C.c_int64), ("packed", C.c_void_p),
-                ("scales", C.c_void_p)]
+    _fields_ = [("format", C.c_int32), ("n", C.c_int64), ("k", C.c_int64),
+                ("row_bytes", C.c_int64), ("packed", C.c_void_p), ("scales", C.c_void_p),
+                ("flags", C.c_int32)]
 
 
 _lib = None
@@ -148,9 +148,9 @@ class Weights:
         if cs is None:
             import torch
             cs = bonsai_weights_t(
-                self.format, self.flags, self.n, self.k, self.row_bytes,
+                self.format, self.n, self.k, self.row_bytes,
                 _ptr(self.packed, (torch.uint8, torch.int32, torch.int8), "packed"),
-                _ptr(self.scales, (torch.float16, torch.int16), "scales"))
+                _ptr(self.scales, (torch.float16, torch.int16), "scales"), self.flags)
             self.__dict__["_cs"] = cs
         return cs
 

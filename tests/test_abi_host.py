@@ -44,6 +44,32 @@ def test_every_declared_symbol_is_exported(libs, header, lib):
         assert hasattr(L, name), "%s does not export %s" % (lib, name)
 
 
+def test_weights_struct_layout_matches_the_header(tmp_path):
+    """The binding's ctypes struct has the field offsets and size that a C
+    compiler gives bonsai_weights from include/bonsai.h (flags last)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in sb.bonsai_weights_t._fields_]
+    assert fields == ["format", "n", "k", "row_bytes", "packed", "scales", "flags"]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"bonsai.h\"\n"
+                   "int main(void) { printf(\"%zu" + " %zu" * len(fields) + "\\n\", "
+                   "sizeof(bonsai_weights)" +
+                   "".join(", offsetof(bonsai_weights, %s)" % f for f in fields) +
+                   "); return 0; }\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [C.sizeof(sb.bonsai_weights_t)] + [getattr(sb.bonsai_weights_t, f).offset
+                                              for f in fields]
+    assert got == want
+
+
 def test_built_for_sm103a():
     # the objects carry sm_103a code (cuobjdump is not used: only the
     # compiler's own record of the target in the build flags is checked)
@@ -65,7 +91,7 @@ def test_row_bytes_and_status_strings(libs, oracle_lib):
 def W(fmt=1, n=16, k=256, row_bytes=None, packed=0x10000, scales=0x20000, flags=0):
     if row_bytes is None:
         row_bytes = sb.bonsai_packed_row_bytes(fmt, k)
-    return sb.bonsai_weights_t(fmt, flags, n, k, row_bytes, packed, scales)
+    return sb.bonsai_weights_t(fmt, n, k, row_bytes, packed, scales, flags)
 
 
 # Each case fails a host check, so nothing is launched and no pointer is read.

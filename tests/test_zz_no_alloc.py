@@ -49,6 +49,26 @@ def test_no_alloc_matches_gemv(fmt, n, k):
     assert np.all(np.abs(a - b) <= 2 * TOL * nrm[0] + 1e-30)
 
 
+def test_no_alloc_leaves_device_memory_untouched():
+    """After a first call (the one-time set-up), a batch of calls changes the
+    device's free memory by nothing: no allocation, by the library or by
+    anything it calls."""
+    t = torch()
+    n, k = 640, 5120
+    w, _, _ = weights(TER, 91, n, k)
+    xd = dev(synth.gen_x(92, 1, k)[0])
+    y = t.empty(n, dtype=t.float16, device="cuda")
+    sb.bonsai_gemv_splitk_static(w, xd, y)
+    t.cuda.synchronize()
+    free0, _ = t.cuda.mem_get_info()
+    for _ in range(50):
+        sb.bonsai_gemv_splitk_static(w, xd, y)
+    t.cuda.synchronize()
+    free1, _ = t.cuda.mem_get_info()
+    assert sb.bonsai_check_async() == 0
+    assert free1 == free0
+
+
 def test_no_alloc_rejects_more_rows_than_its_scratch():
     t = torch()
     n, k = 8193, 128
