@@ -82,6 +82,7 @@ struct Params {
   int sc_pitch;     // smem bytes per row of streamed scales = TMA box width
   int stage_bytes;  // 16 rows x pitch + 16 rows x sc_pitch, rounded to 128
   int stages;       // ring depth
+  int red_cols;     // token columns held per row in the partial-sum slots (m)
   int off_bar, off_red, off_t, off_lut, off_xt, off_stage;
 };
 
@@ -117,7 +118,7 @@ __device__ __forceinline__ float* partial_slot(const Params& p, uint8_t* smem, u
     set_status(BONSAI_ERR_TIMEOUT);
     alive = false;
   }
-  return reinterpret_cast<float*>(smem + p.off_red) + slot * (W * 16 * 8);
+  return reinterpret_cast<float*>(smem + p.off_red) + slot * (W * 16 * p.red_cols);
 }
 
 __device__ __forceinline__ void partial_done(uint32_t red_full, int tcount, int lane) {
@@ -135,7 +136,9 @@ __device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int l
       set_status(BONSAI_ERR_TIMEOUT);
       return;
     }
-    const float* red = reinterpret_cast<const float*>(smem + p.off_red) + slot * (W * 16 * 8);
+    const float* red =
+        reinterpret_cast<const float*>(smem + p.off_red) + slot * (W * 16 * p.red_cols);
+    const int rc = p.red_cols;
     const int row0 = tile * p.rows;
     if (p.swiglu) {
       // 8 gate rows then the 8 up rows of the same features (n % 16 == 0)
@@ -144,8 +147,8 @@ __device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int l
         float g = 0.f, u = 0.f;
 #pragma unroll
         for (int w = 0; w < W; ++w) {
-          g += red[(w * 16 + r) * 8 + col];
-          u += red[(w * 16 + r + 8) * 8 + col];
+          g += red[(w * 16 + r) * rc + col];
+          u += red[(w * 16 + r + 8) * rc + col];
         }
         p.y[(size_t)col * p.y_stride + tile * 8 + r] = __float2half_rn(silu(g) * u);
       }
@@ -155,7 +158,7 @@ __device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int l
         if (row < p.rows && row0 + row < p.n) {
           float sum = 0.f;
 #pragma unroll
-          for (int w = 0; w < W; ++w) sum += red[(w * 16 + row) * 8 + col];
+          for (int w = 0; w < W; ++w) sum += red[(w * 16 + row) * rc + col];
           p.y[(size_t)col * p.y_stride + row0 + row] = __float2half_rn(sum);
         }
       }
@@ -398,10 +401,15 @@ __global__ void __launch_bounds__(threads_for(kBinWarps), 1)
       if (++s == p.stages) { s = 0; ph ^= 1; }
     }
     float* red = partial_slot<kBinWarps>(p, smem, red_full, tcount, alive);
-    red[(warp * 16 + g) * 8 + 2 * q] = yacc[0];
-    red[(warp * 16 + g) * 8 + 2 * q + 1] = yacc[1];
-    red[(warp * 16 + g + 8) * 8 + 2 * q] = yacc[2];
-    red[(warp * 16 + g + 8) * 8 + 2 * q + 1] = yacc[3];
+    const int rc = p.red_cols;  // token columns 2q, 2q+1; only real tokens are kept
+    if (2 * q < rc) {
+      red[(warp * 16 + g) * rc + 2 * q] = yacc[0];
+      red[(warp * 16 + g + 8) * rc + 2 * q] = yacc[2];
+    }
+    if (2 * q + 1 < rc) {
+      red[(warp * 16 + g) * rc + 2 * q + 1] = yacc[1];
+      red[(warp * 16 + g + 8) * rc + 2 * q + 1] = yacc[3];
+    }
     partial_done(red_full, tcount, lane);
   }
 }
@@ -646,8 +654,154 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
       if (++s == p.stages) { s = 0; ph ^= 1; }
     }
     float* red = partial_slot<kTerWarps>(p, smem, red_full, tcount, alive);
-    red[(warp * 16 + g) * 8 + q] = yacc[0];
-    red[(warp * 16 + g + 8) * 8 + q] = yacc[1];
+    if (q < p.red_cols) {  // token column q; only real tokens are kept
+      red[(warp * 16 + g) * p.red_cols + q] = yacc[0];
+      red[(warp * 16 + g + 8) * p.red_cols + q] = yacc[1];
+    }
+    partial_done(red_full, tcount, lane);
+  }
+}
+
+// ===========================================================================
+// binary, one token: subset-sum tables
+// ===========================================================================
+// For one token the products x . w of four consecutive codes take only 16
+// values, sum_{i<4} (2 b_i - 1) x_i over the 16 bit patterns b of a nibble
+// ("multiplication degenerates to addition and sign flip", 三值权重 page).
+// The CTA tabulates them once per launch from x (FP32), and each nibble of a
+// packed word then costs one table load and one add: no MMA and no operand
+// construction. Lanes are rows: lane (r, h) of a warp takes row r of the
+// 16-row tile and words 2h, 2h+1 of each 128-code group it handles, so at
+// every step the 32 lanes read two 16-word tables (one per half-warp) and
+// never conflict on a bank.
+//
+// Table layout, group g, position pos = 16 hp + j of the group (word
+// pos >> 3, nibble pos & 7): entry e at byte
+//   (g >> 1) * 4096 + j * 256 + (g & 1) * 128 + hp * 64 + 4 e.
+// Half hp lands in banks 16 hp .. 16 hp + 15. The part below 256 of that
+// offset, 4 e | 64 hp | 128 (g & 1), is the low byte of the address; it is
+// built in the nibble extraction (one LOP3 per four nibbles), and one PRMT
+// merges it with the 256-aligned group base; j * 256 is the load's
+// immediate offset.
+constexpr int kLutGroupBytes = 2048;   // table bytes per 128-code group
+constexpr int kLutMaxGroups = 64;      // K <= 8192: at most 128 KB of tables
+
+// Entries of the (group, position) pairs of x, one pair per thread.
+template <int W>
+__device__ void build_nibble_tables(const Params& p, uint32_t tab) {
+  const int positions = p.k / 4;
+  for (int t = threadIdx.x; t < positions; t += W * 32) {
+    const uint2 xv = *reinterpret_cast<const uint2*>(p.x + 4 * t);
+    const float x0 = __half2float(__ushort_as_half(uint16_t(xv.x & 0xFFFFu)));
+    const float x1 = __half2float(__ushort_as_half(uint16_t(xv.x >> 16)));
+    const float x2 = __half2float(__ushort_as_half(uint16_t(xv.y & 0xFFFFu)));
+    const float x3 = __half2float(__ushort_as_half(uint16_t(xv.y >> 16)));
+    // codes 0,1 and codes 2,3: index bit i set = code i is +1
+    const float lo[4] = {-x0 - x1, x0 - x1, x1 - x0, x0 + x1};
+    const float hi[4] = {-x2 - x3, x2 - x3, x3 - x2, x2 + x3};
+    const int g = t >> 5, pos = t & 31;
+    const uint32_t dst = tab + (g >> 1) * 4096 + (pos & 15) * 256 + (g & 1) * 128 + (pos >> 4) * 64;
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(dst + 16 * b),
+                   "f"(lo[0] + hi[b]), "f"(lo[1] + hi[b]), "f"(lo[2] + hi[b]), "f"(lo[3] + hi[b])
+                   : "memory");
+  }
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// The 8 nibbles of word w as table loads: t1 holds nibbles 0,2,4,6 and t2
+// nibbles 1,3,5,7, each as 4 e | low address bits `lowbits`; J0 is the
+// word's first position j (0 or 8).
+template <int J0>
+__device__ __forceinline__ void lut_word(uint32_t w, uint32_t lowbits, uint32_t base,
+                                         float& a0, float& a1) {
+  uint32_t t1, t2;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t1) : "r"(w << 2), "r"(0x3C3C3C3Cu), "r"(lowbits));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t2) : "r"(w >> 2), "r"(0x3C3C3C3Cu), "r"(lowbits));
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t ae = __byte_perm(t1, base, 0x7650 | b);   // nibble 2b
+    const uint32_t ao = __byte_perm(t2, base, 0x7650 | b);   // nibble 2b + 1
+    a0 += lds_f32(ae + (J0 + 2 * b) * 256);
+    a1 += lds_f32(ao + (J0 + 2 * b + 1) * 256);
+  }
+}
+
+template <bool SC>
+__global__ void __launch_bounds__(threads_for(kBinWarps), 1)
+    gemv_binary_lut_kernel(const __grid_constant__ CUtensorMap tmw,
+                           const __grid_constant__ CUtensorMap tms,
+                           const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t red_full = bar_full + 16 * kMaxStages;
+  const uint32_t tab = sbase + p.off_lut;
+  if (tab & 255u) {  // the PRMT address merge needs 256-byte aligned group bases
+    if (threadIdx.x == 0) set_status(BONSAI_ERR_UNSUPPORTED);
+    return;
+  }
+  init_barriers<kBinWarps>(bar_full, bar_empty, p.stages);
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == kBinWarps) {
+    if (lane == 0) produce(&tmw, &tms, p, sbase, bar_full, bar_empty);
+    return;
+  }
+  if (warp == kBinWarps + 1) {
+    reducer<kBinWarps>(p, smem, red_full, lane);
+    return;
+  }
+  pdl_wait();  // x is written by earlier work on the stream
+  build_nibble_tables<kBinWarps>(p, tab);
+  named_bar_sync(1, kBinWarps * 32);
+
+  const int r = lane & 15, h = lane >> 4;
+  const int pw = p.pitch >> 2;
+  const uint32_t hbits = h ? 0x40404040u : 0u;
+  int s = 0;
+  uint32_t ph = 0;
+  bool alive = true;
+  int tcount = 0;
+  for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tcount) {
+    const int row0 = tile * 16;
+    float yacc = 0.f;
+    for (int c = 0; c < p.chunks; ++c) {
+      const int len = min(kChunk, p.data_bytes - c * kChunk);
+      const int cg = len >> 4;  // 128-code groups in this chunk
+      const uint8_t* stage = smem + p.off_stage + s * p.stage_bytes;
+      const uint32_t* stg = reinterpret_cast<const uint32_t*>(stage);
+      if (wait_full(bar_full + 8 * s, ph, alive)) {
+        // groups gl = gs, gs + kBinWarps, ...; gs alternates between the two
+        // halves of the warp range from tile to tile
+        const int gs = (warp + (kBinWarps / 2) * (tcount & 1)) % kBinWarps;
+        for (int gl = gs; gl < cg; gl += kBinWarps) {
+          const int gi = c * (kChunk / 16) + gl;
+          const uint4 wv = *reinterpret_cast<const uint4*>(stg + r * pw + gl * 4);
+          const uint32_t w0 = h ? wv.z : wv.x, w1 = h ? wv.w : wv.y;
+          const uint32_t lowbits = hbits | ((gi & 1) ? 0x80808080u : 0u);
+          const uint32_t base = tab + (gi >> 1) * 4096;
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          lut_word<0>(w0, lowbits, base, a0, a1);
+          lut_word<8>(w1, lowbits, base, a2, a3);
+          const float sc = scale_of<SC>(p, stage, r, row0 + r, gl, gi);
+          yacc = fmaf(sc, (a0 + a1) + (a2 + a3), yacc);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+      if (++s == p.stages) { s = 0; ph ^= 1; }
+    }
+    yacc += __shfl_xor_sync(0xFFFFFFFFu, yacc, 16);  // words 0,1 + words 2,3
+    float* red = partial_slot<kBinWarps>(p, smem, red_full, tcount, alive);
+    if (h == 0) red[(warp * 16 + r) * p.red_cols] = yacc;
     partial_done(red_full, tcount, lane);
   }
 }
@@ -697,15 +851,21 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
   }
   p.tiles = (n + p.rows - 1) / p.rows;
   p.stage_bytes = (16 * p.pitch + 16 * p.sc_pitch + 127) / 128 * 128;
+  // one binary token with K <= 8192: the subset-sum kernel
+  const bool lut = !ter && m == 1 && p.G <= kLutMaxGroups;
 
   auto up = [](int v, int a) { return (v + a - 1) / a * a; };
   int off = 0;
-  p.off_lut = off;   if (ter) off = up(off + kLutBytes, 128);  // at 0: the kernel relies on it
+  p.off_lut = off;   // at 0: the kernels rely on it (1024-byte aligned)
+  if (ter) off = up(off + kLutBytes, 128);
+  else if (lut) off = up(off + ((p.G + 1) / 2) * 2 * kLutGroupBytes, 128);
   p.off_bar = off;   off = up(off + 8 * (2 * kMaxStages + 4), 128);
   const int warps = ter ? kTerWarps : kBinWarps;
-  p.off_red = off;   off = up(off + 2 * warps * 16 * 8 * 4, 128);
-  p.off_t = off;     if (!ter) off = up(off + p.G * 8 * 4, 128);
-  p.off_xt = off;    off = up(off + p.m * p.xt_stride, 1024);
+  p.red_cols = m;
+  p.off_red = off;   off = up(off + 2 * warps * 16 * p.red_cols * 4, 128);
+  p.off_t = off;     if (!ter && !lut) off = up(off + p.G * 8 * 4, 128);
+  p.off_xt = off;    if (!lut) off = up(off + p.m * p.xt_stride, 1024);
+  off = up(off, 1024);
   p.off_stage = off;
   {
     const int room = (device_max_smem_optin() - off) / p.stage_bytes;
@@ -732,6 +892,8 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
 
   const void* fn = ter ? (p.sc_tma ? (const void*)gemv_ternary_kernel<true>
                                    : (const void*)gemv_ternary_kernel<false>)
+                 : lut ? (p.sc_tma ? (const void*)gemv_binary_lut_kernel<true>
+                                   : (const void*)gemv_binary_lut_kernel<false>)
                        : (p.sc_tma ? (const void*)gemv_binary_kernel<true>
                                    : (const void*)gemv_binary_kernel<false>);
   if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return BONSAI_ERR_CUDA;

@@ -97,6 +97,7 @@ GEMV_CASES = [
     (BIN, 1024, 1024),    # binary decode workload (M=1, K=N=1024)
     (BIN, 1, 128), (BIN, 17, 640), (BIN, 33, 5120), (BIN, 1000, 1024),
     (BIN, 16, 17408), (BIN, 5120, 5120), (BIN, 301, 9216),
+    (BIN, 7, 384), (BIN, 50, 8192), (BIN, 2000, 8320),  # subset-sum kernel: odd G, largest K; past it
     (TER, 17408, 5120),   # ternary decode workload (M=1, K=5120, N=17408)
     (TER, 1, 128), (TER, 17, 640), (TER, 33, 5120), (TER, 40, 17408),
     (TER, 5120, 17408), (TER, 300, 1280), (TER, 129, 384),
@@ -117,6 +118,27 @@ def test_gemv(fmt, n, k):
     assert sb.bonsai_check_async() == 0
     y_ref, nrm = oracle.linear(fmt, packed, scales, x)
     assert_close(host(y.t), y_ref[0], nrm[0], "gemv fmt=%d n=%d k=%d" % (fmt, n, k))
+    y.check()
+
+
+@pytest.mark.parametrize("fmt", [BIN, TER])
+def test_gemv_wide_range_activations(fmt):
+    """x spanning many binades (1e-4 .. 1e3, both signs) and exact zeros:
+    the one-token kernels (subset-sum tables in FP32 for binary) stay within
+    the bound of every output."""
+    t = torch()
+    n, k = 333, 5120
+    w, packed, scales = weights(fmt, 12, n, k)
+    rng = np.random.default_rng(5)
+    mag = 10.0 ** rng.uniform(-4, 3, size=k)
+    xv = (mag * rng.choice([-1.0, 1.0], size=k)).astype(np.float16)
+    xv[rng.integers(0, k, size=k // 10)] = 0
+    x = xv.view(np.uint16)[None, :]
+    y = Guarded((n,), t.float16)
+    sb.bonsai_gemv(w, dev(x[0]), y.t)
+    assert sb.bonsai_check_async() == 0
+    y_ref, nrm = oracle.linear(fmt, packed, scales, x)
+    assert_close(host(y.t), y_ref[0], nrm[0], "wide-range x fmt=%d" % fmt)
     y.check()
 
 
