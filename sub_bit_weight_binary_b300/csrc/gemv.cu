@@ -59,6 +59,7 @@ constexpr int kMaxStages = 8;
 constexpr int kStageBudget = 96 * 1024;    // bytes in flight per CTA
 constexpr int kChunk = 1024;               // packed bytes per row per stage
 constexpr int kLutBytes = 256 * 256;       // ternary: 256 entries x (32 lanes x 4 B + pad)
+constexpr int kLutBytes8 = 256 * 128;      // the same, packed (5..8 tokens)
 constexpr int kTerEntry = 48;              // ternary x-table bytes per (round, side, lane)
 constexpr int kTerMaxTokens = 4;           // two B columns (group parities) per token
 
@@ -474,9 +475,13 @@ __device__ __forceinline__ void ter_range(Fetch& fetch, Round& round, Epi& epi) 
   epi(round_last_group(R0 + N - 1));
 }
 
-// Byte -> digits table, one copy per lane (entry e at e*256 + lane*4):
-// digit i at bits 2i..2i+1. Independent of x, so it is built before the
-// wait for the previous grid.
+// Byte -> digits table, one copy per lane: digit i at bits 2i..2i+1. Entry e
+// of lane l at e*ROW + l*4; ROW = 256 lets one PRMT build the address from
+// the byte (64 KB, half of each row unused), ROW = 128 packs it into 32 KB
+// (two instructions per address), for the many-token mode whose x tables
+// are large. Independent of x, so it is built before the wait for the
+// previous grid.
+template <int ROW>
 __device__ void build_byte_table(uint8_t* smem) {
   for (int e = threadIdx.x; e < 256; e += kTerWarps * 32) {
     uint32_t v = 0;
@@ -485,7 +490,7 @@ __device__ void build_byte_table(uint8_t* smem) {
 #pragma unroll
       for (int i = 0; i < 5; ++i) { v |= uint32_t(r % 3) << (2 * i); r /= 3; }
     }
-    uint4* dst = reinterpret_cast<uint4*>(smem + e * 256);
+    uint4* dst = reinterpret_cast<uint4*>(smem + e * ROW);
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v, v, v, v);
   }
@@ -530,7 +535,11 @@ __device__ void build_ternary_xtable(const Params& p, uint8_t* smem) {
   }
 }
 
-template <bool SC>
+// TOK8 = false: up to 4 tokens, B column 2t + side (the group-parity trick
+// above). TOK8 = true: 5..8 tokens, B column t; a round that straddles a
+// group edge issues its five MMAs once per side (x of the other side's
+// groups is zero in that B) into separate accumulators, the others once.
+template <bool SC, bool TOK8>
 __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
     gemv_ternary_kernel(const __grid_constant__ CUtensorMap tmw,
                         const __grid_constant__ CUtensorMap tms, const __grid_constant__ Params p) {
@@ -550,15 +559,17 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
     reducer<kTerWarps>(p, smem, red_full, lane);
     return;
   }
-  build_byte_table(smem);
+  build_byte_table<TOK8 ? 128 : 256>(smem);
   pdl_wait();  // x is written by earlier work on the stream
   build_ternary_xtable(p, smem);
   named_bar_sync(1, kTerWarps * 32);
 
   const int g = lane >> 2, q = lane & 3;
-  const bool bcol = (g >> 1) < p.m;  // B column g = token g>>1, side g&1
-  const uint8_t* xt_lane = smem + p.off_xt + (bcol ? (g >> 1) : 0) * p.xt_stride +
-                           ((g & 1) * 4 + q) * kTerEntry;
+  // B column g: token g>>1, side g&1 (up to 4 tokens), or token g (TOK8)
+  const bool bcol = (TOK8 ? g : (g >> 1)) < p.m;
+  const uint8_t* xt_lane =
+      TOK8 ? smem + p.off_xt + (bcol ? g : 0) * p.xt_stride + q * kTerEntry
+           : smem + p.off_xt + (bcol ? (g >> 1) : 0) * p.xt_stride + ((g & 1) * 4 + q) * kTerEntry;
   const uint32_t lut_lane = uint32_t(lane * 4);
   const uint8_t* lut = smem;  // the byte table sits at offset 0
   const int pw = p.pitch >> 2;
@@ -571,7 +582,8 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
   int tcount = 0;
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tcount) {
     const int row0 = tile * 16;
-    float yacc[2] = {0.f, 0.f};  // token q, rows g and g+8
+    // token q, rows g and g+8; TOK8: rows g, g+8 x tokens 2q, 2q+1
+    float yacc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int c = 0; c < p.chunks; ++c) {
       const int len = min(kChunk, p.data_bytes - c * kChunk);
       const int nsg = (len + 127) >> 7;
@@ -582,8 +594,10 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
         const uint32_t* r0 = stg + g * pw + sgw * 32 + q;
         const uint32_t* r1 = stg + (g + 8) * pw + sgw * 32 + q;
         const uint8_t* xt = xt_lane + sg * (64 * kTerEntry);
-        // acc: (row g, token q, side 0 / 1), (row g+8, token q, side 0 / 1)
+        // acc: (row g, token q, side 0 / 1), (row g+8, token q, side 0 / 1);
+        // TOK8: accs[side] = (row g, tokens 2q, 2q+1), (row g+8, same)
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float accs[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         // the part of group grp held in this warp -> yacc; clears its side
         auto epi = [&](int grp) {
           const int side = grp & 1;
@@ -591,16 +605,25 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
           const int gi = 5 * sg + grp;
           const float sa = scale_of<SC>(p, stage, g, row0 + g, gl, gi);
           const float sb = scale_of<SC>(p, stage, g + 8, row0 + g + 8, gl, gi);
-          const float va = side ? acc[1] : acc[0];
-          const float vb = side ? acc[3] : acc[2];
-          yacc[0] = fmaf(sa, va * 1024.f, yacc[0]);
-          yacc[1] = fmaf(sb, vb * 1024.f, yacc[1]);
-          if (side) {
-            acc[1] = 0.f;
-            acc[3] = 0.f;
+          if constexpr (TOK8) {
+            float(&a)[4] = accs[side];
+            yacc[0] = fmaf(sa, a[0] * 1024.f, yacc[0]);
+            yacc[1] = fmaf(sa, a[1] * 1024.f, yacc[1]);
+            yacc[2] = fmaf(sb, a[2] * 1024.f, yacc[2]);
+            yacc[3] = fmaf(sb, a[3] * 1024.f, yacc[3]);
+            a[0] = a[1] = a[2] = a[3] = 0.f;
           } else {
-            acc[0] = 0.f;
-            acc[2] = 0.f;
+            const float va = side ? acc[1] : acc[0];
+            const float vb = side ? acc[3] : acc[2];
+            yacc[0] = fmaf(sa, va * 1024.f, yacc[0]);
+            yacc[1] = fmaf(sb, vb * 1024.f, yacc[1]);
+            if (side) {
+              acc[1] = 0.f;
+              acc[3] = 0.f;
+            } else {
+              acc[0] = 0.f;
+              acc[2] = 0.f;
+            }
           }
         };
         // word loads and byte-table lookups of a round (digits of bytes (0,1)
@@ -608,7 +631,11 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
         auto fetch = [&](int rnd, TerDigits& f) {
           const uint32_t wa = r0[4 * rnd], wb = r1[4 * rnd];
           auto lookup = [&](uint32_t wd, int i) -> uint32_t {
-            const uint32_t off = __byte_perm(wd, lut_lane, 0x5504 | (i << 4));
+            uint32_t off;
+            if constexpr (TOK8)  // byte * 128 + lane * 4
+              off = ((i == 0 ? (wd << 7) : (wd >> (8 * i - 7))) & 0x7F80u) | lut_lane;
+            else  // byte * 256 + lane * 4
+              off = __byte_perm(wd, lut_lane, 0x5504 | (i << 4));
             return *reinterpret_cast<const uint32_t*>(lut + off);
           };
           f.a01 = __byte_perm(lookup(wa, 0), lookup(wa, 1), 0x5410);
@@ -617,24 +644,48 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
           f.b23 = __byte_perm(lookup(wb, 2), lookup(wb, 3), 0x5410);
         };
         // the round's five digit MMAs
-        auto round = [&](int rnd, const TerDigits& f) {
-          // only lanes of real tokens load x; the other columns are not stored
-          const uint4* bp = reinterpret_cast<const uint4*>(xt + rnd * (8 * kTerEntry));
-          if (bcol) {
-            b0 = bp[0];
-            b1 = bp[1];
-            b2 = bp[2];
-          }
-#define TER_MMA(MD, BX, BY)                                                    \
-  mma_16816(acc, ter_operand<MD>(f.a01, E), ter_operand<MD>(f.b01, E),         \
+#define TER_MMA(D, MD, BX, BY)                                                  \
+  mma_16816(D, ter_operand<MD>(f.a01, E), ter_operand<MD>(f.b01, E),            \
             ter_operand<MD>(f.a23, E), ter_operand<MD>(f.b23, E), BX, BY)
-          TER_MMA(0, b0.x, b0.y);
-          TER_MMA(1, b0.z, b0.w);
-          TER_MMA(2, b1.x, b1.y);
-          TER_MMA(3, b1.z, b1.w);
-          TER_MMA(4, b2.x, b2.y);
-#undef TER_MMA
+        auto round = [&](int rnd, const TerDigits& f) {
+          if constexpr (TOK8) {
+            // one pass per side that holds codes of this round
+            for (int side = 0; side < 2; ++side) {
+              const bool used = side == (round_first_group(rnd) & 1) ||
+                                side == (round_last_group(rnd) & 1);
+              if (!used) continue;
+              const uint4* bp =
+                  reinterpret_cast<const uint4*>(xt + (rnd * 8 + side * 4) * kTerEntry);
+              if (bcol) {
+                b0 = bp[0];
+                b1 = bp[1];
+                b2 = bp[2];
+              } else {
+                b0 = b1 = b2 = make_uint4(0, 0, 0, 0);
+              }
+              float(&a)[4] = accs[side];
+              TER_MMA(a, 0, b0.x, b0.y);
+              TER_MMA(a, 1, b0.z, b0.w);
+              TER_MMA(a, 2, b1.x, b1.y);
+              TER_MMA(a, 3, b1.z, b1.w);
+              TER_MMA(a, 4, b2.x, b2.y);
+            }
+          } else {
+            // only lanes of real tokens load x; the other columns are not stored
+            const uint4* bp = reinterpret_cast<const uint4*>(xt + rnd * (8 * kTerEntry));
+            if (bcol) {
+              b0 = bp[0];
+              b1 = bp[1];
+              b2 = bp[2];
+            }
+            TER_MMA(acc, 0, b0.x, b0.y);
+            TER_MMA(acc, 1, b0.z, b0.w);
+            TER_MMA(acc, 2, b1.x, b1.y);
+            TER_MMA(acc, 3, b1.z, b1.w);
+            TER_MMA(acc, 4, b2.x, b2.y);
+          }
         };
+#undef TER_MMA
         // this warp's rounds of the super-group; a group is flushed after its
         // last round in the range
         if constexpr (kTerParts == 2) {
@@ -654,9 +705,19 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
       if (++s == p.stages) { s = 0; ph ^= 1; }
     }
     float* red = partial_slot<kTerWarps>(p, smem, red_full, tcount, alive);
-    if (q < p.red_cols) {  // token column q; only real tokens are kept
-      red[(warp * 16 + g) * p.red_cols + q] = yacc[0];
-      red[(warp * 16 + g + 8) * p.red_cols + q] = yacc[1];
+    const int rc = p.red_cols;  // only real tokens are kept
+    if constexpr (TOK8) {  // token columns 2q, 2q+1
+      if (2 * q < rc) {
+        red[(warp * 16 + g) * rc + 2 * q] = yacc[0];
+        red[(warp * 16 + g + 8) * rc + 2 * q] = yacc[2];
+      }
+      if (2 * q + 1 < rc) {
+        red[(warp * 16 + g) * rc + 2 * q + 1] = yacc[1];
+        red[(warp * 16 + g + 8) * rc + 2 * q + 1] = yacc[3];
+      }
+    } else if (q < rc) {  // token column q
+      red[(warp * 16 + g) * rc + q] = yacc[0];
+      red[(warp * 16 + g + 8) * rc + q] = yacc[1];
     }
     partial_done(red_full, tcount, lane);
   }
@@ -686,26 +747,43 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
 constexpr int kLutGroupBytes = 2048;   // table bytes per 128-code group
 constexpr int kLutMaxGroups = 64;      // K <= 8192: at most 128 KB of tables
 
-// Entries of the (group, position) pairs of x, one pair per thread.
-template <int W>
-__device__ void build_nibble_tables(const Params& p, uint32_t tab) {
-  const int positions = p.k / 4;
-  for (int t = threadIdx.x; t < positions; t += W * 32) {
-    const uint2 xv = *reinterpret_cast<const uint2*>(p.x + 4 * t);
-    const float x0 = __half2float(__ushort_as_half(uint16_t(xv.x & 0xFFFFu)));
-    const float x1 = __half2float(__ushort_as_half(uint16_t(xv.x >> 16)));
-    const float x2 = __half2float(__ushort_as_half(uint16_t(xv.y & 0xFFFFu)));
-    const float x3 = __half2float(__ushort_as_half(uint16_t(xv.y >> 16)));
-    // codes 0,1 and codes 2,3: index bit i set = code i is +1
-    const float lo[4] = {-x0 - x1, x0 - x1, x1 - x0, x0 + x1};
-    const float hi[4] = {-x2 - x3, x2 - x3, x3 - x2, x2 + x3};
-    const int g = t >> 5, pos = t & 31;
-    const uint32_t dst = tab + (g >> 1) * 4096 + (pos & 15) * 256 + (g & 1) * 128 + (pos >> 4) * 64;
+// Entries of the (group, position) pairs of x. A thread takes two adjacent
+// positions (one 16-byte load of x) per pass; all of its loads are issued
+// before the first entry is computed, so the build waits on memory once.
+constexpr int kLutBuildPasses = (kLutMaxGroups * 16 + kBinWarps * 32 - 1) / (kBinWarps * 32);
+
+__device__ __forceinline__ void nibble_entries(uint32_t xw0, uint32_t xw1, uint32_t tab, int t) {
+  const float x0 = __half2float(__ushort_as_half(uint16_t(xw0 & 0xFFFFu)));
+  const float x1 = __half2float(__ushort_as_half(uint16_t(xw0 >> 16)));
+  const float x2 = __half2float(__ushort_as_half(uint16_t(xw1 & 0xFFFFu)));
+  const float x3 = __half2float(__ushort_as_half(uint16_t(xw1 >> 16)));
+  // codes 0,1 and codes 2,3: index bit i set = code i is +1
+  const float lo[4] = {-x0 - x1, x0 - x1, x1 - x0, x0 + x1};
+  const float hi[4] = {-x2 - x3, x2 - x3, x3 - x2, x2 + x3};
+  const int g = t >> 5, pos = t & 31;
+  const uint32_t dst = tab + (g >> 1) * 4096 + (pos & 15) * 256 + (g & 1) * 128 + (pos >> 4) * 64;
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
-      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(dst + 16 * b),
-                   "f"(lo[0] + hi[b]), "f"(lo[1] + hi[b]), "f"(lo[2] + hi[b]), "f"(lo[3] + hi[b])
-                   : "memory");
+  for (int b = 0; b < 4; ++b)
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(dst + 16 * b),
+                 "f"(lo[0] + hi[b]), "f"(lo[1] + hi[b]), "f"(lo[2] + hi[b]), "f"(lo[3] + hi[b])
+                 : "memory");
+}
+
+__device__ void build_nibble_tables(const Params& p, uint32_t tab) {
+  const int pairs = p.k / 8;  // two positions (8 codes) per 16-byte load
+  uint4 xv[kLutBuildPasses];
+#pragma unroll
+  for (int it = 0; it < kLutBuildPasses; ++it) {
+    const int t = threadIdx.x + it * kBinWarps * 32;
+    xv[it] = t < pairs ? reinterpret_cast<const uint4*>(p.x)[t] : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int it = 0; it < kLutBuildPasses; ++it) {
+    const int t = threadIdx.x + it * kBinWarps * 32;
+    if (t < pairs) {
+      nibble_entries(xv[it].x, xv[it].y, tab, 2 * t);
+      nibble_entries(xv[it].z, xv[it].w, tab, 2 * t + 1);
+    }
   }
 }
 
@@ -760,7 +838,7 @@ __global__ void __launch_bounds__(threads_for(kBinWarps), 1)
     return;
   }
   pdl_wait();  // x is written by earlier work on the stream
-  build_nibble_tables<kBinWarps>(p, tab);
+  build_nibble_tables(p, tab);
   named_bar_sync(1, kBinWarps * 32);
 
   const int r = lane & 15, h = lane >> 4;
@@ -857,7 +935,7 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
   auto up = [](int v, int a) { return (v + a - 1) / a * a; };
   int off = 0;
   p.off_lut = off;   // at 0: the kernels rely on it (1024-byte aligned)
-  if (ter) off = up(off + kLutBytes, 128);
+  if (ter) off = up(off + (m > kTerMaxTokens ? kLutBytes8 : kLutBytes), 128);
   else if (lut) off = up(off + ((p.G + 1) / 2) * 2 * kLutGroupBytes, 128);
   p.off_bar = off;   off = up(off + 8 * (2 * kMaxStages + 4), 128);
   const int warps = ter ? kTerWarps : kBinWarps;
@@ -890,8 +968,11 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
                             CU_TENSOR_MAP_SWIZZLE_NONE))
     return BONSAI_ERR_CUDA;
 
-  const void* fn = ter ? (p.sc_tma ? (const void*)gemv_ternary_kernel<true>
-                                   : (const void*)gemv_ternary_kernel<false>)
+  const bool tok8 = ter && m > kTerMaxTokens;
+  const void* fn = ter ? (tok8 ? (p.sc_tma ? (const void*)gemv_ternary_kernel<true, true>
+                                           : (const void*)gemv_ternary_kernel<false, true>)
+                               : (p.sc_tma ? (const void*)gemv_ternary_kernel<true, false>
+                                           : (const void*)gemv_ternary_kernel<false, false>))
                  : lut ? (p.sc_tma ? (const void*)gemv_binary_lut_kernel<true>
                                    : (const void*)gemv_binary_lut_kernel<false>)
                        : (p.sc_tma ? (const void*)gemv_binary_kernel<true>
@@ -913,12 +994,17 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
   return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
 }
 
-// Up to 8 tokens; ternary products of more than 4 tokens take two launches.
+// Up to 8 tokens in one launch; ternary products of more than 4 tokens whose
+// x tables do not fit beside the ring take two launches (4 + the rest).
 bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
                           bool swiglu, cudaStream_t stream) {
   if (m < 1 || m > 8) return BONSAI_ERR_UNSUPPORTED;
   if (w->format != BONSAI_FMT_TERNARY || m <= gemv::kTerMaxTokens)
     return gemv_launch_one(w, x, (int)m, y, swiglu, stream);
+  {
+    const bonsai_status st = gemv_launch_one(w, x, (int)m, y, swiglu, stream);
+    if (st != BONSAI_ERR_UNSUPPORTED) return st;
+  }
   const bonsai_status st = gemv_launch_one(w, x, gemv::kTerMaxTokens, y, swiglu, stream);
   if (st != BONSAI_OK) return st;
   const int64_t y_stride = swiglu ? w->n / 2 : w->n;

@@ -276,7 +276,10 @@ def test_one_nonzero_ternary_per_row():
 
 # ------------------------------------------------------------ GEMM, small m
 @pytest.mark.parametrize("fmt", [BIN, TER])
-@pytest.mark.parametrize("m,n,k", [(2, 300, 1024), (5, 1024, 5120), (8, 129, 640), (3, 64, 17408)])
+@pytest.mark.parametrize("m,n,k", [(2, 300, 1024), (5, 1024, 5120), (8, 129, 640), (3, 64, 17408),
+                                   # ternary 5..8 tokens in one launch (one B column per
+                                   # token), and a K whose x tables force two launches
+                                   (6, 400, 5120), (7, 33, 1280), (5, 50, 17408)])
 def test_gemm_few_tokens(fmt, m, n, k):
     t = torch()
     w, packed, scales = weights(fmt, 40 + m, n, k)
