@@ -483,16 +483,17 @@ __device__ __forceinline__ void ter_range(Fetch& fetch, Round& round, Epi& epi) 
 // previous grid.
 template <int ROW>
 __device__ void build_byte_table(uint8_t* smem) {
-  for (int e = threadIdx.x; e < 256; e += kTerWarps * 32) {
+  // one 16-byte piece (4 lanes' copies) per thread and store: 8 threads fill
+  // an entry's 128 bytes, so a warp's stores cover 4 entries bank-free
+  for (int t = threadIdx.x; t < 256 * 8; t += kTerWarps * 32) {
+    const int e = t >> 3, piece = t & 7;
     uint32_t v = 0;
     if (e < 243) {
       int r = e;
 #pragma unroll
       for (int i = 0; i < 5; ++i) { v |= uint32_t(r % 3) << (2 * i); r /= 3; }
     }
-    uint4* dst = reinterpret_cast<uint4*>(smem + e * ROW);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v, v, v, v);
+    reinterpret_cast<uint4*>(smem + e * ROW)[piece] = make_uint4(v, v, v, v);
   }
 }
 
@@ -747,42 +748,44 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
 constexpr int kLutGroupBytes = 2048;   // table bytes per 128-code group
 constexpr int kLutMaxGroups = 64;      // K <= 8192: at most 128 KB of tables
 
-// Entries of the (group, position) pairs of x. A thread takes two adjacent
-// positions (one 16-byte load of x) per pass; all of its loads are issued
-// before the first entry is computed, so the build waits on memory once.
-constexpr int kLutBuildPasses = (kLutMaxGroups * 16 + kBinWarps * 32 - 1) / (kBinWarps * 32);
-
-__device__ __forceinline__ void nibble_entries(uint32_t xw0, uint32_t xw1, uint32_t tab, int t) {
-  const float x0 = __half2float(__ushort_as_half(uint16_t(xw0 & 0xFFFFu)));
-  const float x1 = __half2float(__ushort_as_half(uint16_t(xw0 >> 16)));
-  const float x2 = __half2float(__ushort_as_half(uint16_t(xw1 & 0xFFFFu)));
-  const float x3 = __half2float(__ushort_as_half(uint16_t(xw1 >> 16)));
-  // codes 0,1 and codes 2,3: index bit i set = code i is +1
-  const float lo[4] = {-x0 - x1, x0 - x1, x1 - x0, x0 + x1};
-  const float hi[4] = {-x2 - x3, x2 - x3, x3 - x2, x2 + x3};
-  const int g = t >> 5, pos = t & 31;
-  const uint32_t dst = tab + (g >> 1) * 4096 + (pos & 15) * 256 + (g & 1) * 128 + (pos >> 4) * 64;
-#pragma unroll
-  for (int b = 0; b < 4; ++b)
-    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(dst + 16 * b),
-                 "f"(lo[0] + hi[b]), "f"(lo[1] + hi[b]), "f"(lo[2] + hi[b]), "f"(lo[3] + hi[b])
-                 : "memory");
-}
+// The tables are written one 16-byte piece (4 entries) per thread and store:
+// a table row (a group pair, position j) is 256 contiguous bytes, 16 pieces
+// (group parity, half hp, entry block b), so the 32 lanes of a warp store
+// two whole rows (512 contiguous bytes) and no two lanes of a wavefront share
+// a bank. A thread's x loads (the four activations of its position, 8 bytes)
+// are all issued before its first entry is computed, so the build waits on
+// memory once.
+constexpr int kLutBuildPasses = (kLutMaxGroups / 2 * 16 * 16 + kBinWarps * 32 - 1) / (kBinWarps * 32);
 
 __device__ void build_nibble_tables(const Params& p, uint32_t tab) {
-  const int pairs = p.k / 8;  // two positions (8 codes) per 16-byte load
-  uint4 xv[kLutBuildPasses];
+  const int rows = (p.G + 1) / 2 * 16;  // (group pair, position j)
+  const int passes = (rows * 16 + kBinWarps * 32 - 1) / (kBinWarps * 32);  // uniform
+  uint2 xv[kLutBuildPasses];
 #pragma unroll
   for (int it = 0; it < kLutBuildPasses; ++it) {
+    if (it >= passes) break;
     const int t = threadIdx.x + it * kBinWarps * 32;
-    xv[it] = t < pairs ? reinterpret_cast<const uint4*>(p.x)[t] : make_uint4(0, 0, 0, 0);
+    const int row = t >> 4, piece = t & 15;
+    const int g = 2 * (row >> 4) + (piece >> 3), pos = 16 * ((piece >> 2) & 1) + (row & 15);
+    xv[it] = (row < rows && g < p.G) ? *reinterpret_cast<const uint2*>(p.x + 128 * g + 4 * pos)
+                                     : make_uint2(0, 0);
   }
 #pragma unroll
   for (int it = 0; it < kLutBuildPasses; ++it) {
+    if (it >= passes) break;
     const int t = threadIdx.x + it * kBinWarps * 32;
-    if (t < pairs) {
-      nibble_entries(xv[it].x, xv[it].y, tab, 2 * t);
-      nibble_entries(xv[it].z, xv[it].w, tab, 2 * t + 1);
+    const int row = t >> 4, piece = t & 15, b = piece & 3;
+    if (row < rows) {
+      const float x0 = __half2float(__ushort_as_half(uint16_t(xv[it].x & 0xFFFFu)));
+      const float x1 = __half2float(__ushort_as_half(uint16_t(xv[it].x >> 16)));
+      const float x2 = __half2float(__ushort_as_half(uint16_t(xv[it].y & 0xFFFFu)));
+      const float x3 = __half2float(__ushort_as_half(uint16_t(xv[it].y >> 16)));
+      // entries 4b .. 4b+3: index bit i set = code i is +1; codes 2,3 fixed by b
+      const float hi = ((b & 1) ? x2 : -x2) + ((b & 2) ? x3 : -x3);
+      // piece offset within the row = (g & 1) * 128 + hp * 64 + b * 16 = piece * 16
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(tab + 256 * row + 16 * piece),
+                   "f"(-x0 - x1 + hi), "f"(x0 - x1 + hi), "f"(x1 - x0 + hi), "f"(x0 + x1 + hi)
+                   : "memory");
     }
   }
 }
