@@ -745,8 +745,8 @@ class GemmWorkload:
                     "ternary" if self.fmt == 2 else "binary"),
                 "achieved": round(a, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": round(a / pk["bf16"], 4),
-                "traffic": profiled_traffic("gemm_%s_m512_k5120_n17408.md" % (
-                    "ternary" if self.fmt == 2 else "binary")) if self.m == 512 else None,
+                "traffic": profiled_traffic("gemm_%s_m%d_k5120_n17408.md" % (
+                    "ternary" if self.fmt == 2 else "binary", self.m)),
                 "peak_src": "%s dense bf16 cuBLAS burst (fp16 has the same dense rate)" % pk["src"]}
 
     def config(self):
@@ -1083,11 +1083,9 @@ SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("ter_gemv_m5"
              ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("hadamard", 200, 10),
              ("xnor", 20, 3),
              ("xnor_fp16", 20, 3)]
-ROOFLINE_KEYS = ("bound", "achieved", "peak", "unit", "frac", "traffic")
-
-
-def short_roofline(rf):
-    return {k: rf.get(k) for k in ROOFLINE_KEYS}
+SECONDARY_FIELDS = ["workload", "value", "unit", "ms_per_step", "gpu_launches", "roofline_bound",
+                    "roofline_achieved", "roofline_peak", "roofline_frac", "roofline_traffic",
+                    "sm_mhz", "throttle_reasons", "cpu_baseline_value_1_core"]
 
 
 # -------------------------------------------------------------------- runs
@@ -1154,20 +1152,19 @@ def run_ours(args, world, rank):
             rf = w2.roofline(r2, pk) if w2.kind != "xnor" else \
                 w2.roofline(r2, pk, c2.report().get("sm_mhz"))
             cr = c2.report()
-            ent = {"workload": name, "value": round(v2, 3), "unit": u2, "steps": r2["steps"],
-                   "ms_per_step": round(r2["ms"] / r2["steps"], 6),
-                   "roofline": short_roofline(rf), "gpu_launches": r2["launches"],
-                   "clocks": {"sm_mhz": cr.get("sm_mhz"), "reasons": cr.get("reasons")}}
             sb.check()
             del w2
             torch.cuda.empty_cache()
+            cpu = None
             if not args.no_cpu_baseline:
                 w3 = WORKLOADS[name]()
                 if hasattr(w3, "cpu_sample"):
-                    cv, cu, csample = w3.cpu_sample(args.secondary_cpu_seconds)
-                    ent["cpu_baseline"] = {"value": round(cv, 6), "unit": cu, "cores": 1,
-                                           "sample": csample}
-            sec.append(ent)
+                    cpu = round(w3.cpu_sample(args.secondary_cpu_seconds)[0], 6)
+            sec.append([name, round(v2, 3), u2, round(r2["ms"] / r2["steps"], 6), r2["launches"],
+                        rf["bound"], rf["achieved"], rf["peak"], rf["frac"], rf["traffic"],
+                        cr.get("sm_mhz"), cr.get("reasons"), cpu])
+        # compact, and last in the line: one array per workload
+        line["secondary_fields"] = SECONDARY_FIELDS
         line["secondary"] = sec
     return line if rank == 0 else None
 
