@@ -570,8 +570,8 @@ class SweepWorkload:
     fixed x of its K."""
     kind = "sweep"
 
-    def __init__(self, fmt, name, layers=64, fused=False):
-        self.fmt, self.name, self.layers, self.fused = fmt, name, layers, fused
+    def __init__(self, fmt, name, layers=64, fused=False, plan=False):
+        self.fmt, self.name, self.layers, self.fused, self.plan = fmt, name, layers, fused, plan
 
     def unit_bytes(self):
         return self.layers * sum(weight_bytes(self.fmt, n, k) for n, k in SWEEP_SHAPES)
@@ -591,11 +591,30 @@ class SweepWorkload:
                   for k in (5120, 17408)}
         self.y = {n: torch.empty(n, dtype=torch.float16, device="cuda") for n, _ in SWEEP_SHAPES}
         self.h = torch.empty(SWEEP_SHAPES[2][0] // 2, dtype=torch.float16, device="cuda")
+        if self.plan:
+            # the token as one decode plan (one launch); with the fused
+            # feed-forward each layer has its own h (down reads it after the
+            # gate/up step), so layers do not overwrite each other's h
+            steps = []
+            self.hs = []
+            for i, w in enumerate(self.w):
+                j = i % len(SWEEP_SHAPES)
+                if self.fused and j == 2:
+                    self.hs.append(torch.empty(w.n // 2, dtype=torch.float16, device="cuda"))
+                    steps.append((w, self.x[w.k], self.hs[-1], 1, -1))
+                elif self.fused and j == 3:
+                    steps.append((w, self.hs[-1], self.y[w.n], 0, len(steps) - 1))
+                else:
+                    steps.append((w, self.x[w.k], self.y[w.n], 0, -1))
+            self.decode_plan = sb.DecodePlan(steps)
         torch.cuda.synchronize()
         sb.check()
 
     def token(self):
         import sub_bit_weight_binary_b300 as sb
+        if self.plan:
+            self.decode_plan.run()
+            return
         for i, w in enumerate(self.w):
             j = i % len(SWEEP_SHAPES)
             if self.fused and j == 2:
@@ -634,7 +653,7 @@ class SweepWorkload:
         if clocks:
             clocks.__exit__()
         ms = e0.elapsed_time(e1)
-        n = len(self.w)
+        n = 1 if self.plan else len(self.w)
         return {"ms": ms, "steps": steps, "launches": steps * n, "kernel_ms": ms / (steps * n)}
 
     def value(self, ms, steps):
@@ -642,8 +661,10 @@ class SweepWorkload:
 
     def roofline(self, r, pk):
         a = self.unit_bytes() / (r["ms"] / r["steps"] / 1e3) / 1e9
-        return {"bound": "hbm", "kernel": "gemv_%s_kernel (%d per token)" % (
-                    "ternary" if self.fmt == 2 else "binary", self.layers * len(SWEEP_SHAPES)),
+        return {"bound": "hbm", "kernel": ("gemv_ternary_plan_kernel (one per token, %d products)"
+                                           % (self.layers * len(SWEEP_SHAPES)) if self.plan else
+                                           "gemv_%s_kernel (%d per token)" % (
+                    "ternary" if self.fmt == 2 else "binary", self.layers * len(SWEEP_SHAPES))),
                 "achieved": round(a, 1),
                 "peak": pk["hbm"], "unit": "GB/s", "frac": round(a / pk["hbm"], 4),
                 "traffic": None, "peak_src": "%s HBM copy (burst)" % pk["src"],
@@ -655,8 +676,11 @@ class SweepWorkload:
                 "stacked": "q/k/v and gate/up weights stored stacked, one product each",
                 "ffn": ("gate/up product writes silu(g)*u; down product reads it" if self.fused
                         else "every product reads a fixed x"),
-                "timing": "one CUDA graph per token (%d launches), replayed per step" % (
-                    self.layers * len(SWEEP_SHAPES)),
+                "timing": ("one decode-plan launch per token (%d products), captured in a CUDA "
+                           "graph and replayed per step" % (self.layers * len(SWEEP_SHAPES))
+                           if self.plan else
+                           "one CUDA graph per token (%d launches), replayed per step" % (
+                               self.layers * len(SWEEP_SHAPES))),
                 "l2": "inputs larger than L2: %.2f GB of weights per token" % (self.unit_bytes() / 1e9)}
 
 
@@ -1059,6 +1083,8 @@ WORKLOADS = {
                                                     "(speculative verification)", ref),
     "sweep_bin": lambda ref=False: SweepWorkload(1, "64-layer decode sweep, binary, batch 1"),
     "sweep_ter": lambda ref=False: SweepWorkload(2, "64-layer decode sweep, ternary, batch 1"),
+    "sweep_ter_plan": lambda ref=False: SweepWorkload(
+        2, "64-layer decode sweep, ternary, batch 1 (one decode-plan launch per token)", plan=True),
     "gemm512_bin": lambda ref=False: GemmWorkload(1, 512, "prefill GEMM M=512 K=5120 N=17408, binary"),
     "gemm512_ter": lambda ref=False: GemmWorkload(2, 512, "prefill GEMM M=512 K=5120 N=17408, ternary"),
     "gemm4096_bin": lambda ref=False: GemmWorkload(1, 4096, "DiT GEMM M=4096 K=5120 N=17408, binary"),
@@ -1066,7 +1092,10 @@ WORKLOADS = {
     "layer_bin": lambda ref=False: SweepWorkload(1, "64-layer decode, fused feed-forward, binary, batch 1",
                                        fused=True),
     "layer_ter": lambda ref=False: SweepWorkload(2, "64-layer decode, fused feed-forward, ternary, batch 1",
-                                       fused=True),
+                                                 fused=True),
+    "layer_ter_plan": lambda ref=False: SweepWorkload(
+        2, "64-layer decode, fused feed-forward, ternary, batch 1 (one decode-plan launch per token)",
+        fused=True, plan=True),
     "pp512_layer_bin": lambda ref=False: LayerGemmWorkload(1, 512, "prefill M=512, one decoder layer "
                                                  "(7 products, fused feed-forward), binary"),
     "pp512_layer_ter": lambda ref=False: LayerGemmWorkload(2, 512, "prefill M=512, one decoder layer "
@@ -1078,6 +1107,7 @@ WORKLOADS = {
 }
 SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("ter_gemv_m5", 2000, 20),
              ("bin_gemv_m5", 2000, 20), ("sweep_bin", 128, 3), ("sweep_ter", 128, 3),
+             ("sweep_ter_plan", 128, 3), ("layer_ter_plan", 128, 3),
              ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
              ("gemm4096_ter", 5, 2), ("layer_bin", 128, 3), ("layer_ter", 128, 3),
              ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("hadamard", 200, 10),

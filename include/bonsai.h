@@ -188,6 +188,66 @@ bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
 bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t* x,
                                         uint16_t* y, bonsai_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Decode plans: the one-token products of a whole decoder token in ONE
+ * persistent launch. Token-by-token decode re-streams every weight per token
+ * and is bound by memory bandwidth ("第一の壁", "速度は二層"); a token of a
+ * deep decoder is hundreds of small products, and as separate launches each
+ * pays a launch, a grid-wide dependency wait and its table prologue. A plan
+ * walks its products in order inside one kernel: the weights of the next
+ * product stream while the current one finishes, and a product whose x is an
+ * earlier product's y waits (on the device, bounded) until that product is
+ * complete on every thread block.
+ *
+ * A step: the product y = x . (s (.) W)^T of `w` with one token, or with
+ * swiglu = 1 the gated feed-forward input of bonsai_gemm_swiglu (w holds 2F
+ * rows interleaved in 16-row blocks, y holds F values). `after` is the index
+ * of an EARLIER step whose y this step reads as x (directly or through
+ * memory written by it), or -1. Steps that reuse a buffer another step
+ * reads must be ordered through `after` as well (a plan runs its products
+ * concurrently where `after` allows).
+ * This build: TERNARY weights, every step's x table must fit on chip
+ * (K up to ~30K); w.flags is ignored (a plan always streams weights ahead:
+ * they must not be written while the plan runs). x, y: device, 16-byte
+ * aligned. */
+typedef struct {
+  bonsai_weights w;
+  const uint16_t* x;   /* device FP16 [k]                      */
+  uint16_t* y;         /* device FP16 [n], or [n/2] with swiglu */
+  int32_t swiglu;      /* 0 or 1                               */
+  int32_t after;       /* earlier step index, or -1            */
+} bonsai_decode_step;
+
+/* Bytes of device memory a plan of `count` steps needs (count >= 1), or -1. */
+int64_t bonsai_decode_plan_bytes(int64_t count);
+
+/* Checks the steps and writes the plan into `plan` (device memory owned by
+ * the caller, 128-byte aligned, plan_bytes >= bonsai_decode_plan_bytes(count)):
+ * per step the TMA descriptors of its weights and its parameters, and zeroed
+ * completion counters. Enqueued on `stream` (the host copy is staged before
+ * the call returns). Do not capture this call in a CUDA graph; capture
+ * bonsai_decode_run. Errors: INVALID_ARG (null pointer, `after` not an
+ * earlier step, count < 1 or > 4096), FORMAT (a binary step), SHAPE /
+ * ALIGN as bonsai_gemv, UNSUPPORTED (a step's x table does not fit). */
+bonsai_status bonsai_decode_plan_init(const bonsai_decode_step* steps, int64_t count,
+                                      void* plan, int64_t plan_bytes, bonsai_stream stream);
+
+/* Runs an initialised plan: one launch on `stream` computes every step's y.
+ * `steps` and `count` must be those the plan was initialised with (the launch
+ * geometry is recomputed from them; nothing else is read on the host). The
+ * last thread block of the run resets the completion counters, so runs of
+ * one plan may follow each other on a stream (or in a CUDA graph); two runs
+ * of the same plan must not overlap. A dependency wait that runs out (2 s)
+ * is reported as BONSAI_ERR_TIMEOUT by bonsai_check_async. */
+bonsai_status bonsai_decode_run(const bonsai_decode_step* steps, int64_t count, void* plan,
+                                bonsai_stream stream);
+
+/* Self-test of the plan's dependency wait: one thread waits on a completion
+ * counter that nothing increments, with a limit of limit_ns (1 us .. 100 ms,
+ * else BONSAI_ERR_INVALID_ARG); the wait gives up and the next
+ * bonsai_check_async reports BONSAI_ERR_TIMEOUT. No fault is involved. */
+bonsai_status bonsai_selftest_plan_wait(uint64_t limit_ns, bonsai_stream stream);
+
 /* Multi-token product Y[m][n] = sum_k X[m][k] * s[n][k/128] * w[n][k],
  * X FP16 [m][k], Y FP16 [m][n]. m <= 8 runs the streaming decode kernel with
  * m columns (speculative verification, prefill of a few tokens); larger m

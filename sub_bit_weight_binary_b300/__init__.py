@@ -51,6 +51,11 @@ class bonsai_weights_t(C.Structure):
                 ("flags", C.c_int32)]
 
 
+class bonsai_decode_step_t(C.Structure):
+    _fields_ = [("w", bonsai_weights_t), ("x", C.c_void_p), ("y", C.c_void_p),
+                ("swiglu", C.c_int32), ("after", C.c_int32)]
+
+
 _lib = None
 
 
@@ -87,6 +92,15 @@ def lib():
         L.bonsai_hadamard.restype = S
         L.bonsai_selftest_wait_timeout.argtypes = [C.c_uint64, P]
         L.bonsai_selftest_wait_timeout.restype = S
+        D = C.POINTER(bonsai_decode_step_t)
+        L.bonsai_decode_plan_bytes.argtypes = [I64]
+        L.bonsai_decode_plan_bytes.restype = I64
+        L.bonsai_decode_plan_init.argtypes = [D, I64, P, I64, P]
+        L.bonsai_decode_plan_init.restype = S
+        L.bonsai_decode_run.argtypes = [D, I64, P, P]
+        L.bonsai_decode_run.restype = S
+        L.bonsai_selftest_plan_wait.argtypes = [C.c_uint64, P]
+        L.bonsai_selftest_plan_wait.restype = S
         L.bonsai_check_async.argtypes = [P]
         L.bonsai_check_async.restype = S
         L.bonsai_status_string.argtypes = [S]
@@ -324,6 +338,67 @@ def bonsai_selftest_wait_timeout(limit_ns: int, stream=None):
     """Launch the bounded-wait self-test (a wait that must run out)."""
     _ok(lib().bonsai_selftest_wait_timeout(int(limit_ns), _stream(stream)),
         "bonsai_selftest_wait_timeout")
+
+
+def bonsai_decode_plan_bytes(count: int) -> int:
+    return int(lib().bonsai_decode_plan_bytes(count))
+
+
+def _steps_array(steps):
+    """steps: list of (Weights, x, y, swiglu, after) -> ctypes array."""
+    import torch
+    arr = (bonsai_decode_step_t * len(steps))()
+    for i, (w, x, y, swiglu, after) in enumerate(steps):
+        arr[i].w = w.c_struct()
+        arr[i].x = _ptr(x, (torch.float16,), "x")
+        arr[i].y = _ptr(y, (torch.float16,), "y")
+        arr[i].swiglu = int(bool(swiglu))
+        arr[i].after = int(after)
+    return arr
+
+
+def bonsai_decode_plan_init(steps_arr, plan, stream=None):
+    import torch
+    _ok(lib().bonsai_decode_plan_init(steps_arr, len(steps_arr),
+                                      _ptr(plan, (torch.uint8,), "plan"), plan.numel(),
+                                      _stream(stream)), "bonsai_decode_plan_init")
+
+
+def bonsai_decode_run(steps_arr, plan, stream=None):
+    import torch
+    _ok(lib().bonsai_decode_run(steps_arr, len(steps_arr), _ptr(plan, (torch.uint8,), "plan"),
+                                _stream(stream)), "bonsai_decode_run")
+
+
+class DecodePlan:
+    """A decode plan: the one-token products of a token in one launch.
+
+    steps: list of (Weights, x, y, swiglu, after) with device tensors; after
+    is the index of an earlier step whose y this step's x is, or -1. The
+    plan's device memory is a torch uint8 tensor owned here; the tensors of
+    the steps must stay alive (and in place) while the plan is used."""
+
+    def __init__(self, steps, stream=None):
+        import torch
+        self._keep = steps
+        self.steps = _steps_array(steps)
+        nbytes = bonsai_decode_plan_bytes(len(steps))
+        if nbytes < 0:
+            raise ValueError("bad number of steps")
+        raw = torch.empty(nbytes + 128, dtype=torch.uint8, device="cuda")
+        off = (-raw.data_ptr()) % 128
+        self._raw = raw
+        self.plan = raw[off:off + nbytes]
+        bonsai_decode_plan_init(self.steps, self.plan, stream)
+
+    def run(self, stream=None):
+        bonsai_decode_run(self.steps, self.plan, stream)
+
+
+def bonsai_selftest_plan_wait(limit_ns: int, stream=None):
+    """Launch the plan dependency-wait self-test (a wait that must run out)."""
+    _ok(lib().bonsai_selftest_plan_wait(int(limit_ns), _stream(stream)),
+        "bonsai_selftest_plan_wait")
 
 
 def bonsai_check_async(stream=None) -> int:

@@ -22,6 +22,10 @@ bonsai_status binarize_launch(const uint16_t*, int64_t, int64_t, uint32_t*, uint
 bonsai_status hadamard_launch(const uint16_t*, int64_t, int64_t, int32_t, const uint32_t*,
                               uint16_t*, cudaStream_t);
 bonsai_status selftest_wait_timeout_launch(uint64_t, cudaStream_t);
+int64_t gemv_plan_bytes(int64_t);
+bonsai_status gemv_plan_init(const bonsai_decode_step*, int64_t, void*, cudaStream_t);
+bonsai_status gemv_plan_run(const bonsai_decode_step*, int64_t, void*, cudaStream_t);
+bonsai_status plan_wait_selftest_launch(uint64_t, cudaStream_t);
 unsigned int read_clear_status_selftest();
 unsigned int read_clear_status_pack();
 unsigned int read_clear_status_gemv();
@@ -343,6 +347,57 @@ bonsai_status bonsai_hadamard(const uint16_t* x, int64_t m, int64_t k, int32_t b
     if (a < b + bytes && b < a + bytes) return BONSAI_ERR_INVALID_ARG;
   }
   return hadamard_launch(x, m, k, block, signs, out, stream);
+}
+
+// ---------------------------------------------------------------- plans
+namespace {
+constexpr int64_t kMaxPlanSteps = 4096;
+
+bonsai_status check_plan_steps(const bonsai_decode_step* steps, int64_t count) {
+  if (!steps || count < 1) return BONSAI_ERR_INVALID_ARG;
+  if (count > kMaxPlanSteps) return BONSAI_ERR_INVALID_ARG;
+  for (int64_t j = 0; j < count; ++j) {
+    const bonsai_decode_step& st = steps[j];
+    bonsai_status e = check_weights(&st.w);
+    if (e != BONSAI_OK) return e;
+    if (st.w.format != BONSAI_FMT_TERNARY) return BONSAI_ERR_FORMAT;
+    if (!st.x || !st.y) return BONSAI_ERR_INVALID_ARG;
+    if (st.swiglu != 0 && st.swiglu != 1) return BONSAI_ERR_INVALID_ARG;
+    if (st.after < -1 || st.after >= j) return BONSAI_ERR_INVALID_ARG;
+    if (st.swiglu && st.w.n % 16) return BONSAI_ERR_SHAPE;
+    if (!aligned16(st.x) || !aligned16(st.y)) return BONSAI_ERR_ALIGN;
+  }
+  return BONSAI_OK;
+}
+}  // namespace
+
+int64_t bonsai_decode_plan_bytes(int64_t count) {
+  if (count < 1 || count > kMaxPlanSteps) return -1;
+  return gemv_plan_bytes(count);
+}
+
+bonsai_status bonsai_decode_plan_init(const bonsai_decode_step* steps, int64_t count,
+                                      void* plan, int64_t plan_bytes, bonsai_stream stream) {
+  bonsai_status st = check_plan_steps(steps, count);
+  if (st != BONSAI_OK) return st;
+  if (!plan) return BONSAI_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(plan) % 128) return BONSAI_ERR_ALIGN;
+  if (plan_bytes < gemv_plan_bytes(count)) return BONSAI_ERR_INVALID_ARG;
+  return gemv_plan_init(steps, count, plan, stream);
+}
+
+bonsai_status bonsai_decode_run(const bonsai_decode_step* steps, int64_t count, void* plan,
+                                bonsai_stream stream) {
+  bonsai_status st = check_plan_steps(steps, count);
+  if (st != BONSAI_OK) return st;
+  if (!plan) return BONSAI_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(plan) % 128) return BONSAI_ERR_ALIGN;
+  return gemv_plan_run(steps, count, plan, stream);
+}
+
+bonsai_status bonsai_selftest_plan_wait(uint64_t limit_ns, bonsai_stream stream) {
+  if (limit_ns < 1000 || limit_ns > 100000000) return BONSAI_ERR_INVALID_ARG;
+  return plan_wait_selftest_launch(limit_ns, stream);
 }
 
 bonsai_status bonsai_selftest_wait_timeout(uint64_t limit_ns, bonsai_stream stream) {

@@ -35,6 +35,7 @@
 //    group gives exactly 0 and the accumulation only rounds the nonzero
 //    terms: sum (c-1) x = 2^10 acc.
 #include <type_traits>
+#include <vector>
 
 #include "common.cuh"
 
@@ -127,15 +128,16 @@ __device__ __forceinline__ void partial_done(uint32_t red_full, int tcount, int 
   if (lane == 0) mbar_arrive(red_full + 8 * (tcount & 1));
 }
 
+// One product's tiles; tcount counts the CTA's tiles over all products of a
+// launch (it selects the slot and its phase). Returns false after a timeout.
 template <int W>
-__device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int lane) {
-  pdl_wait();  // y may be read by earlier work on the stream
-  int tcount = 0;
+__device__ bool reduce_tiles(const Params& p, uint8_t* smem, uint32_t red_full, int lane,
+                             int& tcount) {
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tcount) {
     const int slot = tcount & 1;
     if (!__all_sync(0xFFFFFFFFu, mbar_wait(red_full + 8 * slot, (tcount >> 1) & 1))) {
       set_status(BONSAI_ERR_TIMEOUT);
-      return;
+      return false;
     }
     const float* red =
         reinterpret_cast<const float*>(smem + p.off_red) + slot * (W * 16 * p.red_cols);
@@ -167,23 +169,30 @@ __device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int l
     __syncwarp();
     if (lane == 0) mbar_arrive(red_full + 16 + 8 * slot);
   }
+  return true;
+}
+
+template <int W>
+__device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int lane) {
+  pdl_wait();  // y may be read by earlier work on the stream
+  int tcount = 0;
+  reduce_tiles<W>(p, smem, red_full, lane, tcount);
 }
 
 // Producer (one thread): per chunk one weight box and, if streamed, one
-// scale box, both completing on the stage's full barrier.
-__device__ __forceinline__ void produce(const CUtensorMap* tmw, const CUtensorMap* tms,
-                                        const Params& p, uint32_t sbase, uint32_t bar_full,
-                                        uint32_t bar_empty) {
-  if (!p.prefetch) pdl_wait();
+// scale box, both completing on the stage's full barrier. The ring position
+// (s, ph) carries over from product to product within a launch. Returns
+// false after a timeout.
+__device__ __forceinline__ bool produce_tiles(const CUtensorMap* tmw, const CUtensorMap* tms,
+                                              const Params& p, uint32_t sbase, uint32_t bar_full,
+                                              uint32_t bar_empty, int& s, uint32_t& ph) {
   const uint32_t tx = uint32_t(p.rows * p.pitch + (p.sc_tma ? p.rows * p.sc_pitch : 0));
-  int s = 0;
-  uint32_t ph = 0;
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
     const int row0 = tile * p.rows;
     for (int c = 0; c < p.chunks; ++c) {
       if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
         set_status(BONSAI_ERR_TIMEOUT);
-        return;
+        return false;
       }
       mbar_arrive_expect_tx(bar_full + 8 * s, tx);
       const uint32_t dst = sbase + p.off_stage + s * p.stage_bytes;
@@ -192,6 +201,16 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmw, const CUtensorMa
       if (++s == p.stages) { s = 0; ph ^= 1; }
     }
   }
+  return true;
+}
+
+__device__ __forceinline__ void produce(const CUtensorMap* tmw, const CUtensorMap* tms,
+                                        const Params& p, uint32_t sbase, uint32_t bar_full,
+                                        uint32_t bar_empty) {
+  if (!p.prefetch) pdl_wait();
+  int s = 0;
+  uint32_t ph = 0;
+  produce_tiles(tmw, tms, p, sbase, bar_full, bar_empty, s, ph);
 }
 
 // Consumer wait on a stage, with the same outcome in every lane of the warp.
@@ -501,6 +520,11 @@ __device__ void build_byte_table(uint8_t* smem) {
 // pair (b0, b1) of each digit MMA, at token*stride + (item within the
 // token)*48. An item covers the 20 consecutive codes 640 sg + 80 rnd + 20 q
 // (bytes 4 (4 rnd + q) + 0..3), read from global memory as 5 x 8 bytes.
+// CG: read x through L2 only. A plan step whose x another step of the same
+// launch wrote needs it (this SM's L1 may hold older lines of that buffer);
+// otherwise the ordinary cached loads are faster (neighbouring threads share
+// sectors), and x was written before the launch.
+template <bool CG>
 __device__ void build_ternary_xtable(const Params& p, uint8_t* smem) {
   const int per_token = p.n_sg * 64;
   for (int t = threadIdx.x; t < p.m * per_token; t += kTerWarps * 32) {
@@ -512,7 +536,8 @@ __device__ void build_ternary_xtable(const Params& p, uint8_t* smem) {
     for (int i = 0; i < 5; ++i) {
       uint2 v = make_uint2(0, 0);
       if (k0 + 4 * i < p.k)  // k % 128 == 0: a 4-code piece is all in or all out
-        v = *reinterpret_cast<const uint2*>(p.x + (size_t)col * p.k + k0 + 4 * i);
+        v = CG ? __ldcg(reinterpret_cast<const uint2*>(p.x + (size_t)col * p.k + k0 + 4 * i))
+               : *reinterpret_cast<const uint2*>(p.x + (size_t)col * p.k + k0 + 4 * i);
       u[2 * i] = v.x;
       u[2 * i + 1] = v.y;
     }
@@ -540,31 +565,13 @@ __device__ void build_ternary_xtable(const Params& p, uint8_t* smem) {
 // above). TOK8 = true: 5..8 tokens, B column t; a round that straddles a
 // group edge issues its five MMAs once per side (x of the other side's
 // groups is zero in that B) into separate accumulators, the others once.
+// Consumer warps: the tiles of one product. The ring position (s, ph), the
+// partial-sum slot counter and the timeout state carry over from product to
+// product within a launch.
 template <bool SC, bool TOK8>
-__global__ void __launch_bounds__(threads_for(kTerWarps), 1)
-    gemv_ternary_kernel(const __grid_constant__ CUtensorMap tmw,
-                        const __grid_constant__ CUtensorMap tms, const __grid_constant__ Params p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
-  const uint32_t red_full = bar_full + 16 * kMaxStages;
-  init_barriers<kTerWarps>(bar_full, bar_empty, p.stages);
-  __syncthreads();
-  pdl_launch_dependents();
-  if (warp == kTerWarps) {
-    if (lane == 0) produce(&tmw, &tms, p, sbase, bar_full, bar_empty);
-    return;
-  }
-  if (warp == kTerWarps + 1) {
-    reducer<kTerWarps>(p, smem, red_full, lane);
-    return;
-  }
-  build_byte_table<TOK8 ? 128 : 256>(smem);
-  pdl_wait();  // x is written by earlier work on the stream
-  build_ternary_xtable(p, smem);
-  named_bar_sync(1, kTerWarps * 32);
-
+__device__ void ternary_consume(const Params& p, uint8_t* smem, uint32_t bar_full,
+                                uint32_t bar_empty, uint32_t red_full, int warp, int lane,
+                                int& s, uint32_t& ph, int& tcount, bool& alive) {
   const int g = lane >> 2, q = lane & 3;
   // B column g: token g>>1, side g&1 (up to 4 tokens), or token g (TOK8)
   const bool bcol = (TOK8 ? g : (g >> 1)) < p.m;
@@ -577,10 +584,6 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
   const int sgw = warp / kTerParts, part = warp % kTerParts;  // super-group of the chunk, rounds
   const ExpRegs E;
   uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0, b2 = b0;
-  int s = 0;
-  uint32_t ph = 0;
-  bool alive = true;
-  int tcount = 0;
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tcount) {
     const int row0 = tile * 16;
     // token q, rows g and g+8; TOK8: rows g, g+8 x tokens 2q, 2q+1
@@ -722,6 +725,157 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
     }
     partial_done(red_full, tcount, lane);
   }
+}
+
+
+template <bool SC, bool TOK8>
+__global__ void __launch_bounds__(threads_for(kTerWarps), 1)
+    gemv_ternary_kernel(const __grid_constant__ CUtensorMap tmw,
+                        const __grid_constant__ CUtensorMap tms, const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + p.off_bar, bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t red_full = bar_full + 16 * kMaxStages;
+  init_barriers<kTerWarps>(bar_full, bar_empty, p.stages);
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == kTerWarps) {
+    if (lane == 0) produce(&tmw, &tms, p, sbase, bar_full, bar_empty);
+    return;
+  }
+  if (warp == kTerWarps + 1) {
+    reducer<kTerWarps>(p, smem, red_full, lane);
+    return;
+  }
+  build_byte_table<TOK8 ? 128 : 256>(smem);
+  pdl_wait();  // x is written by earlier work on the stream
+  build_ternary_xtable<false>(p, smem);
+  named_bar_sync(1, kTerWarps * 32);
+  int s = 0, tcount = 0;
+  uint32_t ph = 0;
+  bool alive = true;
+  ternary_consume<SC, TOK8>(p, smem, bar_full, bar_empty, red_full, warp, lane, s, ph, tcount,
+                            alive);
+}
+
+// ===========================================================================
+// a decode plan: many one-token ternary products in one persistent launch
+// ===========================================================================
+// Every weight is re-streamed per token ("第一の壁"), and a token of a deep
+// decoder is hundreds of products; as separate launches each pays the
+// launch, the dependency wait and the table prologue. Here one launch walks
+// the products of a plan in order: the producer streams each product's tiles
+// through the same ring without a break (weights are static, so it runs
+// ahead into the next product), the consumers rebuild the x table per
+// product, and the reducer counts each finished product in the plan's
+// completion counters. A product whose x is another product's y waits (one
+// thread, bounded) until every CTA has counted that product.
+struct alignas(128) PlanStep {
+  CUtensorMap tmw;  // packed weights (and scales) of the product
+  CUtensorMap tms;
+  Params p;         // the product's parameters, with the launch's shared geometry
+  int after;        // earlier product whose y is this x, or -1
+};
+
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* a) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+
+// Waits until *c >= target; false if `limit_ns` of wall-clock time ran out.
+__device__ bool wait_count(const unsigned int* c, unsigned int target,
+                           uint64_t limit_ns = kWaitNs) {
+  if (ld_acquire(c) >= target) return true;
+  const uint64_t t0 = global_ns();
+  while (ld_acquire(c) < target) {
+    __nanosleep(200);
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(threads_for(kTerWarps), 1)
+    gemv_ternary_plan_kernel(const PlanStep* __restrict__ steps, int count, unsigned int* done,
+                             const __grid_constant__ Params g) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + g.off_bar, bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t red_full = bar_full + 16 * kMaxStages;
+  init_barriers<kTerWarps>(bar_full, bar_empty, g.stages);
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == kTerWarps) {  // producer: all products' tiles through one ring
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int j = 0; j < count; ++j) {
+        const Params p = steps[j].p;
+        // the descriptors live in global memory (written by the host before
+        // the launch): acquire them for the tensor-map proxy
+        asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(&steps[j].tmw)
+                     : "memory");
+        asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(&steps[j].tms)
+                     : "memory");
+        if (!produce_tiles(&steps[j].tmw, &steps[j].tms, p, sbase, bar_full, bar_empty, s, ph))
+          break;
+      }
+    }
+    return;
+  }
+  if (warp == kTerWarps + 1) {  // reducer: y of each product, then its count
+    pdl_wait();
+    int tcount = 0;
+    bool ok = true;
+    for (int j = 0; j < count; ++j) {
+      const Params p = steps[j].p;
+      if (ok) ok = reduce_tiles<kTerWarps>(p, smem, red_full, lane, tcount);
+      __threadfence();  // this lane's stores of y before the count
+      __syncwarp();
+      if (lane == 0) atomicAdd(done + j, 1u);
+    }
+    named_bar_sync(2, (kTerWarps + 1) * 32);  // the consumers are past their last wait
+    // the last CTA to finish resets the counters for the next run of the plan
+    if (lane == 0 && atomicAdd(done + count, 1u) == gridDim.x - 1)
+      for (int j = 0; j <= count; ++j) done[j] = 0u;
+    return;
+  }
+  build_byte_table<256>(smem);
+  pdl_wait();  // the first products' x may be written by earlier work on the stream
+  int s = 0, tcount = 0;
+  uint32_t ph = 0;
+  bool alive = true, deps = true;  // after a wait runs out, later waits are skipped
+  for (int j = 0; j < count; ++j) {
+    const Params p = steps[j].p;
+    const int after = steps[j].after;
+    if (threadIdx.x == 0 && after >= 0 && deps && !wait_count(done + after, gridDim.x)) {
+      set_status(BONSAI_ERR_TIMEOUT);
+      deps = false;
+    }
+    named_bar_sync(1, kTerWarps * 32);  // also: every warp is done with the previous x table
+    __threadfence();
+    if (after >= 0) build_ternary_xtable<true>(p, smem);
+    else build_ternary_xtable<false>(p, smem);
+    named_bar_sync(1, kTerWarps * 32);
+    if (p.sc_tma)
+      ternary_consume<true, false>(p, smem, bar_full, bar_empty, red_full, warp, lane, s, ph,
+                                   tcount, alive);
+    else
+      ternary_consume<false, false>(p, smem, bar_full, bar_empty, red_full, warp, lane, s, ph,
+                                    tcount, alive);
+  }
+  named_bar_sync(2, (kTerWarps + 1) * 32);
+}
+
+// Self-test of the plan's dependency wait: one thread waits, with a limit of
+// limit_ns, on a counter that nothing increments; the wait gives up and
+// records BONSAI_ERR_TIMEOUT.
+static __device__ unsigned int g_never_counted;  // stays 0
+
+__global__ void plan_wait_selftest_kernel(uint64_t limit_ns) {
+  if (!wait_count(&g_never_counted, 1u, limit_ns)) set_status(BONSAI_ERR_TIMEOUT);
 }
 
 // ===========================================================================
@@ -891,13 +1045,27 @@ __global__ void __launch_bounds__(threads_for(kBinWarps), 1)
 
 // One launch for up to 8 binary / 4 ternary tokens. Returns UNSUPPORTED
 // when the per-CTA tables do not fit in shared memory.
-static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x, int m,
-                                     uint16_t* y, bool swiglu, cudaStream_t stream) {
+namespace gemv {
+// A product ready to launch: parameters, tensor maps, shared memory, kernel.
+struct Prepared {
+  Params p;
+  CUtensorMap tmw, tms;
+  int smem;
+  const void* fn;
+  int threads;
+};
+}  // namespace gemv
+
+// Parameters of one launch over w (tensor maps too when `maps`). Returns
+// UNSUPPORTED when the per-CTA tables do not fit in shared memory.
+static bonsai_status gemv_prepare(const bonsai_weights* w, const uint16_t* x, int m, uint16_t* y,
+                                  bool swiglu, bool maps, gemv::Prepared& out) {
   using namespace gemv;
+  Params& p = out.p;
   const bool ter = w->format == BONSAI_FMT_TERNARY;
   const int k = (int)w->k;
   const int n = (int)w->n;
-  Params p{};
+  p = Params{};
   p.scales = reinterpret_cast<const __half*>(w->scales);
   p.x = reinterpret_cast<const __half*>(x);
   p.y = reinterpret_cast<__half*>(y);
@@ -958,13 +1126,14 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
   off = up(off + p.stages * p.stage_bytes, 128);
   const int smem = off;
 
-  CUtensorMap tmw, tms;
-  if (!encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT64, const_cast<void*>(w->packed),
+  CUtensorMap& tmw = out.tmw;
+  CUtensorMap& tms = out.tms;
+  if (maps && !encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT64, const_cast<void*>(w->packed),
                             (uint64_t)(w->row_bytes / 8), (uint64_t)n, (uint64_t)w->row_bytes,
                             (uint32_t)(p.pitch / 8), (uint32_t)p.rows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return BONSAI_ERR_CUDA;
   tms = tmw;  // unused unless the scales are streamed
-  if (p.sc_tma &&
+  if (maps && p.sc_tma &&
       !encode_tensor_map_2d(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT16, const_cast<uint16_t*>(w->scales),
                             (uint64_t)p.G, (uint64_t)n, (uint64_t)p.G * 2,
                             (uint32_t)(p.sc_pitch / 2), (uint32_t)p.rows,
@@ -980,21 +1149,32 @@ static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x,
                                    : (const void*)gemv_binary_lut_kernel<false>)
                        : (p.sc_tma ? (const void*)gemv_binary_kernel<true>
                                    : (const void*)gemv_binary_kernel<false>);
-  if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return BONSAI_ERR_CUDA;
+  out.smem = smem;
+  out.fn = fn;
+  out.threads = threads_for(warps);
+  return BONSAI_OK;
+}
 
+static bonsai_status gemv_launch_one(const bonsai_weights* w, const uint16_t* x, int m,
+                                     uint16_t* y, bool swiglu, cudaStream_t stream) {
+  using namespace gemv;
+  Prepared pr;
+  const bonsai_status st = gemv_prepare(w, x, m, y, swiglu, true, pr);
+  if (st != BONSAI_OK) return st;
+  if (ensure_dynamic_smem(pr.fn, pr.smem) != cudaSuccess) return BONSAI_ERR_CUDA;
   const int sms = device_sm_count();
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(p.tiles < sms ? p.tiles : sms);
-  cfg.blockDim = dim3(threads_for(warps));
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3(pr.p.tiles < sms ? pr.p.tiles : sms);
+  cfg.blockDim = dim3(pr.threads);
+  cfg.dynamicSmemBytes = pr.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {&tmw, &tms, &p};
-  return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
+  void* args[] = {&pr.tmw, &pr.tms, &pr.p};
+  return cuda_status(cudaLaunchKernelExC(&cfg, pr.fn, args));
 }
 
 // Up to 8 tokens in one launch; ternary products of more than 4 tokens whose
@@ -1013,6 +1193,114 @@ bonsai_status gemv_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   const int64_t y_stride = swiglu ? w->n / 2 : w->n;
   return gemv_launch_one(w, x + gemv::kTerMaxTokens * w->k, (int)m - gemv::kTerMaxTokens,
                          y + gemv::kTerMaxTokens * y_stride, swiglu, stream);
+}
+
+// ------------------------------------------------------------------ plans
+// Plan memory: count PlanStep records, then count + 1 counters (one per
+// product, one for the CTAs that finished the run).
+int64_t gemv_plan_bytes(int64_t count) {
+  const int64_t b = count * (int64_t)sizeof(gemv::PlanStep) + 4 * (count + 1);
+  return (b + 127) / 128 * 128;
+}
+
+// Parameters of every product of a plan (with tensor maps when `host` is
+// given) and the launch's shared shared-memory geometry.
+static bonsai_status gemv_plan_prepare(const bonsai_decode_step* steps, int64_t count,
+                                       gemv::PlanStep* host, gemv::Params& g, int& smem) {
+  using namespace gemv;
+  auto up = [](int v, int a) { return (v + a - 1) / a * a; };
+  int xt_max = 0, stage_max = 0;
+  for (int64_t j = 0; j < count; ++j) {
+    const bonsai_decode_step& st = steps[j];
+    if (st.w.format != BONSAI_FMT_TERNARY) return BONSAI_ERR_FORMAT;
+    Prepared pr;
+    const bonsai_status e =
+        gemv_prepare(&st.w, st.x, 1, st.y, st.swiglu != 0, host != nullptr, pr);
+    if (e != BONSAI_OK) return e;
+    xt_max = pr.p.xt_stride > xt_max ? pr.p.xt_stride : xt_max;
+    stage_max = pr.p.stage_bytes > stage_max ? pr.p.stage_bytes : stage_max;
+    if (host) {
+      host[j].tmw = pr.tmw;
+      host[j].tms = pr.tms;
+      host[j].p = pr.p;
+      host[j].after = st.after;
+    }
+    if (j == 0) g = pr.p;
+  }
+  // one layout for all products: byte table, barriers, one-token partial
+  // slots, the largest x table, a ring of the largest stages
+  int off = 0;
+  g.off_lut = off;   off = up(off + kLutBytes, 128);
+  g.off_bar = off;   off = up(off + 8 * (2 * kMaxStages + 4), 128);
+  g.red_cols = 1;
+  g.off_red = off;   off = up(off + 2 * kTerWarps * 16 * 4, 128);
+  g.off_t = off;
+  g.off_xt = off;    off = up(off + xt_max, 1024);
+  g.off_stage = off;
+  g.stage_bytes = stage_max;
+  {
+    const int room = (device_max_smem_optin() - off) / stage_max;
+    int st = kStageBudget / stage_max;
+    st = st < 3 ? 3 : (st > kMaxStages ? kMaxStages : st);
+    g.stages = st < room ? st : room;
+  }
+  if (g.stages < 2) return BONSAI_ERR_UNSUPPORTED;
+  smem = up(off + g.stages * g.stage_bytes, 128);
+  if (host)
+    for (int64_t j = 0; j < count; ++j) {
+      Params& p = host[j].p;
+      p.off_lut = g.off_lut; p.off_bar = g.off_bar; p.red_cols = g.red_cols;
+      p.off_red = g.off_red; p.off_t = g.off_t; p.off_xt = g.off_xt;
+      p.off_stage = g.off_stage; p.stage_bytes = g.stage_bytes; p.stages = g.stages;
+      p.prefetch = 1;
+    }
+  return BONSAI_OK;
+}
+
+bonsai_status gemv_plan_init(const bonsai_decode_step* steps, int64_t count, void* plan,
+                             cudaStream_t stream) {
+  std::vector<gemv::PlanStep> host((size_t)count);
+  gemv::Params g;
+  int smem = 0;
+  bonsai_status st = gemv_plan_prepare(steps, count, host.data(), g, smem);
+  if (st != BONSAI_OK) return st;
+  const size_t rec = (size_t)count * sizeof(gemv::PlanStep);
+  // pageable source: the copy is staged before the call returns
+  if (cudaMemcpyAsync(plan, host.data(), rec, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return BONSAI_ERR_CUDA;
+  return cuda_status(cudaMemsetAsync(static_cast<uint8_t*>(plan) + rec, 0,
+                                     4 * (size_t)(count + 1), stream));
+}
+
+bonsai_status gemv_plan_run(const bonsai_decode_step* steps, int64_t count, void* plan,
+                            cudaStream_t stream) {
+  gemv::Params g;
+  int smem = 0;
+  bonsai_status st = gemv_plan_prepare(steps, count, nullptr, g, smem);
+  if (st != BONSAI_OK) return st;
+  const void* fn = (const void*)gemv::gemv_ternary_plan_kernel;
+  if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return BONSAI_ERR_CUDA;
+  const gemv::PlanStep* recs = static_cast<const gemv::PlanStep*>(plan);
+  unsigned int* done = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(plan) +
+                                                       (size_t)count * sizeof(gemv::PlanStep));
+  int cnt = (int)count;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(device_sm_count());  // every CTA takes part in every product
+  cfg.blockDim = dim3(gemv::threads_for(gemv::kTerWarps));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&recs, &cnt, &done, &g};
+  return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
+}
+
+bonsai_status plan_wait_selftest_launch(uint64_t limit_ns, cudaStream_t stream) {
+  gemv::plan_wait_selftest_kernel<<<1, 1, 0, stream>>>(limit_ns);
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace bonsai

@@ -177,6 +177,37 @@ def test_other_host_checks(libs):
     assert sb.STATUS[L.bonsai_pack_binary(0x10000, 0, 128, 0x20000, 16, None)] == "BONSAI_OK"
 
 
+def test_plan_host_checks(libs):
+    """Plan calls reject bad steps on the host before any CUDA call."""
+    L = sb.lib()
+    assert L.bonsai_decode_plan_bytes(0) == -1
+    assert L.bonsai_decode_plan_bytes(5000) == -1
+    nb = L.bonsai_decode_plan_bytes(3)
+    assert nb > 0 and nb % 128 == 0
+
+    def steps(fmt=2, after=(-1, 0, 1), swiglu=(0, 0, 0), x=0x30000, y=0x40000, n=32):
+        arr = (sb.bonsai_decode_step_t * len(after))()
+        for i, a in enumerate(after):
+            arr[i].w = W(fmt=fmt, n=n)
+            arr[i].x, arr[i].y, arr[i].swiglu, arr[i].after = x, y, swiglu[i], a
+        return arr
+    init, run = L.bonsai_decode_plan_init, L.bonsai_decode_run
+    good = steps()
+    assert sb.STATUS[init(good, 0, 0x80000, nb, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[init(good, 3, None, nb, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[init(good, 3, 0x80040, nb, None)] == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[init(good, 3, 0x80000, nb - 128, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[init(steps(after=(-1, 1, 0)), 3, 0x80000, nb, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[init(steps(after=(-2, 0, 0)), 3, 0x80000, nb, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[init(steps(fmt=1), 3, 0x80000, nb, None)] == "BONSAI_ERR_FORMAT"
+    assert sb.STATUS[init(steps(swiglu=(0, 2, 0)), 3, 0x80000, nb, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[init(steps(swiglu=(0, 1, 0), n=24), 3, 0x80000, nb, None)] == "BONSAI_ERR_SHAPE"
+    assert sb.STATUS[init(steps(x=0x30004), 3, 0x80000, nb, None)] == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[run(steps(after=(-1, 2, 1)), 3, 0x80000, None)] == "BONSAI_ERR_INVALID_ARG"
+    assert sb.STATUS[run(good, 3, 0x80010, None)] == "BONSAI_ERR_ALIGN"
+    assert sb.STATUS[L.bonsai_selftest_plan_wait(10, None)] == "BONSAI_ERR_INVALID_ARG"
+
+
 def test_binding_refuses_cpu_tensors(libs):
     import torch
     w = sb.Weights(1, 4, 128, torch.zeros(4, 16, dtype=torch.uint8),
