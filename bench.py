@@ -804,7 +804,9 @@ class LayerGemmWorkload(GemmWorkload):
     weight products (q, k, v, o, gate, up, down) as 4 launches -- q/k/v and
     gate/up stacked, silu(g)*u applied in the gate/up epilogue, the down
     product reading that h. The o product reads the prompt x in place of an
-    attention output (attention itself is not a weight product)."""
+    attention output (attention itself is not a weight product). Products
+    whose tiles fill the SMs unevenly (o and down, N=5120) run the stream-K
+    schedule with a workspace allocated once at setup."""
 
     def __init__(self, fmt, m, name):
         super().__init__(fmt, m, name)
@@ -824,6 +826,7 @@ class LayerGemmWorkload(GemmWorkload):
         self.x = torch.from_numpy(synth.gen_x(seed, self.m, 5120).view(np.float16)).cuda()
         self.h = torch.empty((self.m, SWEEP_SHAPES[2][0] // 2), dtype=torch.float16, device="cuda")
         self.ys = [torch.empty((self.m, n), dtype=torch.float16, device="cuda") for n, _ in SWEEP_SHAPES]
+        self.work = [sb.gemm_workspace(w, self.m) for w in self.ws]
         self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         torch.cuda.synchronize()
         sb.check()
@@ -831,10 +834,11 @@ class LayerGemmWorkload(GemmWorkload):
     def call(self):
         import sub_bit_weight_binary_b300 as sb
         qkv, o, gu, down = self.ws
-        sb.bonsai_gemm(qkv, self.x, self.ys[0])
-        sb.bonsai_gemm(o, self.x, self.ys[1])
-        sb.bonsai_gemm_swiglu(gu, self.x, self.h)
-        sb.bonsai_gemm(down, self.h, self.ys[3])
+        wq, wo, wg, wd = self.work
+        sb.bonsai_gemm_ws(qkv, self.x, self.ys[0], wq)
+        sb.bonsai_gemm_ws(o, self.x, self.ys[1], wo)
+        sb.bonsai_gemm_swiglu_ws(gu, self.x, self.h, wg)
+        sb.bonsai_gemm_ws(down, self.h, self.ys[3], wd)
 
     def measure(self, steps, warmup, clocks=None):
         r = GemmWorkload.measure(self, steps, warmup, clocks)
@@ -853,6 +857,7 @@ class LayerGemmWorkload(GemmWorkload):
         return {"workload": self.name, "m": self.m, "shapes_nk": SWEEP_SHAPES,
                 "format": "ternary" if self.fmt == 2 else "binary",
                 "ffn": "gate/up product writes silu(g)*u; down product reads it",
+                "stream_k": [n for (n, _), wk in zip(SWEEP_SHAPES, self.work) if wk is not None],
                 "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
 
 

@@ -275,6 +275,33 @@ bonsai_status bonsai_gemm(const bonsai_weights* w, const uint16_t* x,
 bonsai_status bonsai_gemm_swiglu(const bonsai_weights* w, const uint16_t* x,
                                  int64_t m, uint16_t* h, bonsai_stream stream);
 
+/* bonsai_gemm and bonsai_gemm_swiglu with a caller workspace for a
+ * stream-K schedule. Products whose 128-feature x 256-token tiles fill the
+ * SMs unevenly (prompt processing with N=5120: 80 tiles on 148 SMs) keep
+ * their whole waves of tiles and cut the last wave's k-steps into equal
+ * ranges, one per SM; a tile split over several SMs sums their FP32 partial
+ * tiles (fixed order, the first range's own sums first, the rest in SM order)
+ * before the one FP16 rounding, so results stay within the same 2e-3 norm
+ * bound. The pages' prompt-processing workload is pp512 (Bonsai 27B on
+ * phone page, "速度は二層"), whose N=5120 products are the uneven case.
+ *   workspace        device memory, 256-byte aligned, zero-filled before its
+ *                    first use; every call that completes leaves it zeroed
+ *                    again (its counters), so it can be reused call after
+ *                    call and inside CUDA graphs. Calls that may overlap on
+ *                    the GPU need separate workspaces. After a call that
+ *                    reported BONSAI_ERR_TIMEOUT, zero it again.
+ *   workspace_bytes  its size; below bonsai_gemm_workspace_bytes(w, m) (or
+ *                    workspace NULL) the call runs the plain schedule.
+ * Same results and errors as bonsai_gemm / bonsai_gemm_swiglu otherwise,
+ * plus BONSAI_ERR_ALIGN for a workspace not 256-byte aligned. */
+int64_t bonsai_gemm_workspace_bytes(const bonsai_weights* w, int64_t m);
+bonsai_status bonsai_gemm_ws(const bonsai_weights* w, const uint16_t* x, int64_t m,
+                             uint16_t* y, void* workspace, int64_t workspace_bytes,
+                             bonsai_stream stream);
+bonsai_status bonsai_gemm_swiglu_ws(const bonsai_weights* w, const uint16_t* x,
+                                    int64_t m, uint16_t* h, void* workspace,
+                                    int64_t workspace_bytes, bonsai_stream stream);
+
 /* XNOR-popcount product of +-1 activations with +-1 weights ("1-bit 嘅數學":
  * binary GEMM via XOR + popcount).
  *   a_bits  device uint32 [m][k/32], same bit layout as BINARY weights

@@ -84,6 +84,12 @@ def lib():
         L.bonsai_gemm.restype = S
         L.bonsai_gemm_swiglu.argtypes = [W, P, I64, P, P]
         L.bonsai_gemm_swiglu.restype = S
+        L.bonsai_gemm_workspace_bytes.argtypes = [W, I64]
+        L.bonsai_gemm_workspace_bytes.restype = I64
+        L.bonsai_gemm_ws.argtypes = [W, P, I64, P, P, I64, P]
+        L.bonsai_gemm_ws.restype = S
+        L.bonsai_gemm_swiglu_ws.argtypes = [W, P, I64, P, P, I64, P]
+        L.bonsai_gemm_swiglu_ws.restype = S
         L.bonsai_xnor_gemm.argtypes = [P, P, I64, W, P, P, P]
         L.bonsai_xnor_gemm.restype = S
         L.bonsai_binarize_activations.argtypes = [P, I64, I64, P, P, P]
@@ -277,6 +283,53 @@ def bonsai_gemm_swiglu(w: Weights, x, h, stream=None):
     _ok(lib().bonsai_gemm_swiglu(C.byref(ws), _ptr(x, (torch.float16,), "x"), m,
                                  _ptr(h, (torch.float16,), "h"), _stream(stream)),
         "bonsai_gemm_swiglu")
+
+
+def bonsai_gemm_workspace_bytes(w: Weights, m: int) -> int:
+    """Bytes of the stream-K workspace that bonsai_gemm_ws needs for m tokens
+    (0: the product's tiles fill the SMs evenly, no workspace is used)."""
+    ws = w.c_struct()
+    return int(lib().bonsai_gemm_workspace_bytes(C.byref(ws), int(m)))
+
+
+def gemm_workspace(w: Weights, m: int, device="cuda"):
+    """A zero-filled workspace for bonsai_gemm_ws / bonsai_gemm_swiglu_ws
+    (uint8 tensor, 256-byte aligned by the allocator), or None if the shape
+    needs none."""
+    import torch
+    nbytes = bonsai_gemm_workspace_bytes(w, m)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device) if nbytes else None
+
+
+def _ws_args(workspace):
+    if workspace is None:
+        return None, 0
+    import torch
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    return C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
+def bonsai_gemm_ws(w: Weights, x, y, workspace, stream=None):
+    """bonsai_gemm with a stream-K workspace (see gemm_workspace)."""
+    import torch
+    ws = w.c_struct()
+    m = x.shape[0] if x.dim() == 2 else 1
+    wp, wb = _ws_args(workspace)
+    _ok(lib().bonsai_gemm_ws(C.byref(ws), _ptr(x, (torch.float16,), "x"), m,
+                             _ptr(y, (torch.float16,), "y"), wp, wb, _stream(stream)),
+        "bonsai_gemm_ws")
+
+
+def bonsai_gemm_swiglu_ws(w: Weights, x, h, workspace, stream=None):
+    """bonsai_gemm_swiglu with a stream-K workspace (see gemm_workspace)."""
+    import torch
+    ws = w.c_struct()
+    m = x.shape[0] if x.dim() == 2 else 1
+    wp, wb = _ws_args(workspace)
+    _ok(lib().bonsai_gemm_swiglu_ws(C.byref(ws), _ptr(x, (torch.float16,), "x"), m,
+                                    _ptr(h, (torch.float16,), "h"), wp, wb, _stream(stream)),
+        "bonsai_gemm_swiglu_ws")
 
 
 def interleave_gate_up(gate, up):

@@ -14,7 +14,8 @@ bonsai_status gemv_launch(const bonsai_weights*, const uint16_t*, int64_t, uint1
 bonsai_status splitk_launch(const bonsai_weights*, const uint16_t*, uint16_t*, cudaStream_t);
 bonsai_status stage_x_launch(const uint16_t*, uint16_t*, int64_t, cudaStream_t);
 bonsai_status gemm_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, bool,
-                          cudaStream_t);
+                          cudaStream_t, void* ws = nullptr, int64_t ws_bytes = 0);
+int64_t gemm_workspace_bytes(const bonsai_weights*, int64_t);
 bonsai_status xnor_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
                           int32_t*, uint16_t*, cudaStream_t);
 bonsai_status binarize_launch(const uint16_t*, int64_t, int64_t, uint32_t*, uint16_t*,
@@ -280,33 +281,49 @@ bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t*
   return splitk_launch(w, x, y, stream);
 }
 
-bonsai_status bonsai_gemm(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
-                          bonsai_stream stream) {
+// bonsai_gemm / bonsai_gemm_swiglu, with or without a stream-K workspace
+static bonsai_status gemm_common(const bonsai_weights* w, const uint16_t* x, int64_t m,
+                                 uint16_t* y, bool swiglu, void* ws, int64_t ws_bytes,
+                                 bonsai_stream stream) {
   bonsai_status st = check_weights(w);
   if (st != BONSAI_OK) return st;
   if (!x || !y || m <= 0) return BONSAI_ERR_INVALID_ARG;
+  if (swiglu && w->n % 16) return BONSAI_ERR_SHAPE;
   if (m > kMaxM) return BONSAI_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
+  if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return BONSAI_ERR_INVALID_ARG;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return BONSAI_ERR_ALIGN;
   if (m <= 8) {
-    st = gemv_launch(w, x, m, y, false, stream);
+    st = gemv_launch(w, x, m, y, swiglu, stream);
     if (st != BONSAI_ERR_UNSUPPORTED) return st;
   }
-  return gemm_launch(w, x, m, y, false, stream);
+  return gemm_launch(w, x, m, y, swiglu, stream, ws, ws_bytes);
+}
+
+bonsai_status bonsai_gemm(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
+                          bonsai_stream stream) {
+  return gemm_common(w, x, m, y, false, nullptr, 0, stream);
 }
 
 bonsai_status bonsai_gemm_swiglu(const bonsai_weights* w, const uint16_t* x, int64_t m,
                                  uint16_t* h, bonsai_stream stream) {
-  bonsai_status st = check_weights(w);
-  if (st != BONSAI_OK) return st;
-  if (!x || !h || m <= 0) return BONSAI_ERR_INVALID_ARG;
-  if (w->n % 16) return BONSAI_ERR_SHAPE;
-  if (m > kMaxM) return BONSAI_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(h)) return BONSAI_ERR_ALIGN;
-  if (m <= 8) {
-    st = gemv_launch(w, x, m, h, true, stream);
-    if (st != BONSAI_ERR_UNSUPPORTED) return st;
-  }
-  return gemm_launch(w, x, m, h, true, stream);
+  return gemm_common(w, x, m, h, true, nullptr, 0, stream);
+}
+
+int64_t bonsai_gemm_workspace_bytes(const bonsai_weights* w, int64_t m) {
+  if (check_weights(w) != BONSAI_OK || m <= 8 || m > kMaxM) return 0;
+  return gemm_workspace_bytes(w, m);
+}
+
+bonsai_status bonsai_gemm_ws(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
+                             void* workspace, int64_t workspace_bytes, bonsai_stream stream) {
+  return gemm_common(w, x, m, y, false, workspace, workspace_bytes, stream);
+}
+
+bonsai_status bonsai_gemm_swiglu_ws(const bonsai_weights* w, const uint16_t* x, int64_t m,
+                                    uint16_t* h, void* workspace, int64_t workspace_bytes,
+                                    bonsai_stream stream) {
+  return gemm_common(w, x, m, h, true, workspace, workspace_bytes, stream);
 }
 
 bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,

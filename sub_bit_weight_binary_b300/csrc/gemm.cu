@@ -82,7 +82,79 @@ struct Params {
   int prefetch;
   int swiglu;    // rows 16t..16t+7 gate, 16t+8..16t+15 up: write silu(g)*u
   int y_stride;  // elements per token row of y: n, or n/2 with swiglu
+  // Stream-K (128 x 256 tiles, caller workspace): tiles [0, dp) run whole,
+  // one per CTA and wave; the k-steps of tiles [dp, tiles) are cut into
+  // sk_ctas equal ranges. sk_ctas = 0: every tile whole.
+  int dp, sk_ctas;
+  int sk_iters;                // (tiles - dp) * nk; sk_iters * sk_ctas < 2^31
+  float* ws;                   // one BM x BN FP32 partial tile per stream-K CTA
+  unsigned int* ws_count;      // partials delivered, one counter per stream-K tile
 };
+
+// A tile is split over at most kMaxPartners + 1 stream-K ranges.
+constexpr int kMaxPartners = 20;
+
+// ---- the work of a CTA -----------------------------------------------------
+// Segments: its whole tiles blockIdx.x + i * gridDim.x below dp, then at most
+// two stream-K pieces [a, b) of the cut k-steps (b - a <= nk, so a piece
+// ends the first tile it starts in, or begins the next). The piece that
+// holds k-step 0 of a tile finishes it: it adds the partial tiles of the
+// CTAs that hold the rest (their first pieces) and writes Y.
+__device__ __forceinline__ int sk_start(const Params& p, int c) {
+  return c * p.sk_iters / p.sk_ctas;
+}
+// SK = false (the larger tiles, never cut): whole tiles only.
+template <bool SK>
+struct Segs {
+  int whole, count;
+  int a, b;
+  __device__ __forceinline__ explicit Segs(const Params& p) {
+    const int c = blockIdx.x, gd = gridDim.x;
+    whole = p.dp > c ? (p.dp - c + gd - 1) / gd : 0;
+    count = whole;
+    a = b = 0;
+    if (SK && c < p.sk_ctas) {
+      a = sk_start(p, c);
+      b = sk_start(p, c + 1);
+      if (b > a) count += b > (a / p.nk + 1) * p.nk ? 2 : 1;
+    }
+  }
+  // tile and k-step range [j0, j1) (in the tile's K order) of segment i
+  __device__ __forceinline__ void at(const Params& p, int i, int& tile, int& j0, int& j1) const {
+    if (!SK || i < whole) {
+      tile = blockIdx.x + i * (int)gridDim.x;
+      j0 = 0;
+      j1 = p.nk;
+      return;
+    }
+    const int t0 = a / p.nk;
+    if (i == whole) {
+      tile = p.dp + t0;
+      j0 = a - t0 * p.nk;
+      j1 = b - t0 * p.nk < p.nk ? b - t0 * p.nk : p.nk;
+    } else {
+      tile = p.dp + t0 + 1;
+      j0 = 0;
+      j1 = b - (t0 + 1) * p.nk;
+    }
+  }
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* a) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+// Waits until *c >= target; false if kWaitNs of wall-clock time ran out.
+__device__ bool wait_at_least(const unsigned int* c, unsigned int target) {
+  if (ld_acquire_u32(c) >= target) return true;
+  const uint64_t t0 = global_ns();
+  while (ld_acquire_u32(c) < target) {
+    __nanosleep(100);
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+  return true;
+}
 
 // ---- tcgen05 / TMA wrappers ------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
@@ -128,6 +200,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),      \
         "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),      \
         "=r"(v[30]), "=r"(v[31])                                                           \
+      : "r"(taddr))
+
+#define TMEM_LD_16(taddr, v)                                                              \
+  asm volatile(                                                                           \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"     \
+      "%12,%13,%14,%15}, [%16];"                                                          \
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),            \
+        "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),          \
+        "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])                                 \
       : "r"(taddr))
 
 // Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
@@ -311,6 +392,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t acc_full = empty_b + 8 * NB, acc_empty = acc_full + 16;
   const uint32_t drain = acc_empty + 16;
   const uint32_t tmem_slot = drain + 8;
+  const uint32_t epi_bar = sBar + 192;  // the epilogue warps' own barrier (stream-K)
+  const uint32_t stg_bar = sBar + 200;  // partial tiles copied into the idle rings
+  static_assert(8 * (2 * A_STAGES + 2 * NB + 5) + 4 <= 192, "barriers overlap epi_bar");
 
   if ((sA & 1023u) != 0) {  // the swizzle atoms need 1024-byte alignment
     if (threadIdx.x == 0) set_status(BONSAI_ERR_UNSUPPORTED);
@@ -330,6 +414,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(acc_empty + 8 * a, 4);
     }
     mbar_init(drain, 1);
+    mbar_init(epi_bar, 4);
+    mbar_init(stg_bar, 1);
     fence_barrier_init();
   }
   if (FMT == BONSAI_FMT_TERNARY && warp >= W_DQ) {
@@ -368,15 +454,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int rows = p.n - n0 < FM ? p.n - n0 : FM;
         prefetch_l2(p.w + (long long)n0 * p.row_bytes, (long long)rows * p.row_bytes);
       };
-      prefetch_tile(blockIdx.x);
+      const Segs<MODE == NARROW> sg(p);
+      int tile = p.tiles, j0 = 0, j1 = 0;
+      if (sg.count > 0) {
+        sg.at(p, 0, tile, j0, j1);
+        prefetch_tile(tile);
+      }
       uint32_t g = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      for (int i = 0; i < sg.count && ok; ++i) {
+        sg.at(p, i, tile, j0, j1);
         const int m0 = (tile % p.tok_tiles) * TT;
         // token halves of a wide tile that hold tokens (rows past m read as 0)
         const int halves = (p.m - m0 + BN - 1) / BN < C::HALVES ? (p.m - m0 + BN - 1) / BN : C::HALVES;
-        prefetch_tile(tile + gridDim.x);
-        for (int kk = 0; kk < p.nk; ++kk, ++g) {
+        if (i + 1 < sg.count) {
+          int t2, a2, b2;
+          sg.at(p, i + 1, t2, a2, b2);
+          if (t2 != tile) prefetch_tile(t2);
+        }
+        for (int kk = j0; kk < j1; ++kk, ++g) {
           const int s = g % B_STAGES;
           const uint32_t ph = (g / B_STAGES) & 1;
           for (int h = 0; h < C::HALVES && ok; ++h) {
@@ -403,14 +499,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t g = 0, it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++it) {
+      const Segs<MODE == NARROW> sg(p);
+      for (int i = 0; i < sg.count && ok; ++i, ++it) {
+        int tile, j0, j1;
+        sg.at(p, i, tile, j0, j1);
         const uint32_t a = it % C::NACC, use = it / C::NACC;
         if (!mbar_wait(acc_empty + 8 * a, (use & 1) ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + a * 256;
         const int m0 = (tile % p.tok_tiles) * TT;
         const int halves = (p.m - m0 + BN - 1) / BN < C::HALVES ? (p.m - m0 + BN - 1) / BN : C::HALVES;
-        for (int kk = 0; kk < p.nk; ++kk, ++g) {
+        for (int kk = j0; kk < j1; ++kk, ++g) {
           const int sa = g % A_STAGES, sb = g % B_STAGES;
           const uint32_t pb = (g / B_STAGES) & 1;
           if (!mbar_wait(full_a + 8 * sa, (g / A_STAGES) & 1)) {
@@ -435,7 +534,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int k4 = 0; k4 < BK / 16; ++k4)  // +32 bytes per K=16 step inside the atom
                   mma_f16_ss(d_tmem + (f + h) * 256, ad + 2 * k4, bd + 2 * k4, kIdesc,
-                             (kk | k4) != 0);
+                             ((kk - j0) | k4) != 0);
               }
               mma_commit(empty_b + 8 * ib);
             } else {
@@ -454,48 +553,192 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------- epilogue -------------------------------
     pdl_wait();
     const int e = warp - W_EPI;  // TMEM lanes 32e .. 32e+31
+    const int et = threadIdx.x - W_EPI * 32;  // 0..127
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
+    // all four epilogue warps at one point (bounded: a warp that gave up on
+    // a wait still arrives, and a wait that runs out is recorded)
+    uint32_t ephase = 0;
+    auto epi_sync = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(epi_bar);
+      if (!mbar_wait(epi_bar, ephase & 1)) set_status(BONSAI_ERR_TIMEOUT);
+      ++ephase;
+    };
+    const Segs<MODE == NARROW> sg(p);
+    for (int i = 0; i < sg.count; ++i, ++it) {
+      int tile, j0, j1;
+      sg.at(p, i, tile, j0, j1);
+      // stream-K: a piece that does not hold k-step 0 leaves its sums in its
+      // partial tile; the piece that does adds those of the next CTAs
+      // (their first pieces lie in this tile), in CTA order
+      const bool sk = MODE == NARROW && i >= sg.whole;
+      const bool partial = sk && j0 > 0;
+      int np = 0;
+      if (sk && !partial) {
+        const int t_end = (tile - p.dp + 1) * p.nk;
+        while ((int)blockIdx.x + 1 + np < p.sk_ctas &&
+               sk_start(p, (int)blockIdx.x + 1 + np) < t_end)
+          ++np;
+        if (np > kMaxPartners) {  // the host keeps ranges long enough for this never to happen
+          if (et == 0) set_status(BONSAI_ERR_UNSUPPORTED);
+          np = kMaxPartners;
+        }
+        if (np > 0) {
+          if (et == 0 && !wait_at_least(p.ws_count + (tile - p.dp), (unsigned)np))
+            set_status(BONSAI_ERR_TIMEOUT);
+          epi_sync();
+        }
+      }
       const uint32_t a = it % C::NACC, use = it / C::NACC;
       if (!mbar_wait(acc_full + 8 * a, use & 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
       tc_fence_after();
       const int n0 = (tile / p.tok_tiles) * FM, m0 = (tile % p.tok_tiles) * TT;
-      // column chunks that hold tokens (the MMAs wrote only the used halves)
-      const int chunks = (p.m - m0 + 31) / 32 < TT / 32 ? (p.m - m0 + 31) / 32 : TT / 32;
+      if constexpr (MODE == NARROW) {
+        if (sk) {
+          // Stream-K pieces, 16 tokens (a step) at a time. Partial tile
+          // layout [step][i4][feature row][4 tokens] FP32: a warp's float4
+          // stores and loads cover 512 contiguous bytes. The finishing piece
+          // is its CTA's last segment, so its MMAs have completed and the A
+          // and B rings (192 KB) are idle: the partners' partial tiles are
+          // brought there by bulk copies, a group of steps of all partners
+          // at a time, and added from shared memory.
+          const int steps = (p.m - m0 + 15) / 16 < BN / 16 ? (p.m - m0 + 15) / 16 : BN / 16;
+          const uint32_t tl = tmem_base + ((uint32_t)(32 * e) << 16) + a * 256;
+          constexpr int STEP_BYTES = BM * 16 * 4;  // 8 KB
+          auto part_at = [&](int cta, int st) {
+            return p.ws + (size_t)cta * (BM * BN) + (size_t)st * (BM * 16);
+          };
+          if (partial) {
+            for (int st = 0; st < steps; ++st) {
+              uint32_t v[16];
+              TMEM_LD_16(tl + 16 * st, v);
+              tmem_ld_wait();
+              float4* dst = reinterpret_cast<float4*>(part_at(blockIdx.x, st)) + et;
+#pragma unroll
+              for (int i4 = 0; i4 < 4; ++i4)
+                dst[i4 * BM] = make_float4(__uint_as_float(v[4 * i4]), __uint_as_float(v[4 * i4 + 1]),
+                                           __uint_as_float(v[4 * i4 + 2]), __uint_as_float(v[4 * i4 + 3]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + 8 * a);
+          } else {
+            const int feat = n0 + 32 * e + lane;
+            const bool fok = feat < p.n;
+            constexpr int RING = A_STAGES * A_BYTES + B_STAGES * B_BYTES;
+            static_assert(RING >= 24 * STEP_BYTES, "the rings hold 24 steps");
+            // steps per group: np partners x group <= 24 steps
+            const int grp = np > 0 ? (24 / np < steps ? 24 / np : steps) : steps;
+            static_assert(kMaxPartners <= 24, "one step of every partner fits the rings");
+            uint32_t gphase = 0;
+            for (int s0 = 0; s0 < steps; s0 += grp) {
+              const int gn = steps - s0 < grp ? steps - s0 : grp;
+              if (np > 0) {
+                if (et == 0) {
+                  mbar_arrive_expect_tx(stg_bar, (uint32_t)(np * gn * STEP_BYTES));
+                  for (int q = 0; q < np; ++q)
+                    for (int st = 0; st < gn; ++st)
+                      bulk_g2s(sA + (q * grp + st) * STEP_BYTES, part_at(blockIdx.x + 1 + q, s0 + st),
+                               STEP_BYTES, stg_bar, policy_evict_first());
+                }
+                if (!mbar_wait(stg_bar, gphase & 1)) set_status(BONSAI_ERR_TIMEOUT);
+                ++gphase;
+              }
+              for (int st = s0; st < s0 + gn; ++st) {
+                uint32_t v[16];
+                TMEM_LD_16(tl + 16 * st, v);
+                tmem_ld_wait();
+                if (st == steps - 1) {
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(acc_empty + 8 * a);
+                }
+                for (int q = 0; q < np; ++q) {
+                  const uint32_t src = sA + (q * grp + st - s0) * STEP_BYTES + et * 16;
+#pragma unroll
+                  for (int i4 = 0; i4 < 4; ++i4) {
+                    float4 f;
+                    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                                 : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                                 : "r"(src + i4 * BM * 16));
+                    v[4 * i4] = __float_as_uint(__uint_as_float(v[4 * i4]) + f.x);
+                    v[4 * i4 + 1] = __float_as_uint(__uint_as_float(v[4 * i4 + 1]) + f.y);
+                    v[4 * i4 + 2] = __float_as_uint(__uint_as_float(v[4 * i4 + 2]) + f.z);
+                    v[4 * i4 + 3] = __float_as_uint(__uint_as_float(v[4 * i4 + 3]) + f.w);
+                  }
+                }
+                if (p.swiglu) {
+                  const int hcol = (feat >> 4) * 8 + (feat & 7);
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    const float g = __uint_as_float(v[j]);
+                    const float u = __shfl_down_sync(0xFFFFFFFFu, g, 8);
+                    const int tok = m0 + 16 * st + j;
+                    if (fok && !(lane & 8) && tok < p.m)
+                      p.y[(size_t)tok * p.y_stride + hcol] = __float2half_rn(silu(g) * u);
+                  }
+                } else if (fok) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    const int tok = m0 + 16 * st + j;
+                    if (tok < p.m)
+                      p.y[(size_t)tok * p.y_stride + feat] = __float2half_rn(__uint_as_float(v[j]));
+                  }
+                }
+              }
+              if (np > 0 && s0 + gn < steps) epi_sync();  // every read of the group before the next copy
+            }
+          }
+        }
+      }
+      if (!(MODE == NARROW && sk)) {
+        // column chunks that hold tokens (the MMAs wrote only the used halves)
+        const int chunks = (p.m - m0 + 31) / 32 < TT / 32 ? (p.m - m0 + 31) / 32 : TT / 32;
 #pragma unroll 1
-      for (int cf = 0; cf < chunks * C::FHALVES; ++cf) {
-        const int f = cf / chunks, c = cf - f * chunks;  // feature half, token chunk
-        const int feat = n0 + BM * f + 32 * e + lane;
-        const bool fok = feat < p.n;
-        uint32_t v[32];
-        TMEM_LD_32(tmem_base + ((uint32_t)(32 * e) << 16) + (a + f) * 256 + 32 * c, v);
-        tmem_ld_wait();
-        if (cf == chunks * C::FHALVES - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty + 8 * a);
-        }
-        if (p.swiglu) {
-          // lanes 0-7 / 16-23 hold gate features, lanes 8-15 / 24-31 the up
-          // features of the same outputs (n % 16 == 0, so fok is uniform
-          // over each 16-lane block)
-          const int hcol = (feat >> 4) * 8 + (feat & 7);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float g = __uint_as_float(v[j]);
-            const float u = __shfl_down_sync(0xFFFFFFFFu, g, 8);
-            const int tok = m0 + 32 * c + j;
-            if (fok && !(lane & 8) && tok < p.m)
-              p.y[(size_t)tok * p.y_stride + hcol] = __float2half_rn(silu(g) * u);
+        for (int cf = 0; cf < chunks * C::FHALVES; ++cf) {
+          const int f = cf / chunks, c = cf - f * chunks;  // feature half, token chunk
+          const int feat = n0 + BM * f + 32 * e + lane;
+          const bool fok = feat < p.n;
+          uint32_t v[32];
+          TMEM_LD_32(tmem_base + ((uint32_t)(32 * e) << 16) + (a + f) * 256 + 32 * c, v);
+          tmem_ld_wait();
+          if (cf == chunks * C::FHALVES - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + 8 * a);
           }
-        } else if (fok) {
+          if (p.swiglu) {
+            // lanes 0-7 / 16-23 hold gate features, lanes 8-15 / 24-31 the up
+            // features of the same outputs (n % 16 == 0, so fok is uniform
+            // over each 16-lane block)
+            const int hcol = (feat >> 4) * 8 + (feat & 7);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int tok = m0 + 32 * c + j;
-            if (tok < p.m)
-              p.y[(size_t)tok * p.y_stride + feat] = __float2half_rn(__uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) {
+              const float g = __uint_as_float(v[j]);
+              const float u = __shfl_down_sync(0xFFFFFFFFu, g, 8);
+              const int tok = m0 + 32 * c + j;
+              if (fok && !(lane & 8) && tok < p.m)
+                p.y[(size_t)tok * p.y_stride + hcol] = __float2half_rn(silu(g) * u);
+            }
+          } else if (fok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int tok = m0 + 32 * c + j;
+              if (tok < p.m)
+                p.y[(size_t)tok * p.y_stride + feat] = __float2half_rn(__uint_as_float(v[j]));
+            }
           }
         }
+      }
+      if (partial) {  // every row stored, then one count for the tile
+        __threadfence();
+        epi_sync();
+        if (et == 0)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.ws_count + (tile - p.dp))
+                       : "memory");
+      } else if (np > 0) {  // every partial read: the counter is zero again for the next call
+        epi_sync();
+        if (et == 0) p.ws_count[tile - p.dp] = 0;
       }
     }
   } else if (warp >= W_DQ) {
@@ -534,7 +777,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     uint32_t g = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+    const Segs<MODE == NARROW> sg(p);
+    for (int i = 0; i < sg.count && ok; ++i) {
+      int tile, j0, j1;
+      sg.at(p, i, tile, j0, j1);
       const int n = (tile / p.tok_tiles) * FM + r;
       const bool nok = n < p.n;
       const uint8_t* wrow = p.w + (long long)(nok ? n : 0) * p.row_bytes;
@@ -544,7 +790,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool nok2 = FM > BM && n + BM < p.n;
       const uint8_t* wrow2 = p.w + (long long)(nok2 ? n + BM : 0) * p.row_bytes;
       const __half* srow2 = p.scales + (size_t)(nok2 ? n + BM : 0) * p.G;
-      for (int j = 0; j < p.nk; ++j, ++g) {
+      for (int j = j0; j < j1; ++j, ++g) {
         if ((g & 1) != h) continue;
         const int kk = k_at(p, tile, j);  // the k-step this stage holds
         const int s = g % A_STAGES;
@@ -580,12 +826,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             cur_key = key;
             // prefetch the block that follows in this thread's order: the
-            // next one of the tile's rotated order, or the next tile's first
-            const int un = u + 1 < nblk ? u + 1 : 0;
-            const bool last = un == k_rot(p, tile);
-            const int nt = last ? tile + (int)gridDim.x : tile;
-            const int nu = last ? k_rot(p, nt) : un;
-            if (nt < p.tiles) {
+            // one of the segment's next k-step outside this block, or the
+            // next segment's first
+            const int jn = j + (KPB - kk % KPB < p.nk - kk ? KPB - kk % KPB : p.nk - kk);
+            int nt = -1, nj = 0;
+            if (jn < j1) {
+              nt = tile;
+              nj = jn;
+            } else if (i + 1 < sg.count) {
+              int b2;
+              sg.at(p, i + 1, nt, nj, b2);
+            }
+            if (nt >= 0) {
+              const int nu = k_at(p, nt, nj) / KPB;
               load_block(nt, nu, nxt, nsc);
               nxt_key = nt * nblk + nu;
             }
@@ -616,10 +869,100 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == W_TMEM) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// Stream-K schedule of `tiles` 128 x 256 tiles of nk k-steps on `sms` CTAs:
+// the whole waves stay data-parallel; when the plain schedule would leave
+// more than an eighth of the SM time idle, the last wave is cut into equal
+// k-step ranges of at least kMinSkSteps, each CTA's range within two
+// consecutive tiles. (A finishing range adds the others' partial tiles at
+// the end of the kernel, ~10 us measured at 512 tokens, so an almost full
+// last wave is not worth cutting.)
+constexpr int kMinSkSteps = 8;
+struct SkPlan {
+  int dp = 0, sk_ctas = 0;
+  long long iters = 0;
+  long long bytes = 0;  // workspace: counters, then the partial tiles
+  long long count_bytes = 0;
+};
+static SkPlan sk_plan(long long tiles, int nk, int sms) {
+  SkPlan s;
+  const long long rest = tiles % sms;
+  const long long waves = (tiles + sms - 1) / sms;
+  if (rest == 0 || tiles * 8 >= 7 * waves * sms) return s;
+  const long long iters = rest * nk;
+  if (iters * sms >= (1LL << 31)) return s;  // the device splits ranges in 32-bit
+  long long ctas = iters / kMinSkSteps;
+  if (ctas > sms) ctas = sms;
+  // ranges of at least nk / (kMaxPartners - 1) k-steps: a tile meets at most
+  // kMaxPartners + 1 of them
+  if (ctas > (kMaxPartners - 1) * rest) ctas = (kMaxPartners - 1) * rest;
+  if (ctas <= rest) return s;  // ranges of a whole tile: nothing to gain
+  s.dp = (int)(tiles - rest);
+  s.sk_ctas = (int)ctas;
+  s.iters = iters;
+  s.count_bytes = (rest * 4 + 255) / 256 * 256;
+  s.bytes = s.count_bytes + ctas * (long long)BM * BN * 4;
+  return s;
+}
+
+// The tile shape (NARROW / WIDE / TALL) and, for NARROW tiles with a
+// workspace, the stream-K schedule.
+struct Shape {
+  int mode, tt, fm;
+  long long tiles;
+  SkPlan sk;
+};
+static Shape gemm_shape(const bonsai_weights* w, int64_t m, bool stream_k) {
+  const bool ter = w->format == BONSAI_FMT_TERNARY;
+  auto smem_of = [](int a, int a_bytes, int b, int b_bytes, bool lut) {
+    return a * a_bytes + b * b_bytes + (lut ? LUT_BYTES : 0) + BAR_BYTES;
+  };
+  using CTW = Cfg<BONSAI_FMT_TERNARY, WIDE>;
+  using CBT = Cfg<BONSAI_FMT_BINARY, TALL>;
+  const int smem_big = ter ? smem_of(CTW::A, CTW::A_BYTES, CTW::B, CTW::B_BYTES, true)
+                           : smem_of(CBT::A, CBT::A_BYTES, CBT::B, CBT::B_BYTES, false);
+  // Besides the 128-feature x 256-token tiles (two TMEM accumulators, the
+  // epilogue overlapping the next tile), each format has a larger tile with
+  // one 512-column accumulator: ternary 512 tokens (halves the dequantisation
+  // per FLOP, the ternary limiter: +7% at M=512, N=17408), binary 256
+  // features (halves the activation-tile traffic per FLOP, where binary's MMA
+  // thread waits; 512-token tiles measured -9% for binary). The larger tile
+  // is taken when the SMs stay about as busy (busy = tiles / (waves * SMs);
+  // 0.9 for stream-K narrow tiles): a layer's N=5120 products would
+  // otherwise drop from 80 to 40 tiles.
+  const long long sms_l = device_sm_count();
+  auto busy = [&](long long tiles) {
+    return (double)tiles / (double)(((tiles + sms_l - 1) / sms_l) * sms_l);
+  };
+  const long long ft = (w->n + BM - 1) / BM, ft2 = (w->n + 2 * BM - 1) / (2 * BM);
+  const long long tok = (m + 255) / 256, tok2 = (m + 511) / 512;
+  const int nk = (int)(w->k / BK);
+  const SkPlan skn = stream_k ? sk_plan(ft * tok, nk, (int)sms_l) : SkPlan{};
+  // a cut last wave fills the SMs, less its partial-tile traffic
+  const double busy_narrow = skn.sk_ctas ? 0.9 : busy(ft * tok);
+  const double busy_big = ter ? busy(ft * tok2) : busy(ft2 * tok);
+  // Binary takes 256-feature tiles only while every SM gets at most one: the
+  // gain is the halved X traffic, and with several tiles per SM the
+  // epilogue no longer overlapped cancels it (interleaved A/B on one GPU:
+  // M=512, N=17408 +13%, M=4096 even, a layer whose q/k/v and gate/up took
+  // them -4.5%).
+  const bool big = (ter ? m > BN : ft2 * tok <= sms_l) && busy_big >= 0.85 * busy_narrow &&
+                   smem_big <= device_max_smem_optin();
+  Shape sh;
+  sh.mode = !big ? NARROW : (ter ? WIDE : TALL);
+  sh.tt = sh.mode == WIDE ? 512 : 256;
+  sh.fm = sh.mode == TALL ? 256 : BM;
+  sh.tiles = ((w->n + sh.fm - 1) / sh.fm) * ((m + sh.tt - 1) / sh.tt);
+  if (sh.mode == NARROW) sh.sk = skn;
+  return sh;
+}
 }  // namespace gemm
 
+int64_t gemm_workspace_bytes(const bonsai_weights* w, int64_t m) {
+  return gemm::gemm_shape(w, m, true).sk.bytes;
+}
+
 bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m, uint16_t* y,
-                          bool swiglu, cudaStream_t stream) {
+                          bool swiglu, cudaStream_t stream, void* ws, int64_t ws_bytes) {
   using namespace gemm;
   if (m > 0x7FFFFFFF / 2) return BONSAI_ERR_UNSUPPORTED;
   CUtensorMap tm;
@@ -639,32 +982,12 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
                               : smem_of(CBN::A, CBN::A_BYTES, CBN::B, CBN::B_BYTES, false);
   const int smem_big = ter ? smem_of(CTW::A, CTW::A_BYTES, CTW::B, CTW::B_BYTES, true)
                            : smem_of(CBT::A, CBT::A_BYTES, CBT::B, CBT::B_BYTES, false);
-  // Besides the 128-feature x 256-token tiles (two TMEM accumulators, the
-  // epilogue overlapping the next tile), each format has a larger tile with
-  // one 512-column accumulator: ternary 512 tokens (halves the dequantisation
-  // per FLOP, the ternary limiter: +7% at M=512, N=17408), binary 256
-  // features (halves the activation-tile traffic per FLOP, where binary's MMA
-  // thread waits; 512-token tiles measured -9% for binary). The larger tile
-  // is taken when the SMs stay about as busy (busy = tiles / (waves * SMs)):
-  // a layer's N=5120 products would otherwise drop from 80 to 40 tiles.
-  const long long sms_l = device_sm_count();
-  auto busy = [&](long long tiles) {
-    return (double)tiles / (double)(((tiles + sms_l - 1) / sms_l) * sms_l);
-  };
-  const long long ft = (w->n + BM - 1) / BM, ft2 = (w->n + 2 * BM - 1) / (2 * BM);
-  const long long tok = (m + 255) / 256, tok2 = (m + 511) / 512;
-  const double busy_narrow = busy(ft * tok);
-  const double busy_big = ter ? busy(ft * tok2) : busy(ft2 * tok);
-  // Binary takes 256-feature tiles only while every SM gets at most one: the
-  // gain is the halved X traffic, and with several tiles per SM the
-  // epilogue no longer overlapped cancels it (interleaved A/B on one GPU:
-  // M=512, N=17408 +13%, M=4096 even, a layer whose q/k/v and gate/up took
-  // them -4.5%).
-  const bool big = (ter ? m > BN : ft2 * tok <= sms_l) && busy_big >= 0.85 * busy_narrow &&
-                   smem_big <= device_max_smem_optin();
-  const int mode = !big ? NARROW : (ter ? WIDE : TALL);
-  const int tt = mode == WIDE ? 512 : 256;
-  const int fm = mode == TALL ? 256 : BM;
+  Shape sh = gemm_shape(w, m, ws != nullptr);
+  if (sh.sk.sk_ctas && sh.sk.bytes > ws_bytes) {  // workspace too small: whole tiles
+    sh = gemm_shape(w, m, false);
+  }
+  const bool big = sh.mode != NARROW;
+  const int tt = sh.tt, fm = sh.fm;
 
   Params p{};
   p.w = static_cast<const uint8_t*>(w->packed);
@@ -681,6 +1004,15 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
   p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.y_stride = swiglu ? p.n / 2 : p.n;
+  if (sh.sk.sk_ctas) {
+    p.dp = sh.sk.dp;
+    p.sk_ctas = sh.sk.sk_ctas;
+    p.sk_iters = (int)sh.sk.iters;
+    p.ws_count = static_cast<unsigned int*>(ws);
+    p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sh.sk.count_bytes);
+  } else {
+    p.dp = p.tiles;
+  }
 
   const int smem = big ? smem_big : smem_narrow;
   if (smem > device_max_smem_optin()) return BONSAI_ERR_UNSUPPORTED;
@@ -693,7 +1025,7 @@ bonsai_status gemm_launch(const bonsai_weights* w, const uint16_t* x, int64_t m,
 
   const int sms = device_sm_count();
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(p.tiles < sms ? p.tiles : sms);
+  cfg.gridDim = dim3(p.sk_ctas ? sms : (p.tiles < sms ? p.tiles : sms));
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

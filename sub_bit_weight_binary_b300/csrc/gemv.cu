@@ -57,6 +57,10 @@ constexpr int kBinWarps = 16;
 constexpr int kTerWarps = 16;
 __host__ __device__ constexpr int threads_for(int w) { return (w + 2) * 32; }
 constexpr int kMaxStages = 8;
+// Stages the producer may issue before the consumers have their activations:
+// the weight boxes and the activation loads share the SM's return path from
+// L2, so a full ring requested ahead of x delays x by its whole size.
+constexpr int kEarlyStages = 2;
 constexpr int kStageBudget = 96 * 1024;    // bytes in flight per CTA
 constexpr int kChunk = 1024;               // packed bytes per row per stage
 constexpr int kLutBytes = 256 * 256;       // ternary: 256 entries x (32 lanes x 4 B + pad)
@@ -90,7 +94,12 @@ struct Params {
 
 // ---------------------------------------------------------------------------
 // Barriers at off_bar: full[kMaxStages], empty[kMaxStages] of the weight
-// ring, then red_full[2], red_empty[2] of the two partial-sum slots.
+// ring, then red_full[2], red_empty[2] of the two partial-sum slots, then
+// x_ready (the consumers' tables are built).
+constexpr int kBarriers = 2 * kMaxStages + 5;
+__device__ __forceinline__ uint32_t x_ready_bar(uint32_t bar_full) {
+  return bar_full + 8 * (2 * kMaxStages + 4);
+}
 template <int W>
 __device__ __forceinline__ void init_barriers(uint32_t bar_full, uint32_t bar_empty, int stages) {
   if (threadIdx.x == 0) {
@@ -103,6 +112,7 @@ __device__ __forceinline__ void init_barriers(uint32_t bar_full, uint32_t bar_em
       mbar_init(red_full + 8 * s, W);
       mbar_init(red_full + 16 + 8 * s, 1);
     }
+    mbar_init(x_ready_bar(bar_full), 1);
     fence_barrier_init();
   }
 }
@@ -181,15 +191,22 @@ __device__ void reducer(const Params& p, uint8_t* smem, uint32_t red_full, int l
 
 // Producer (one thread): per chunk one weight box and, if streamed, one
 // scale box, both completing on the stage's full barrier. The ring position
-// (s, ph) carries over from product to product within a launch. Returns
-// false after a timeout.
+// (s, ph) carries over from product to product within a launch. With x_ready
+// (not 0) only the first kEarlyStages stages go out before the consumers
+// signal it. Returns false after a timeout.
 __device__ __forceinline__ bool produce_tiles(const CUtensorMap* tmw, const CUtensorMap* tms,
                                               const Params& p, uint32_t sbase, uint32_t bar_full,
-                                              uint32_t bar_empty, int& s, uint32_t& ph) {
+                                              uint32_t bar_empty, int& s, uint32_t& ph,
+                                              uint32_t x_ready = 0) {
   const uint32_t tx = uint32_t(p.rows * p.pitch + (p.sc_tma ? p.rows * p.sc_pitch : 0));
+  int issued = 0;
   for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
     const int row0 = tile * p.rows;
-    for (int c = 0; c < p.chunks; ++c) {
+    for (int c = 0; c < p.chunks; ++c, ++issued) {
+      if (x_ready && issued == kEarlyStages && !mbar_wait(x_ready, 0)) {
+        set_status(BONSAI_ERR_TIMEOUT);
+        return false;
+      }
       if (!mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
         set_status(BONSAI_ERR_TIMEOUT);
         return false;
@@ -210,7 +227,7 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmw, const CUtensorMa
   if (!p.prefetch) pdl_wait();
   int s = 0;
   uint32_t ph = 0;
-  produce_tiles(tmw, tms, p, sbase, bar_full, bar_empty, s, ph);
+  produce_tiles(tmw, tms, p, sbase, bar_full, bar_empty, s, ph, x_ready_bar(bar_full));
 }
 
 // Consumer wait on a stage, with the same outcome in every lane of the warp.
@@ -359,6 +376,7 @@ __global__ void __launch_bounds__(threads_for(kBinWarps), 1)
   pdl_wait();  // x is written by earlier work on the stream
   build_binary_tables<kBinWarps>(p, smem);
   named_bar_sync(1, kBinWarps * 32);
+  if (threadIdx.x == 0) mbar_arrive(x_ready_bar(bar_full));
 
   const int g = lane >> 2, q = lane & 3;
   const bool bcol = g < p.m;
@@ -752,6 +770,7 @@ __global__ void __launch_bounds__(threads_for(kTerWarps), 1)
   pdl_wait();  // x is written by earlier work on the stream
   build_ternary_xtable<false>(p, smem);
   named_bar_sync(1, kTerWarps * 32);
+  if (threadIdx.x == 0) mbar_arrive(x_ready_bar(bar_full));
   int s = 0, tcount = 0;
   uint32_t ph = 0;
   bool alive = true;
@@ -997,6 +1016,7 @@ __global__ void __launch_bounds__(threads_for(kBinWarps), 1)
   pdl_wait();  // x is written by earlier work on the stream
   build_nibble_tables(p, tab);
   named_bar_sync(1, kBinWarps * 32);
+  if (threadIdx.x == 0) mbar_arrive(x_ready_bar(bar_full));
 
   const int r = lane & 15, h = lane >> 4;
   const int pw = p.pitch >> 2;
@@ -1108,7 +1128,7 @@ static bonsai_status gemv_prepare(const bonsai_weights* w, const uint16_t* x, in
   p.off_lut = off;   // at 0: the kernels rely on it (1024-byte aligned)
   if (ter) off = up(off + (m > kTerMaxTokens ? kLutBytes8 : kLutBytes), 128);
   else if (lut) off = up(off + ((p.G + 1) / 2) * 2 * kLutGroupBytes, 128);
-  p.off_bar = off;   off = up(off + 8 * (2 * kMaxStages + 4), 128);
+  p.off_bar = off;   off = up(off + 8 * kBarriers, 128);
   const int warps = ter ? kTerWarps : kBinWarps;
   p.red_cols = m;
   p.off_red = off;   off = up(off + 2 * warps * 16 * p.red_cols * 4, 128);
@@ -1231,7 +1251,7 @@ static bonsai_status gemv_plan_prepare(const bonsai_decode_step* steps, int64_t 
   // slots, the largest x table, a ring of the largest stages
   int off = 0;
   g.off_lut = off;   off = up(off + kLutBytes, 128);
-  g.off_bar = off;   off = up(off + 8 * (2 * kMaxStages + 4), 128);
+  g.off_bar = off;   off = up(off + 8 * kBarriers, 128);
   g.red_cols = 1;
   g.off_red = off;   off = up(off + 2 * kTerWarps * 16 * 4, 128);
   g.off_t = off;
