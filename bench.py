@@ -949,10 +949,12 @@ class HadamardWorkload:
 
 
 class XnorWorkload:
+    """+-1 x +-1 product, D (int32) and Y (FP16): on the tensor cores, or
+    (popc=True) the literal XOR + popcount kernel."""
     kind = "xnor"
 
-    def __init__(self, name, m=512, n=4096, k=4096):
-        self.name, self.m, self.n, self.k = name, m, n, k
+    def __init__(self, name, m=512, n=4096, k=4096, popc=False):
+        self.name, self.m, self.n, self.k, self.popc = name, m, n, k, popc
 
     def words(self):
         return self.m * self.n * (self.k // 32)
@@ -975,7 +977,7 @@ class XnorWorkload:
 
     def call(self):
         import sub_bit_weight_binary_b300 as sb
-        sb.bonsai_xnor_gemm(self.a, self.a_s, self.w, self.d, self.y)
+        sb.bonsai_xnor_gemm(self.a, self.a_s, self.w, self.d, self.y, popc=self.popc)
 
     measure = GemmWorkload.measure
 
@@ -983,6 +985,15 @@ class XnorWorkload:
         return 2.0 * self.m * self.n * self.k * steps / (ms / 1e3) / 1e12, "bit-TOPS"
 
     def roofline(self, r, pk, mhz=None):
+        if not self.popc:
+            # D and Y are two FP16 MMAs over the same operands: 2 x 2*M*N*K
+            # tensor FLOP per step against the dense FP16 (= bf16) peak
+            a = 4.0 * self.m * self.n * self.k / (r["kernel_ms"] / 1e3) / 1e12
+            return {"bound": "tensor", "kernel": "xnor_tc_kernel", "achieved": round(a, 1),
+                    "peak": pk["bf16"], "unit": "TFLOP/s", "frac": round(a / pk["bf16"], 4),
+                    "traffic": profiled_traffic("xnor_tc_m512_k4096_n4096.md"),
+                    "note": "FLOP = 2 outputs x 2*M*N*K on the FP16 tensor pipe",
+                    "peak_src": "%s dense bf16 cuBLAS burst (fp16 has the same dense rate)" % pk["src"]}
         mhz = mhz or pk["sm_max_mhz"] or 2032.0
         peak = POPC_PER_CLK_SM * 148 * mhz * 1e6 / 1e12  # T popc/s
         a = self.words() / (r["kernel_ms"] / 1e3) / 1e12
@@ -1041,7 +1052,7 @@ class XnorFp16Workload(XnorWorkload):
     def call(self):
         import sub_bit_weight_binary_b300 as sb
         self.binarize()
-        sb.bonsai_xnor_gemm(self.a, self.a_s, self.w, self.d, self.y)
+        sb.bonsai_xnor_gemm(self.a, self.a_s, self.w, self.d, self.y, popc=self.popc)
 
     def measure(self, steps, warmup, clocks=None):
         import torch
@@ -1106,7 +1117,9 @@ WORKLOADS = {
     "pp512_layer_ter": lambda ref=False: LayerGemmWorkload(2, 512, "prefill M=512, one decoder layer "
                                                  "(7 products, fused feed-forward), ternary"),
     "hadamard": lambda ref=False: HadamardWorkload("signed Hadamard rotation of x, M=512 K=5120, block 128"),
-    "xnor": lambda ref=False: XnorWorkload("XNOR-popcount GEMM M=512 K=4096 N=4096"),
+    "xnor": lambda ref=False: XnorWorkload("XNOR-popcount GEMM M=512 K=4096 N=4096 (tensor cores)"),
+    "xnor_popc": lambda ref=False: XnorWorkload(
+        "XNOR-popcount GEMM M=512 K=4096 N=4096 (XOR + popcount kernel)", popc=True),
     "xnor_fp16": lambda ref=False: XnorFp16Workload(
         "FP16 activations binarised, then XNOR-popcount GEMM M=512 K=4096 N=4096"),
 }
@@ -1116,7 +1129,7 @@ SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("ter_gemv_m5"
              ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
              ("gemm4096_ter", 5, 2), ("layer_bin", 128, 3), ("layer_ter", 128, 3),
              ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("hadamard", 200, 10),
-             ("xnor", 20, 3),
+             ("xnor", 20, 3), ("xnor_popc", 20, 3),
              ("xnor_fp16", 20, 3)]
 SECONDARY_FIELDS = ["workload", "value", "unit", "ms_per_step", "gpu_launches", "roofline_bound",
                     "roofline_achieved", "roofline_peak", "roofline_frac", "roofline_traffic",

@@ -303,7 +303,12 @@ bonsai_status bonsai_gemm_swiglu_ws(const bonsai_weights* w, const uint16_t* x,
                                     int64_t workspace_bytes, bonsai_stream stream);
 
 /* XNOR-popcount product of +-1 activations with +-1 weights ("1-bit 嘅數學":
- * binary GEMM via XOR + popcount).
+ * binary GEMM via XOR + popcount). bonsai_xnor_gemm computes it on the
+ * tensor cores: +-1 codes (and +-s, the scale times a code) are exact FP16
+ * operands and every sum of up to 2^24 products of +-1 is exact in the FP32
+ * accumulator, so D equals k - 2*popc(a XOR w) bit for bit; Y's FP32 sum
+ * rounds once to FP16 after the a_scale product. bonsai_xnor_gemm_popc is
+ * the literal XOR + popcount kernel (same arguments, same results).
  *   a_bits  device uint32 [m][k/32], same bit layout as BINARY weights
  *           (bit 1 = +1); row stride k/32 words.
  *   a_scale device FP16 [m], one scale per activation row.
@@ -317,6 +322,10 @@ bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale,
                                int64_t m, const bonsai_weights* w,
                                int32_t* d_out, uint16_t* y_out,
                                bonsai_stream stream);
+bonsai_status bonsai_xnor_gemm_popc(const uint32_t* a_bits, const uint16_t* a_scale,
+                                    int64_t m, const bonsai_weights* w,
+                                    int32_t* d_out, uint16_t* y_out,
+                                    bonsai_stream stream);
 
 /* Activation binarisation: the +-1 A operand of bonsai_xnor_gemm, made from
  * FP16 activation rows in one pass over x. The pages ("1-bit 嘅數學") use

@@ -92,6 +92,8 @@ def lib():
         L.bonsai_gemm_swiglu_ws.restype = S
         L.bonsai_xnor_gemm.argtypes = [P, P, I64, W, P, P, P]
         L.bonsai_xnor_gemm.restype = S
+        L.bonsai_xnor_gemm_popc.argtypes = [P, P, I64, W, P, P, P]
+        L.bonsai_xnor_gemm_popc.restype = S
         L.bonsai_binarize_activations.argtypes = [P, I64, I64, P, P, P]
         L.bonsai_binarize_activations.restype = S
         L.bonsai_hadamard.argtypes = [P, I64, I64, C.c_int32, P, P, P]
@@ -352,14 +354,18 @@ def interleave_gate_up(gate, up):
     return np.concatenate([g, u], axis=1).reshape((2 * f,) + rest)
 
 
-def bonsai_xnor_gemm(a_bits, a_scale, w: Weights, d_out=None, y_out=None, stream=None):
+def bonsai_xnor_gemm(a_bits, a_scale, w: Weights, d_out=None, y_out=None, stream=None,
+                     popc=False):
+    """D = a . w^T (exact int32) and/or Y (FP16) for +-1 bits; tensor cores,
+    or the literal XOR + popcount kernel with popc=True."""
     import torch
     ws = w.c_struct()
-    _ok(lib().bonsai_xnor_gemm(_ptr(a_bits, (torch.int32, torch.uint8), "a_bits"),
-                               _ptr(a_scale, (torch.float16,), "a_scale"), a_bits.shape[0],
-                               C.byref(ws), _ptr(d_out, (torch.int32,), "d_out"),
-                               _ptr(y_out, (torch.float16,), "y_out"), _stream(stream)),
-        "bonsai_xnor_gemm")
+    fn = lib().bonsai_xnor_gemm_popc if popc else lib().bonsai_xnor_gemm
+    _ok(fn(_ptr(a_bits, (torch.int32, torch.uint8), "a_bits"),
+           _ptr(a_scale, (torch.float16,), "a_scale"), a_bits.shape[0],
+           C.byref(ws), _ptr(d_out, (torch.int32,), "d_out"),
+           _ptr(y_out, (torch.float16,), "y_out"), _stream(stream)),
+        "bonsai_xnor_gemm_popc" if popc else "bonsai_xnor_gemm")
 
 
 def bonsai_binarize_activations(x, a_bits, a_scale, stream=None):

@@ -18,6 +18,8 @@ bonsai_status gemm_launch(const bonsai_weights*, const uint16_t*, int64_t, uint1
 int64_t gemm_workspace_bytes(const bonsai_weights*, int64_t);
 bonsai_status xnor_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
                           int32_t*, uint16_t*, cudaStream_t);
+bonsai_status xnor_tc_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
+                             int32_t*, uint16_t*, cudaStream_t);
 bonsai_status binarize_launch(const uint16_t*, int64_t, int64_t, uint32_t*, uint16_t*,
                               cudaStream_t);
 bonsai_status hadamard_launch(const uint16_t*, int64_t, int64_t, int32_t, const uint32_t*,
@@ -32,6 +34,7 @@ unsigned int read_clear_status_pack();
 unsigned int read_clear_status_gemv();
 unsigned int read_clear_status_gemm();
 unsigned int read_clear_status_xnor();
+unsigned int read_clear_status_xnor_tc();
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -326,9 +329,8 @@ bonsai_status bonsai_gemm_swiglu_ws(const bonsai_weights* w, const uint16_t* x, 
   return gemm_common(w, x, m, h, true, workspace, workspace_bytes, stream);
 }
 
-bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,
-                               const bonsai_weights* w, int32_t* d_out, uint16_t* y_out,
-                               bonsai_stream stream) {
+static bonsai_status check_xnor(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,
+                                const bonsai_weights* w, int32_t* d_out, uint16_t* y_out) {
   bonsai_status st = check_weights(w);
   if (st != BONSAI_OK) return st;
   if (w->format != BONSAI_FMT_BINARY) return BONSAI_ERR_FORMAT;
@@ -337,6 +339,22 @@ bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale, 
   if (!aligned16(a_bits) || !aligned16(a_scale) || (d_out && !aligned16(d_out)) ||
       (y_out && !aligned16(y_out)))
     return BONSAI_ERR_ALIGN;
+  return BONSAI_OK;
+}
+
+bonsai_status bonsai_xnor_gemm(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,
+                               const bonsai_weights* w, int32_t* d_out, uint16_t* y_out,
+                               bonsai_stream stream) {
+  const bonsai_status st = check_xnor(a_bits, a_scale, m, w, d_out, y_out);
+  if (st != BONSAI_OK) return st;
+  return xnor_tc_launch(a_bits, a_scale, m, w, d_out, y_out, stream);
+}
+
+bonsai_status bonsai_xnor_gemm_popc(const uint32_t* a_bits, const uint16_t* a_scale, int64_t m,
+                                    const bonsai_weights* w, int32_t* d_out, uint16_t* y_out,
+                                    bonsai_stream stream) {
+  const bonsai_status st = check_xnor(a_bits, a_scale, m, w, d_out, y_out);
+  if (st != BONSAI_OK) return st;
   return xnor_launch(a_bits, a_scale, m, w, d_out, y_out, stream);
 }
 
@@ -424,9 +442,9 @@ bonsai_status bonsai_selftest_wait_timeout(uint64_t limit_ns, bonsai_stream stre
 
 bonsai_status bonsai_check_async(bonsai_stream stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return BONSAI_ERR_CUDA;
-  const unsigned int codes[5] = {read_clear_status_pack(), read_clear_status_gemv(),
+  const unsigned int codes[6] = {read_clear_status_pack(), read_clear_status_gemv(),
                                  read_clear_status_gemm(), read_clear_status_xnor(),
-                                 read_clear_status_selftest()};
+                                 read_clear_status_xnor_tc(), read_clear_status_selftest()};
   if (cudaGetLastError() != cudaSuccess) return BONSAI_ERR_CUDA;
   for (unsigned int c : codes)
     if (c != 0) return static_cast<bonsai_status>(c);

@@ -375,14 +375,17 @@ def test_gemm_prefill_workload_sampled(fmt, m):
 
 
 # --------------------------------------------------------------------- XNOR
-@pytest.mark.parametrize("m,n,k", [(64, 256, 4096), (70, 100, 640), (1, 1, 128), (130, 65, 1024)])
-def test_xnor_full(m, n, k):
+# popc=False: the tensor-core kernel; True: the literal XOR + popcount kernel
+@pytest.mark.parametrize("popc", [False, True])
+@pytest.mark.parametrize("m,n,k", [(64, 256, 4096), (70, 100, 640), (1, 1, 128), (130, 65, 1024),
+                                   (300, 260, 2048), (129, 129, 128)])
+def test_xnor_full(m, n, k, popc):
     t = torch()
     a_bits, a_s, w_bits, s = synth.gen_xnor_inputs(90 + m, m, n, k)
     w = sb.Weights(BIN, n, k, dev(w_bits.view(np.uint8).reshape(n, -1)), dev(s))
     d = Guarded((m, n), t.int32)
     y = Guarded((m, n), t.float16)
-    sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, d.t, y.t)
+    sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, d.t, y.t, popc=popc)
     assert sb.bonsai_check_async() == 0
     d_ref, y_ref, nrm = oracle.xnor(a_bits, a_s, w_bits, s, k)
     assert np.array_equal(host(d.t).astype(np.int64), d_ref)
@@ -391,21 +394,29 @@ def test_xnor_full(m, n, k):
     y.check()
 
 
-def test_xnor_workload():
+@pytest.mark.parametrize("popc", [False, True])
+def test_xnor_workload(popc):
     """XNOR workload M=512, K=4096, N=4096: D sampled against the oracle and
-    every D checked against the popcount route of numpy; Y sampled."""
+    every D checked against the popcount route of numpy; Y sampled. Both
+    kernels (tensor cores, XOR + popcount)."""
     t = torch()
     m, n, k = 512, 4096, 4096
     a_bits, a_s, w_bits, s = synth.gen_xnor_inputs(95, m, n, k)
     w = sb.Weights(BIN, n, k, dev(w_bits.view(np.uint8).reshape(n, -1)), dev(s))
     d = Guarded((m, n), t.int32)
     y = Guarded((m, n), t.float16)
-    sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, d.t, y.t)
+    sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, d.t, y.t, popc=popc)
     d_only = t.empty((m, n), dtype=t.int32, device="cuda")
-    sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, d_only, None)
+    sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, d_only, None, popc=popc)
     y_only = t.empty((m, n), dtype=t.float16, device="cuda")
-    sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, None, y_only)
+    sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, None, y_only, popc=popc)
     assert sb.bonsai_check_async() == 0
+    if not popc:  # the two kernels agree: D bit for bit, Y within the sum of both bounds
+        d_p = t.empty((m, n), dtype=t.int32, device="cuda")
+        y_p = t.empty((m, n), dtype=t.float16, device="cuda")
+        sb.bonsai_xnor_gemm(dev(a_bits.view(np.int32)), dev(a_s), w, d_p, y_p, popc=True)
+        assert sb.bonsai_check_async() == 0
+        assert t.equal(d.t, d_p)
     dg = host(d.t)
     assert np.array_equal(dg, host(d_only))
     assert np.array_equal(host(y.t), host(y_only))
