@@ -92,7 +92,7 @@ struct Params {
 };
 
 // A tile is split over at most kMaxPartners + 1 stream-K ranges.
-constexpr int kMaxPartners = 20;
+constexpr int kMaxPartners = 12;
 
 // ---- the work of a CTA -----------------------------------------------------
 // Segments: its whole tiles blockIdx.x + i * gridDim.x below dp, then at most
@@ -139,6 +139,15 @@ struct Segs {
     }
   }
 };
+
+// Number of CTAs after this one whose first stream-K range lies in `tile`
+// (the partners whose partial tiles this CTA's finishing range adds).
+__device__ __forceinline__ int sk_partners(const Params& p, int tile) {
+  const int t_end = (tile - p.dp + 1) * p.nk;
+  int np = 0;
+  while ((int)blockIdx.x + 1 + np < p.sk_ctas && sk_start(p, (int)blockIdx.x + 1 + np) < t_end) ++np;
+  return np;
+}
 
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* a) {
   unsigned int v;
@@ -284,6 +293,95 @@ __device__ __forceinline__ int k_at(const Params& p, int tile, int j) {
   return k < p.nk ? k : k - p.nk;
 }
 
+// Finishing a cut tile. Its range holds k-step 0 and is its CTA's last
+// segment, so all the CTA's MMAs have completed, the A and B rings are idle
+// and so are the dequantiser warps. Three groups of four warps (the epilogue
+// warps, then the two dequantiser groups), each covering the 128
+// tensor-memory lanes, share the tile's 16-token steps round robin. The np
+// partners' partial tiles come into the rings by bulk copies, a group of
+// steps of every partner into one of two 96 KB buffers, so the next group is
+// copied while one is added (measured: ~4 us of copies and ~6 us of adds and
+// FP16 stores at 512 tokens when the 4 epilogue warps did it alone). The sum
+// is this CTA's accumulator, then the partners in CTA order. `issuer` (one
+// thread) issues the copies; fin_bar has 12 arrivals per group.
+constexpr int kFinishBufSteps = 12;  // 16-token steps of one partner per 96 KB buffer
+__device__ void finish_cut_tile(const Params& p, int tile, int np, uint32_t acc, uint32_t ring,
+                                uint32_t stg_bar, uint32_t fin_bar, int grp, bool issuer) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;          // tensor-memory lanes 32 quarter ..
+  const int row = 32 * quarter + lane;   // feature row of the tile
+  const int n0 = (tile / p.tok_tiles) * BM, m0 = (tile % p.tok_tiles) * BN;
+  const int steps = (p.m - m0 + 15) / 16 < BN / 16 ? (p.m - m0 + 15) / 16 : BN / 16;
+  const uint32_t tl = acc + ((uint32_t)(32 * quarter) << 16);
+  constexpr int STEP_BYTES = BM * 16 * 4;  // one partner, one step: 8 KB
+  const int gsz = np > 0 ? (kFinishBufSteps / np < steps ? kFinishBufSteps / np : steps) : steps;
+  const int groups = (steps + gsz - 1) / gsz;
+  auto copy_group = [&](int j) {
+    const int s0 = j * gsz, gn = steps - s0 < gsz ? steps - s0 : gsz;
+    const uint32_t buf = ring + (j & 1) * kFinishBufSteps * STEP_BYTES, bar = stg_bar + 8 * (j & 1);
+    mbar_arrive_expect_tx(bar, (uint32_t)(np * gn * STEP_BYTES));
+    for (int q = 0; q < np; ++q)
+      for (int st = 0; st < gn; ++st)
+        bulk_g2s(buf + (q * gsz + st) * STEP_BYTES,
+                 p.ws + (size_t)(blockIdx.x + 1 + q) * (BM * BN) + (size_t)(s0 + st) * (BM * 16),
+                 STEP_BYTES, bar, policy_evict_first());
+  };
+  if (np > 0 && issuer) {
+    copy_group(0);
+    if (groups > 1) copy_group(1);
+  }
+  const int feat = n0 + row;
+  const bool fok = feat < p.n;
+  for (int j = 0; j < groups; ++j) {
+    const int s0 = j * gsz, gn = steps - s0 < gsz ? steps - s0 : gsz;
+    const uint32_t buf = ring + (j & 1) * kFinishBufSteps * STEP_BYTES;
+    if (np > 0 && !mbar_wait(stg_bar + 8 * (j & 1), (j >> 1) & 1)) set_status(BONSAI_ERR_TIMEOUT);
+    for (int st = s0 + ((grp - s0 % 3) + 3) % 3; st < s0 + gn; st += 3) {  // steps = grp mod 3
+      uint32_t v[16];
+      TMEM_LD_16(tl + 16 * st, v);
+      tmem_ld_wait();
+      for (int q = 0; q < np; ++q) {
+        const uint32_t src = buf + (q * gsz + st - s0) * STEP_BYTES + row * 16;
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+          float4 f;
+          asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                       : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                       : "r"(src + i4 * BM * 16));
+          v[4 * i4] = __float_as_uint(__uint_as_float(v[4 * i4]) + f.x);
+          v[4 * i4 + 1] = __float_as_uint(__uint_as_float(v[4 * i4 + 1]) + f.y);
+          v[4 * i4 + 2] = __float_as_uint(__uint_as_float(v[4 * i4 + 2]) + f.z);
+          v[4 * i4 + 3] = __float_as_uint(__uint_as_float(v[4 * i4 + 3]) + f.w);
+        }
+      }
+      if (p.swiglu) {
+        const int hcol = (feat >> 4) * 8 + (feat & 7);
+#pragma unroll
+        for (int j2 = 0; j2 < 16; ++j2) {
+          const float g = __uint_as_float(v[j2]);
+          const float u = __shfl_down_sync(0xFFFFFFFFu, g, 8);
+          const int tok = m0 + 16 * st + j2;
+          if (fok && !(lane & 8) && tok < p.m)
+            p.y[(size_t)tok * p.y_stride + hcol] = __float2half_rn(silu(g) * u);
+        }
+      } else if (fok) {
+#pragma unroll
+        for (int j2 = 0; j2 < 16; ++j2) {
+          const int tok = m0 + 16 * st + j2;
+          if (tok < p.m) p.y[(size_t)tok * p.y_stride + feat] = __float2half_rn(__uint_as_float(v[j2]));
+        }
+      }
+    }
+    if (np > 0) {  // every warp done with this buffer before its next copy
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fin_bar);
+      if (!mbar_wait(fin_bar, j & 1)) set_status(BONSAI_ERR_TIMEOUT);
+      if (issuer && j + 2 < groups) copy_group(j + 2);
+    }
+  }
+}
+
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ Params p) {
@@ -310,7 +408,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t drain = acc_empty + 16;
   const uint32_t tmem_slot = drain + 8;
   const uint32_t epi_bar = sBar + 192;  // the epilogue warps' own barrier (stream-K)
-  const uint32_t stg_bar = sBar + 200;  // partial tiles copied into the idle rings
+  const uint32_t stg_bar = sBar + 200;  // two: partial tiles copied into the idle rings
+  const uint32_t fin_bar = sBar + 216;  // the 12 warps that finish a cut tile
   static_assert(8 * (2 * A_STAGES + 2 * NB + 5) + 4 <= 192, "barriers overlap epi_bar");
 
   if ((sA & 1023u) != 0) {  // the swizzle atoms need 1024-byte alignment
@@ -333,6 +432,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(drain, 1);
     mbar_init(epi_bar, 4);
     mbar_init(stg_bar, 1);
+    mbar_init(stg_bar + 8, 1);
+    mbar_init(fin_bar, 12);
     fence_barrier_init();
   }
   if (FMT == BONSAI_FMT_TERNARY && warp >= W_DQ) {
@@ -492,10 +593,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool partial = sk && j0 > 0;
       int np = 0;
       if (sk && !partial) {
-        const int t_end = (tile - p.dp + 1) * p.nk;
-        while ((int)blockIdx.x + 1 + np < p.sk_ctas &&
-               sk_start(p, (int)blockIdx.x + 1 + np) < t_end)
-          ++np;
+        np = sk_partners(p, tile);
         if (np > kMaxPartners) {  // the host keeps ranges long enough for this never to happen
           if (et == 0) set_status(BONSAI_ERR_UNSUPPORTED);
           np = kMaxPartners;
@@ -540,71 +638,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty + 8 * a);
           } else {
-            const int feat = n0 + 32 * e + lane;
-            const bool fok = feat < p.n;
-            constexpr int RING = A_STAGES * A_BYTES + B_STAGES * B_BYTES;
-            static_assert(RING >= 24 * STEP_BYTES, "the rings hold 24 steps");
-            // steps per group: np partners x group <= 24 steps
-            const int grp = np > 0 ? (24 / np < steps ? 24 / np : steps) : steps;
-            static_assert(kMaxPartners <= 24, "one step of every partner fits the rings");
-            uint32_t gphase = 0;
-            for (int s0 = 0; s0 < steps; s0 += grp) {
-              const int gn = steps - s0 < grp ? steps - s0 : grp;
-              if (np > 0) {
-                if (et == 0) {
-                  mbar_arrive_expect_tx(stg_bar, (uint32_t)(np * gn * STEP_BYTES));
-                  for (int q = 0; q < np; ++q)
-                    for (int st = 0; st < gn; ++st)
-                      bulk_g2s(sA + (q * grp + st) * STEP_BYTES, part_at(blockIdx.x + 1 + q, s0 + st),
-                               STEP_BYTES, stg_bar, policy_evict_first());
-                }
-                if (!mbar_wait(stg_bar, gphase & 1)) set_status(BONSAI_ERR_TIMEOUT);
-                ++gphase;
-              }
-              for (int st = s0; st < s0 + gn; ++st) {
-                uint32_t v[16];
-                TMEM_LD_16(tl + 16 * st, v);
-                tmem_ld_wait();
-                if (st == steps - 1) {
-                  tc_fence_before();
-                  __syncwarp();
-                  if (lane == 0) mbar_arrive(acc_empty + 8 * a);
-                }
-                for (int q = 0; q < np; ++q) {
-                  const uint32_t src = sA + (q * grp + st - s0) * STEP_BYTES + et * 16;
-#pragma unroll
-                  for (int i4 = 0; i4 < 4; ++i4) {
-                    float4 f;
-                    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                                 : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
-                                 : "r"(src + i4 * BM * 16));
-                    v[4 * i4] = __float_as_uint(__uint_as_float(v[4 * i4]) + f.x);
-                    v[4 * i4 + 1] = __float_as_uint(__uint_as_float(v[4 * i4 + 1]) + f.y);
-                    v[4 * i4 + 2] = __float_as_uint(__uint_as_float(v[4 * i4 + 2]) + f.z);
-                    v[4 * i4 + 3] = __float_as_uint(__uint_as_float(v[4 * i4 + 3]) + f.w);
-                  }
-                }
-                if (p.swiglu) {
-                  const int hcol = (feat >> 4) * 8 + (feat & 7);
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    const float g = __uint_as_float(v[j]);
-                    const float u = __shfl_down_sync(0xFFFFFFFFu, g, 8);
-                    const int tok = m0 + 16 * st + j;
-                    if (fok && !(lane & 8) && tok < p.m)
-                      p.y[(size_t)tok * p.y_stride + hcol] = __float2half_rn(silu(g) * u);
-                  }
-                } else if (fok) {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    const int tok = m0 + 16 * st + j;
-                    if (tok < p.m)
-                      p.y[(size_t)tok * p.y_stride + feat] = __float2half_rn(__uint_as_float(v[j]));
-                  }
-                }
-              }
-              if (np > 0 && s0 + gn < steps) epi_sync();  // every read of the group before the next copy
-            }
+            static_assert(A_STAGES * A_BYTES + B_STAGES * B_BYTES >= 2 * kFinishBufSteps * STEP_BYTES,
+                          "two finishing buffers fit the rings");
+            finish_cut_tile(p, tile, np, tmem_base + a * 256, sA, stg_bar, fin_bar, 0, et == 0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + 8 * a);
           }
         }
       }
@@ -775,6 +814,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
         __syncwarp();
         if (lane == 0) mbar_arrive(full_a + 8 * s);
+      }
+    }
+    if constexpr (MODE == NARROW) {
+      // no k-steps left: help finish this CTA's cut tile (its last segment)
+      if (ok && sg.count > sg.whole) {
+        const int i = sg.count - 1;
+        int tile, j0, j1;
+        sg.at(p, i, tile, j0, j1);
+        if (j0 == 0) {
+          int np = sk_partners(p, tile);
+          np = np > kMaxPartners ? kMaxPartners : np;
+          const uint32_t a = (uint32_t)i % C::NACC, use = (uint32_t)i / C::NACC;
+          if (!mbar_wait(acc_full + 8 * a, use & 1)) {
+            set_status(BONSAI_ERR_TIMEOUT);
+          } else {
+            tc_fence_after();
+            finish_cut_tile(p, tile, np, tmem_base + a * 256, sA, stg_bar, fin_bar, 1 + (dq >> 2),
+                            false);
+          }
+        }
       }
     }
   }
