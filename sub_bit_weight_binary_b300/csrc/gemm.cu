@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // Stream-K schedule of `tiles` 128 x 256 tiles of nk k-steps on `sms` CTAs:
 // the whole waves stay data-parallel; when the plain schedule would leave
-// more than an eighth of the SM time idle, the last wave is cut into equal
+// more than a sixteenth of the SM time idle, the last wave is cut into equal
 // k-step ranges of at least kMinSkSteps, each CTA's range within two
 // consecutive tiles. (A finishing range adds the others' partial tiles at
 // the end of the kernel, ~10 us measured at 512 tokens, so an almost full
@@ -863,7 +863,7 @@ static SkPlan sk_plan(long long tiles, int nk, int sms) {
   SkPlan s;
   const long long rest = tiles % sms;
   const long long waves = (tiles + sms - 1) / sms;
-  if (rest == 0 || tiles * 8 >= 7 * waves * sms) return s;
+  if (rest == 0 || tiles * 16 >= 15 * waves * sms) return s;
   const long long iters = rest * nk;
   if (iters * sms >= (1LL << 31)) return s;  // the device splits ranges in 32-bit
   long long ctas = iters / kMinSkSteps;
