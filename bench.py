@@ -708,11 +708,14 @@ class SweepWorkload:
 
 
 class GemmWorkload:
-    """Prefill / DiT product on the tensor cores, K=5120, N=17408."""
+    """Prefill / DiT product on the tensor cores (K=5120, N=17408 unless
+    given); stream_k: through bonsai_gemm_ws with a workspace allocated at
+    setup (the stream-K schedule, where the shape takes it)."""
     kind = "gemm"
 
-    def __init__(self, fmt, m, name, n=17408, k=5120):
+    def __init__(self, fmt, m, name, n=17408, k=5120, stream_k=False):
         self.fmt, self.m, self.n, self.k, self.name = fmt, m, n, k, name
+        self.stream_k = stream_k
 
     def flops(self):
         return 2.0 * self.m * self.n * self.k
@@ -726,13 +729,17 @@ class GemmWorkload:
         self.w = make_weights(self.fmt, self.n, self.k, seed, tid, synth.TID_SCALES, 0)
         self.x = torch.from_numpy(synth.gen_x(seed, self.m, self.k).view(np.float16)).cuda()
         self.y = torch.empty((self.m, self.n), dtype=torch.float16, device="cuda")
+        self.work = sb.gemm_workspace(self.w, self.m) if self.stream_k else None
         self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         torch.cuda.synchronize()
         sb.check()
 
     def call(self):
         import sub_bit_weight_binary_b300 as sb
-        sb.bonsai_gemm(self.w, self.x, self.y)
+        if self.stream_k:
+            sb.bonsai_gemm_ws(self.w, self.x, self.y, self.work)
+        else:
+            sb.bonsai_gemm(self.w, self.x, self.y)
 
     def measure(self, steps, warmup, clocks=None):
         """Per-step event pairs around one replay of a CUDA graph that holds
@@ -769,13 +776,14 @@ class GemmWorkload:
                     "ternary" if self.fmt == 2 else "binary"),
                 "achieved": round(a, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
                 "frac": round(a / pk["bf16"], 4),
-                "traffic": profiled_traffic("gemm_%s_m%d_k5120_n17408.md" % (
-                    "ternary" if self.fmt == 2 else "binary", self.m)),
+                "traffic": profiled_traffic("gemm_%s_m%d_k%d_n%d.md" % (
+                    "ternary" if self.fmt == 2 else "binary", self.m, self.k, self.n)),
                 "peak_src": "%s dense bf16 cuBLAS burst (fp16 has the same dense rate)" % pk["src"]}
 
     def config(self):
         return {"workload": self.name, "m": self.m, "k": self.k, "n": self.n,
                 "format": "ternary" if self.fmt == 2 else "binary",
+                "stream_k": bool(self.stream_k and self.work is not None),
                 "timing": "per-step CUDA events", "l2": "flushed between steps (512 MB write)"}
 
 
@@ -1105,6 +1113,12 @@ WORKLOADS = {
     "gemm512_ter": lambda ref=False: GemmWorkload(2, 512, "prefill GEMM M=512 K=5120 N=17408, ternary"),
     "gemm4096_bin": lambda ref=False: GemmWorkload(1, 4096, "DiT GEMM M=4096 K=5120 N=17408, binary"),
     "gemm4096_ter": lambda ref=False: GemmWorkload(2, 4096, "DiT GEMM M=4096 K=5120 N=17408, ternary"),
+    "gemm512_down_bin": lambda ref=False: GemmWorkload(
+        1, 512, "prefill down product M=512 K=17408 N=5120, binary (stream-K)", n=5120, k=17408,
+        stream_k=True),
+    "gemm512_down_ter": lambda ref=False: GemmWorkload(
+        2, 512, "prefill down product M=512 K=17408 N=5120, ternary (stream-K)", n=5120, k=17408,
+        stream_k=True),
     "layer_bin": lambda ref=False: SweepWorkload(1, "64-layer decode, fused feed-forward, binary, batch 1",
                                        fused=True),
     "layer_ter": lambda ref=False: SweepWorkload(2, "64-layer decode, fused feed-forward, ternary, batch 1",
@@ -1127,7 +1141,8 @@ SECONDARY = [("bin_gemv_1k", 20000, 50), ("bin_gemv", 20000, 50), ("ter_gemv_m5"
              ("bin_gemv_m5", 2000, 20), ("sweep_bin", 128, 3), ("sweep_ter", 128, 3),
              ("sweep_ter_plan", 128, 3), ("layer_ter_plan", 128, 3),
              ("gemm512_bin", 20, 3), ("gemm512_ter", 20, 3), ("gemm4096_bin", 5, 2),
-             ("gemm4096_ter", 5, 2), ("layer_bin", 128, 3), ("layer_ter", 128, 3),
+             ("gemm4096_ter", 5, 2), ("gemm512_down_bin", 20, 3), ("gemm512_down_ter", 20, 3),
+             ("layer_bin", 128, 3), ("layer_ter", 128, 3),
              ("pp512_layer_bin", 10, 3), ("pp512_layer_ter", 10, 3), ("hadamard", 200, 10),
              ("xnor", 20, 3), ("xnor_popc", 20, 3),
              ("xnor_fp16", 20, 3)]
