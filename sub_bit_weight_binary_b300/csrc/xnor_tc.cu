@@ -49,7 +49,7 @@ constexpr int TN = 128;       // tokens per tile (MMA N)
 constexpr int BK = 64;        // codes per k-step: one 128-byte swizzle row of FP16
 constexpr int THREADS = 512;
 constexpr int A_STAGES = 8;   // in tensor memory: 8 of 32 columns (one output), 4 of 64 (both)
-constexpr int B_STAGES = 6;   // in shared memory, 16 KB each
+constexpr int B_STAGES = A_STAGES;  // in shared memory, 16 KB each; one ring index for A and B
 constexpr int B_BYTES = TN * BK * 2;
 constexpr int TMEM_COLS = 512;
 constexpr int COL_D = 0, COL_Y = TN, COL_A = 2 * TN;
@@ -126,11 +126,15 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sB = (raw + 1023u) & ~1023u;
   const uint32_t sBar = sB + B_STAGES * B_BYTES;
-  const uint32_t full_a = sBar, empty_a = full_a + 8 * A_STAGES;
-  const uint32_t full_b = empty_a + 8 * A_STAGES, empty_b = full_b + 8 * B_STAGES;
-  const uint32_t acc_full = empty_b + 8 * B_STAGES, acc_empty = acc_full + 8;
+  // One ring for both operands (stage s of the A stages in tensor memory and
+  // of the B stages in shared memory hold the same k-step): full[s] gets the
+  // 4 weight-expander warps of the k-step's group and the 4 activation
+  // expanders, empty[s] one commit. One wait and one commit per k-step for
+  // the MMA thread (each commit costs ~85 cycles of its issue).
+  const uint32_t full = sBar, empty = full + 8 * A_STAGES;
+  const uint32_t acc_full = empty + 8 * A_STAGES, acc_empty = acc_full + 8;
   const uint32_t drain = acc_empty + 8, tmem_slot = drain + 8;
-  static_assert(8 * (2 * A_STAGES + 2 * B_STAGES + 3) + 4 <= 256, "barrier area");
+  static_assert(8 * (2 * A_STAGES + 3) + 4 <= 256, "barrier area");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool do_d = p.d != nullptr, do_y = p.y != nullptr;
   // A stages: 32 columns per wanted output (+-1 codes first, then +-s)
@@ -139,12 +143,8 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a_stages; ++s) {
-      mbar_init(full_a + 8 * s, 4);  // the 4 weight-expander warps of the k-step's group
-      mbar_init(empty_a + 8 * s, 1);
-    }
-    for (int s = 0; s < B_STAGES; ++s) {
-      mbar_init(full_b + 8 * s, 4);  // the 4 activation-expander (epilogue) warps
-      mbar_init(empty_b + 8 * s, 1);
+      mbar_init(full + 8 * s, 8);  // 4 weight expanders (the k-step's group) + 4 activation expanders
+      mbar_init(empty + 8 * s, 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
@@ -171,9 +171,8 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
         if (!mbar_wait(acc_empty, (it & 1) ^ 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
         tc_fence_after();
         for (int kk = 0; kk < p.nk; ++kk, ++ga, ++gb) {
-          const int sa = ga % a_stages, sb = gb % B_STAGES;
-          if (!mbar_wait(full_a + 8 * sa, (ga / a_stages) & 1) ||
-              !mbar_wait(full_b + 8 * sb, (gb / B_STAGES) & 1)) {
+          const int sa = ga % a_stages, sb = sa;
+          if (!mbar_wait(full + 8 * sa, (ga / a_stages) & 1)) {
             set_status(BONSAI_ERR_TIMEOUT);
             ok = false;
             break;
@@ -186,8 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
             if (do_d) mma_f16_ts(tmem_base + COL_D, a_u + 8 * k4, bd + 2 * k4, kIdesc, (kk | k4) != 0);
             if (do_y) mma_f16_ts(tmem_base + COL_Y, a_s + 8 * k4, bd + 2 * k4, kIdesc, (kk | k4) != 0);
           }
-          mma_commit(empty_a + 8 * sa);
-          mma_commit(empty_b + 8 * sb);
+          mma_commit(empty + 8 * sa);
         }
         if (ok) mma_commit(acc_full);
       }
@@ -235,7 +233,7 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
         for (int i = 0; i < W_AHEAD - 1; ++i) { ring_w[i] = ring_w[i + 1]; ring_s[i] = ring_s[i + 1]; }
         load(t_ld, k_ld, ring_w[W_AHEAD - 1], ring_s[W_AHEAD - 1]);
         advance();
-        if (!mbar_wait(empty_a + 8 * s, ((g / a_stages) & 1) ^ 1)) {
+        if (!mbar_wait(empty + 8 * s, ((g / a_stages) & 1) ^ 1)) {
           set_status(BONSAI_ERR_TIMEOUT);
           ok = false;
           break;
@@ -261,7 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(full_a + 8 * s);
+        if (lane == 0) mbar_arrive(full + 8 * s);
       }
     }
   } else if (warp >= W_EPI && warp < W_EPI + 4) {
@@ -289,8 +287,8 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
             if (kk >= p.nk) break;
             const uint2 bits = pre[i];
             pre[i] = real && kk + B_AHEAD < p.nk ? src[kk + B_AHEAD] : make_uint2(0u, 0u);
-            const int s = gb % B_STAGES;
-            if (!mbar_wait(empty_b + 8 * s, ((gb / B_STAGES) & 1) ^ 1)) {
+            const int s = gb % a_stages;
+            if (!mbar_wait(empty + 8 * s, ((gb / a_stages) & 1) ^ 1)) {
               set_status(BONSAI_ERR_TIMEOUT);
               ok = false;
               break;
@@ -304,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
             }
             fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
             __syncwarp();
-            if (lane == 0) mbar_arrive(full_b + 8 * s);
+            if (lane == 0) mbar_arrive(full + 8 * s);
             ++gb;
           }
         }
