@@ -382,6 +382,67 @@ __device__ void finish_cut_tile(const Params& p, int tile, int np, uint32_t acc,
   }
 }
 
+// Outputs of a whole tile from its TMEM accumulator (column a*256, feature
+// half f at +256 f): the 32-token chunks grp, grp + ngrp, ... of the tile,
+// read by this warp's lane quarter. On a CTA's last tile the epilogue warps
+// (grp 0) share the chunks with the two dequantiser groups, which have no
+// k-steps left (a tile's epilogue is otherwise exposed when no next tile
+// follows: the larger tiles' one accumulator, or the last wave). acc_empty
+// (not 0): arrived on after this warp's last TMEM load. Wide (ternary
+// 512-token) tiles do not take the help: with it the kernel rose from 110 to
+// 117 registers and the M=4096 product lost 2% (A/B on one GPU), more than
+// the M=512 product gained; out of line it cost 28%.
+template <int FM, int TT, int FHALVES>
+__device__ void store_tile(const Params& p, int tile, uint32_t tmem_base, uint32_t a, int grp,
+                           int ngrp, uint32_t acc_empty) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
+  const int n0 = (tile / p.tok_tiles) * FM, m0 = (tile % p.tok_tiles) * TT;
+  // column chunks that hold tokens (the MMAs wrote only the used halves)
+  const int chunks = (p.m - m0 + 31) / 32 < TT / 32 ? (p.m - m0 + 31) / 32 : TT / 32;
+  const int total = chunks * FHALVES;
+  const int last = grp < total ? grp + (total - 1 - grp) / ngrp * ngrp : -1;
+#pragma unroll 1
+  for (int cf = grp; cf < total; cf += ngrp) {
+    const int f = cf / chunks, c = cf - f * chunks;  // feature half, token chunk
+    const int feat = n0 + BM * f + 32 * quarter + lane;
+    const bool fok = feat < p.n;
+    uint32_t v[32];
+    TMEM_LD_32(tmem_base + ((uint32_t)(32 * quarter) << 16) + (a + f) * 256 + 32 * c, v);
+    tmem_ld_wait();
+    if (cf == last && acc_empty) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+    if (p.swiglu) {
+      // lanes 0-7 / 16-23 hold gate features, lanes 8-15 / 24-31 the up
+      // features of the same outputs (n % 16 == 0, so fok is uniform
+      // over each 16-lane block)
+      const int hcol = (feat >> 4) * 8 + (feat & 7);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float g = __uint_as_float(v[j]);
+        const float u = __shfl_down_sync(0xFFFFFFFFu, g, 8);
+        const int tok = m0 + 32 * c + j;
+        if (fok && !(lane & 8) && tok < p.m)
+          p.y[(size_t)tok * p.y_stride + hcol] = __float2half_rn(silu(g) * u);
+      }
+    } else if (fok) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int tok = m0 + 32 * c + j;
+        if (tok < p.m)
+          p.y[(size_t)tok * p.y_stride + feat] = __float2half_rn(__uint_as_float(v[j]));
+      }
+    }
+  }
+  if (last < 0 && acc_empty) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(acc_empty);
+  }
+}
+
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ Params p) {
@@ -410,6 +471,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t epi_bar = sBar + 192;  // the epilogue warps' own barrier (stream-K)
   const uint32_t stg_bar = sBar + 200;  // two: partial tiles copied into the idle rings
   const uint32_t fin_bar = sBar + 216;  // the 12 warps that finish a cut tile
+  // The epilogue warps arrive here once the CTA's last accumulator is
+  // complete; the dequantisers wait on it (once) before they help store it.
+  // They must not wait on acc_full themselves: they can finish their k-steps
+  // two accumulator phases ahead of the MMAs (short K), and a parity wait
+  // cannot tell those phases apart.
+  const uint32_t help_bar = sBar + 224;
   static_assert(8 * (2 * A_STAGES + 2 * NB + 5) + 4 <= 192, "barriers overlap epi_bar");
 
   if ((sA & 1023u) != 0) {  // the swizzle atoms need 1024-byte alignment
@@ -434,6 +501,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(stg_bar, 1);
     mbar_init(stg_bar + 8, 1);
     mbar_init(fin_bar, 12);
+    mbar_init(help_bar, 4);
     fence_barrier_init();
   }
   if (FMT == BONSAI_FMT_TERNARY && warp >= W_DQ) {
@@ -607,6 +675,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t a = it % C::NACC, use = it / C::NACC;
       if (!mbar_wait(acc_full + 8 * a, use & 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
       tc_fence_after();
+      if (i == sg.count - 1) {  // the last accumulator is complete: the dequantisers may help
+        __syncwarp();
+        if (lane == 0) mbar_arrive(help_bar);
+      }
       const int n0 = (tile / p.tok_tiles) * FM, m0 = (tile % p.tok_tiles) * TT;
       if constexpr (MODE == NARROW) {
         if (sk) {
@@ -648,43 +720,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (!(MODE == NARROW && sk)) {
-        // column chunks that hold tokens (the MMAs wrote only the used halves)
-        const int chunks = (p.m - m0 + 31) / 32 < TT / 32 ? (p.m - m0 + 31) / 32 : TT / 32;
-#pragma unroll 1
-        for (int cf = 0; cf < chunks * C::FHALVES; ++cf) {
-          const int f = cf / chunks, c = cf - f * chunks;  // feature half, token chunk
-          const int feat = n0 + BM * f + 32 * e + lane;
-          const bool fok = feat < p.n;
-          uint32_t v[32];
-          TMEM_LD_32(tmem_base + ((uint32_t)(32 * e) << 16) + (a + f) * 256 + 32 * c, v);
-          tmem_ld_wait();
-          if (cf == chunks * C::FHALVES - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty + 8 * a);
-          }
-          if (p.swiglu) {
-            // lanes 0-7 / 16-23 hold gate features, lanes 8-15 / 24-31 the up
-            // features of the same outputs (n % 16 == 0, so fok is uniform
-            // over each 16-lane block)
-            const int hcol = (feat >> 4) * 8 + (feat & 7);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float g = __uint_as_float(v[j]);
-              const float u = __shfl_down_sync(0xFFFFFFFFu, g, 8);
-              const int tok = m0 + 32 * c + j;
-              if (fok && !(lane & 8) && tok < p.m)
-                p.y[(size_t)tok * p.y_stride + hcol] = __float2half_rn(silu(g) * u);
-            }
-          } else if (fok) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int tok = m0 + 32 * c + j;
-              if (tok < p.m)
-                p.y[(size_t)tok * p.y_stride + feat] = __float2half_rn(__uint_as_float(v[j]));
-            }
-          }
-        }
+        // the last tile: with the dequantisers (not for wide tiles)
+        const int ngrp = MODE != WIDE && i == sg.count - 1 ? 3 : 1;
+        store_tile<FM, TT, C::FHALVES>(p, tile, tmem_base, a, 0, ngrp, acc_empty + 8 * a);
       }
       if (partial) {  // every row stored, then one count for the tile
         __threadfence();
@@ -816,8 +854,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(full_a + 8 * s);
       }
     }
+    // no k-steps left: help with this CTA's last tile (its stores, or finishing a cut tile)
+    if (ok && sg.count > 0) {
+      const int i = sg.count - 1;
+      int tile, j0, j1;
+      sg.at(p, i, tile, j0, j1);
+      const uint32_t a = (uint32_t)i % C::NACC;
+      if (MODE != WIDE && !(MODE == NARROW && i >= sg.whole)) {
+        if (!mbar_wait(help_bar, 0)) {
+          set_status(BONSAI_ERR_TIMEOUT);
+        } else {
+          tc_fence_after();
+          store_tile<FM, TT, C::FHALVES>(p, tile, tmem_base, a, 1 + (dq >> 2), 3, 0);
+        }
+      }
+    }
     if constexpr (MODE == NARROW) {
-      // no k-steps left: help finish this CTA's cut tile (its last segment)
       if (ok && sg.count > sg.whole) {
         const int i = sg.count - 1;
         int tile, j0, j1;
@@ -825,8 +877,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (j0 == 0) {
           int np = sk_partners(p, tile);
           np = np > kMaxPartners ? kMaxPartners : np;
-          const uint32_t a = (uint32_t)i % C::NACC, use = (uint32_t)i / C::NACC;
-          if (!mbar_wait(acc_full + 8 * a, use & 1)) {
+          const uint32_t a = (uint32_t)i % C::NACC;
+          if (!mbar_wait(help_bar, 0)) {
             set_status(BONSAI_ERR_TIMEOUT);
           } else {
             tc_fence_after();
