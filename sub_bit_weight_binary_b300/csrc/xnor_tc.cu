@@ -120,6 +120,51 @@ __device__ __forceinline__ uint32_t sign_pair(uint32_t nb, int i) {
   return (((nb >> (2 * i)) & 3u) * 0x40008000u) & 0x80008000u;
 }
 
+// D and Y of a tile from tensor memory: its 16-token chunks grp, grp + ngrp,
+// ... read by this warp's lane quarter. On a CTA's last tile the epilogue
+// warps (grp 0) share the chunks with the two weight-expander groups, which
+// have no k-steps left (with one tile per CTA the whole epilogue is
+// otherwise exposed). acc_empty (not 0): arrived on after this warp's last
+// tensor-memory load.
+__device__ __forceinline__ void store_dy(const Params& p, int tile, uint32_t tmem_base, int grp,
+                                         int ngrp, uint32_t acc_empty) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
+  const bool do_d = p.d != nullptr, do_y = p.y != nullptr;
+  const int n0 = (tile / p.tok_tiles) * TM, m0 = (tile % p.tok_tiles) * TN;
+  const int feat = n0 + 32 * quarter + lane;
+  const bool fok = feat < p.n;
+  const int chunks = (p.m - m0 + 15) / 16 < TN / 16 ? (p.m - m0 + 15) / 16 : TN / 16;
+  const int last = grp < chunks ? grp + (chunks - 1 - grp) / ngrp * ngrp : -1;
+  const uint32_t tl = tmem_base + ((uint32_t)(32 * quarter) << 16);
+#pragma unroll 1
+  for (int c = grp; c < chunks; c += ngrp) {
+    uint32_t vd[16], vy[16];
+    if (do_d) TMEM_LD_16(tl + COL_D + 16 * c, vd);
+    if (do_y) TMEM_LD_16(tl + COL_Y + 16 * c, vy);
+    tmem_ld_wait();
+    if (c == last && acc_empty) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+    if (!fok) continue;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int tok = m0 + 16 * c + j;
+      if (tok >= p.m) break;
+      if (do_d) p.d[(size_t)tok * p.n + feat] = __float2int_rn(__uint_as_float(vd[j]));
+      if (do_y)
+        p.y[(size_t)tok * p.n + feat] =
+            __float2half_rn(__half2float(p.a_scale[tok]) * __uint_as_float(vy[j]));
+    }
+  }
+  if (last < 0 && acc_empty) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(acc_empty);
+  }
+}
+
 __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   // the swizzled B stages need 1024-byte alignment
@@ -134,7 +179,11 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
   const uint32_t full = sBar, empty = full + 8 * A_STAGES;
   const uint32_t acc_full = empty + 8 * A_STAGES, acc_empty = acc_full + 8;
   const uint32_t drain = acc_empty + 8, tmem_slot = drain + 8;
-  static_assert(8 * (2 * A_STAGES + 3) + 4 <= 256, "barrier area");
+  // the epilogue warps arrive once the CTA's last accumulator is complete;
+  // the weight expanders wait on it (once) before they help store it (not
+  // on acc_full: they may finish their k-steps two accumulator phases ahead)
+  const uint32_t help_bar = tmem_slot + 8;
+  static_assert(8 * (2 * A_STAGES + 5) <= 256, "barrier area");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool do_d = p.d != nullptr, do_y = p.y != nullptr;
   // A stages: 32 columns per wanted output (+-1 codes first, then +-s)
@@ -149,6 +198,7 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
     mbar_init(drain, 1);
+    mbar_init(help_bar, 4);
     fence_barrier_init();
   }
   if (warp == W_TMEM) {
@@ -262,6 +312,16 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
         if (lane == 0) mbar_arrive(full + 8 * s);
       }
     }
+    // no k-steps left: help store this CTA's last tile
+    if (ok && (int)blockIdx.x < p.tiles) {
+      const int last = (int)blockIdx.x + (p.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x * (int)gridDim.x;
+      if (!mbar_wait(help_bar, 0)) {
+        set_status(BONSAI_ERR_TIMEOUT);
+      } else {
+        tc_fence_after();
+        store_dy(p, last, tmem_base, 1 + (int)h, 3, 0);
+      }
+    }
   } else if (warp >= W_EPI && warp < W_EPI + 4) {
     // ------------------------------- epilogue -------------------------------
     pdl_wait();
@@ -311,33 +371,12 @@ __global__ void __launch_bounds__(THREADS, 1) xnor_tc_kernel(const __grid_consta
       // ---- epilogue of the tile
       if (!mbar_wait(acc_full, it & 1)) { set_status(BONSAI_ERR_TIMEOUT); break; }
       tc_fence_after();
-      const int n0 = (tile / p.tok_tiles) * TM, m0 = (tile % p.tok_tiles) * TN;
-      const int feat = n0 + 32 * e + lane;
-      const bool fok = feat < p.n;
-      const int chunks = (p.m - m0 + 31) / 32 < TN / 32 ? (p.m - m0 + 31) / 32 : TN / 32;
-      const uint32_t tl = tmem_base + ((uint32_t)(32 * e) << 16);
-#pragma unroll 1
-      for (int c = 0; c < chunks; ++c) {
-        uint32_t vd[32], vy[32];
-        if (do_d) TMEM_LD_32(tl + COL_D + 32 * c, vd);
-        if (do_y) TMEM_LD_32(tl + COL_Y + 32 * c, vy);
-        tmem_ld_wait();
-        if (c == chunks - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty);
-        }
-        if (!fok) continue;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int tok = m0 + 32 * c + j;
-          if (tok >= p.m) break;
-          if (do_d) p.d[(size_t)tok * p.n + feat] = __float2int_rn(__uint_as_float(vd[j]));
-          if (do_y)
-            p.y[(size_t)tok * p.n + feat] =
-                __float2half_rn(__half2float(p.a_scale[tok]) * __uint_as_float(vy[j]));
-        }
+      const bool last_tile = tile + (int)gridDim.x >= p.tiles;
+      if (last_tile) {  // the weight expanders may help
+        __syncwarp();
+        if (lane == 0) mbar_arrive(help_bar);
       }
+      store_dy(p, tile, tmem_base, 0, last_tile ? 3 : 1, acc_empty);
     }
   }
 
