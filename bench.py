@@ -331,8 +331,10 @@ class GemvWorkload:
     """Decode product M=1 over rotating weight replicas."""
     kind = "gemv"
 
-    def __init__(self, fmt, n, k, cfg_id, name, ref=False):
+    def __init__(self, fmt, n, k, cfg_id, name, ref=False, lut=False):
         self.fmt, self.n, self.k, self.cfg_id, self.name, self.ref = fmt, n, k, cfg_id, name, ref
+        self.lut = lut  # one-token table kernel through bonsai_gemv_ws (one shared workspace)
+        self.ws = None
         self.reps = max(1, math.ceil(2 * L2_BYTES / self.unit_bytes()) + 1)
 
     def unit_bytes(self):
@@ -352,13 +354,20 @@ class GemvWorkload:
         self.x = self.x_host.cuda()
         self.y = torch.empty(self.n, dtype=torch.float16, device="cuda")
         self.y_host = torch.empty(self.n, dtype=torch.float16).pin_memory()
+        if self.lut:
+            self.ws = sb.gemv_workspace(self.w[0])
+            if self.ws is None:
+                raise RuntimeError("%s does not take the table kernel" % self.name)
         torch.cuda.synchronize()
         sb.check()
 
     def launches(self, start, count):
         import sub_bit_weight_binary_b300 as sb
         for i in range(start, start + count):
-            sb.bonsai_gemv(self.w[i % self.reps], self.x, self.y)
+            if self.ws is None:
+                sb.bonsai_gemv(self.w[i % self.reps], self.x, self.y)
+            else:
+                sb.bonsai_gemv_ws(self.w[i % self.reps], self.x, self.y, self.ws)
 
     def measure(self, steps, warmup, clocks=None):
         ms = graph_time(self.launches, steps, warmup, clocks)
@@ -375,13 +384,15 @@ class GemvWorkload:
           eager -- the plain bonsai_gemv_host C call per token."""
         import torch
         import sub_bit_weight_binary_b300 as sb
-        plans = [sb.GemvHostPlan(w, self.x_host, self.x, self.y, self.y_host) for w in self.w]
+        plans = [sb.GemvHostPlan(w, self.x_host, self.x, self.y, self.y_host, self.ws)
+                 for w in self.w]
 
         def plan(i):
             plans[i % self.reps]()
 
         def eager(i):
-            sb.bonsai_gemv_host(self.w[i % self.reps], self.x_host, self.x, self.y, self.y_host)
+            sb.bonsai_gemv_host(self.w[i % self.reps], self.x_host, self.x, self.y, self.y_host,
+                                workspace=self.ws)
 
         out = {}
         for name, one in (("plan", plan), ("eager", eager)):
@@ -405,9 +416,13 @@ class GemvWorkload:
 
     def roofline(self, r, pk):
         a = self.unit_bytes() / (r["kernel_ms"] / 1e3) / 1e9
-        prof = {(2, 17408, 5120): "gemv_ternary_k5120_n17408.md",
-                (1, 17408, 5120): "gemv_binary_k5120_n17408.md"}.get((self.fmt, self.n, self.k))
-        return {"bound": "hbm", "kernel": "gemv_%s_kernel" % ("ternary" if self.fmt == 2 else "binary"),
+        prof = {(2, 17408, 5120, False): "gemv_ternary_k5120_n17408.md",
+                (2, 17408, 5120, True): "gemv_ter_lut_k5120_n17408.md",
+                (1, 17408, 5120, False): "gemv_binary_k5120_n17408.md"}.get(
+                    (self.fmt, self.n, self.k, self.lut))
+        kern = "gemv_ter_lut_kernel" if self.lut else \
+            "gemv_%s_kernel" % ("ternary" if self.fmt == 2 else "binary")
+        return {"bound": "hbm", "kernel": kern,
                 "achieved": round(a, 1), "peak": pk["hbm"], "unit": "GB/s",
                 "frac": round(a / pk["hbm"], 4), "traffic": profiled_traffic(prof) if prof else None,
                 "peak_src": "%s HBM copy (burst)" % pk["src"],
@@ -1096,6 +1111,8 @@ class XnorFp16Workload(XnorWorkload):
 WORKLOADS = {
     "ter_gemv": lambda ref=False: GemvWorkload(2, 17408, 5120, 2,
                                                "ternary GEMV M=1 K=5120 N=17408 (decode)", ref),
+    "ter_gemv_lut": lambda ref=False: GemvWorkload(
+        2, 17408, 5120, 2, "ternary GEMV M=1 K=5120 N=17408 (decode), table kernel", ref, lut=True),
     "bin_gemv_1k": lambda ref=False: GemvWorkload(1, 1024, 1024, 1,
                                                   "binary GEMV M=1 K=1024 N=1024 (decode)", ref),
     "bin_gemv": lambda ref=False: GemvWorkload(1, 17408, 5120, 2,

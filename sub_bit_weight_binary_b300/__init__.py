@@ -79,6 +79,12 @@ def lib():
         L.bonsai_gemv_host.argtypes = [W, P, P, P, P, P]
         L.bonsai_gemv_host.restype = S
         L.bonsai_gemv_splitk_static.argtypes = [W, P, P, P]
+        L.bonsai_gemv_workspace_bytes.argtypes = [W]
+        L.bonsai_gemv_workspace_bytes.restype = I64
+        L.bonsai_gemv_ws.argtypes = [W, P, P, P, I64, P]
+        L.bonsai_gemv_ws.restype = S
+        L.bonsai_gemv_host_ws.argtypes = [W, P, P, P, P, P, I64, P]
+        L.bonsai_gemv_host_ws.restype = S
         L.bonsai_gemv_splitk_static.restype = S
         L.bonsai_gemm.argtypes = [W, P, I64, P, P]
         L.bonsai_gemm.restype = S
@@ -220,16 +226,45 @@ def _host_ptr(t, name):
     return t.data_ptr()
 
 
-def bonsai_gemv_host(w: Weights, x_host, x_dev, y_dev, y_host, stream=None):
+def bonsai_gemv_workspace_bytes(w: Weights) -> int:
+    """Bytes of the workspace that bonsai_gemv_ws needs to run the one-token
+    product on the table kernel (0: the shape does not take it)."""
+    return int(lib().bonsai_gemv_workspace_bytes(C.byref(w.c_struct())))
+
+
+def gemv_workspace(w: Weights, device="cuda"):
+    """A zero-filled workspace for bonsai_gemv_ws / bonsai_gemv_host_ws (and
+    bonsai_gemm_ws with one token), or None if the shape takes none."""
+    import torch
+    nbytes = bonsai_gemv_workspace_bytes(w)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device) if nbytes else None
+
+
+def bonsai_gemv_ws(w: Weights, x, y, workspace, stream=None):
+    """bonsai_gemv with a workspace (see gemv_workspace): the table kernel for
+    ternary weights of a shape that takes it, bonsai_gemv's kernels otherwise."""
+    import torch
+    wp, wb = _ws_args(workspace)
+    _ok(lib().bonsai_gemv_ws(C.byref(w.c_struct()), _ptr(x, (torch.float16,), "x"),
+                             _ptr(y, (torch.float16,), "y"), wp, wb, _stream(stream)),
+        "bonsai_gemv_ws")
+
+
+def bonsai_gemv_host(w: Weights, x_host, x_dev, y_dev, y_host, stream=None, workspace=None):
     """Host x in, host y out: enqueue x_host -> x_dev, the decode product into
-    y_dev and y_dev -> y_host on the stream (synchronise before reading y_host)."""
+    y_dev and y_dev -> y_host on the stream (synchronise before reading y_host).
+    With a workspace (see gemv_workspace) the product runs as bonsai_gemv_ws."""
     import torch
     if x_host.numel() != w.k or y_host.numel() != w.n:
         raise ValueError("x_host must hold k and y_host n values")
-    _ok(lib().bonsai_gemv_host(C.byref(w.c_struct()), _host_ptr(x_host, "x_host"),
-                               _ptr(x_dev, (torch.float16,), "x_dev"),
-                               _ptr(y_dev, (torch.float16,), "y_dev"),
-                               _host_ptr(y_host, "y_host"), _stream(stream)), "bonsai_gemv_host")
+    args = (C.byref(w.c_struct()), _host_ptr(x_host, "x_host"),
+            _ptr(x_dev, (torch.float16,), "x_dev"), _ptr(y_dev, (torch.float16,), "y_dev"),
+            _host_ptr(y_host, "y_host"))
+    if workspace is None:
+        _ok(lib().bonsai_gemv_host(*args, _stream(stream)), "bonsai_gemv_host")
+    else:
+        wp, wb = _ws_args(workspace)
+        _ok(lib().bonsai_gemv_host_ws(*args, wp, wb, _stream(stream)), "bonsai_gemv_host_ws")
 
 
 class GemvHostPlan:
@@ -237,22 +272,23 @@ class GemvHostPlan:
     product of bonsai_gemv_host are captured in a CUDA graph, and each call
     replays it (one launch per token; the contents of x_host may change
     between calls, the buffers themselves may not). Synchronise before
-    reading y_host. x_host and y_host must be pinned."""
+    reading y_host. x_host and y_host must be pinned; the optional workspace
+    is used as by bonsai_gemv_host."""
 
-    def __init__(self, w: Weights, x_host, x_dev, y_dev, y_host):
+    def __init__(self, w: Weights, x_host, x_dev, y_dev, y_host, workspace=None):
         import torch
         if not (x_host.is_pinned() and y_host.is_pinned()):
             raise ValueError("x_host and y_host must be pinned host tensors")
-        self._keep = (w, x_host, x_dev, y_dev, y_host)
+        self._keep = (w, x_host, x_dev, y_dev, y_host, workspace)
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):  # eager call first: one-time setup stays outside the capture
-            bonsai_gemv_host(w, x_host, x_dev, y_dev, y_host)
+            bonsai_gemv_host(w, x_host, x_dev, y_dev, y_host, workspace=workspace)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            bonsai_gemv_host(w, x_host, x_dev, y_dev, y_host)
+            bonsai_gemv_host(w, x_host, x_dev, y_dev, y_host, workspace=workspace)
 
     def __call__(self):
         self.graph.replay()
@@ -288,8 +324,9 @@ def bonsai_gemm_swiglu(w: Weights, x, h, stream=None):
 
 
 def bonsai_gemm_workspace_bytes(w: Weights, m: int) -> int:
-    """Bytes of the stream-K workspace that bonsai_gemm_ws needs for m tokens
-    (0: the product's tiles fill the SMs evenly, no workspace is used)."""
+    """Bytes of the workspace that bonsai_gemm_ws needs for m tokens: the
+    stream-K partial tiles for m > 8, the table kernel's partial sums for
+    m = 1 (0: no workspace is used for this shape)."""
     ws = w.c_struct()
     return int(lib().bonsai_gemm_workspace_bytes(C.byref(ws), int(m)))
 

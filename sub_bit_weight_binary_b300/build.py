@@ -25,7 +25,7 @@ NVFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                   "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 
 LIBS = {
-    "libbonsai.so": ["api.cu", "pack.cu", "gemv.cu", "gemm.cu", "xnor.cu", "xnor_tc.cu", "splitk.cu", "rotate.cu", "stage.cu", "selftest.cu"],
+    "libbonsai.so": ["api.cu", "pack.cu", "gemv.cu", "gemv_lut.cu", "gemm.cu", "xnor.cu", "xnor_tc.cu", "splitk.cu", "rotate.cu", "stage.cu", "selftest.cu"],
     "libbonsai_synth.so": ["synth.cu"],
 }
 HEADERS = ["common.cuh", "tcgen05.cuh"]

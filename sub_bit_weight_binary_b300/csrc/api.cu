@@ -16,6 +16,9 @@ bonsai_status stage_x_launch(const uint16_t*, uint16_t*, int64_t, cudaStream_t);
 bonsai_status gemm_launch(const bonsai_weights*, const uint16_t*, int64_t, uint16_t*, bool,
                           cudaStream_t, void* ws = nullptr, int64_t ws_bytes = 0);
 int64_t gemm_workspace_bytes(const bonsai_weights*, int64_t);
+int64_t gemv_lut_workspace_bytes(const bonsai_weights*);
+bonsai_status gemv_lut_launch(const bonsai_weights*, const uint16_t*, uint16_t*, bool, void*,
+                              int64_t, cudaStream_t);
 bonsai_status xnor_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
                           int32_t*, uint16_t*, cudaStream_t);
 bonsai_status xnor_tc_launch(const uint32_t*, const uint16_t*, int64_t, const bonsai_weights*,
@@ -35,6 +38,7 @@ unsigned int read_clear_status_gemv();
 unsigned int read_clear_status_gemm();
 unsigned int read_clear_status_xnor();
 unsigned int read_clear_status_xnor_tc();
+unsigned int read_clear_status_lut();
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -159,6 +163,12 @@ constexpr int64_t kMaxM = 1 << 24;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bonsai_status check_workspace(const void* ws, int64_t ws_bytes) {
+  if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return BONSAI_ERR_INVALID_ARG;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return BONSAI_ERR_ALIGN;
+  return BONSAI_OK;
+}
+
 bonsai_status check_row_bytes(int32_t format, int64_t k, int64_t row_bytes) {
   if (format == BONSAI_FMT_BINARY) {
     if (row_bytes < k / 8 || row_bytes % 16) return BONSAI_ERR_SHAPE;
@@ -223,26 +233,54 @@ bonsai_status bonsai_pack_ternary(const int8_t* codes, int64_t rows, int64_t k, 
   return pack_ternary_launch(codes, rows, k, out, row_bytes, stream);
 }
 
-bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
-                          bonsai_stream stream) {
-  bonsai_status st = check_weights(w);
-  if (st != BONSAI_OK) return st;
-  if (!x || !y) return BONSAI_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
+// One token on the device: the table kernel when a large enough workspace
+// is given and the shape takes it, else the streaming decode kernel, else
+// (very long rows: the decode kernel's per-CTA x table no longer fits in
+// shared memory) the tensor-core kernel, which takes any K.
+static bonsai_status gemv_any(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
+                              void* ws, int64_t ws_bytes, cudaStream_t stream) {
+  bonsai_status st = gemv_lut_launch(w, x, y, false, ws, ws_bytes, stream);
+  if (st != BONSAI_ERR_UNSUPPORTED) return st;
   st = gemv_launch(w, x, 1, y, false, stream);
-  // very long rows: the decode kernel's per-CTA x table no longer fits in
-  // shared memory; the tensor-core kernel takes any K
   if (st == BONSAI_ERR_UNSUPPORTED) st = gemm_launch(w, x, 1, y, false, stream);
   return st;
 }
 
-bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
-                               uint16_t* x_dev, uint16_t* y_dev, uint16_t* y_host,
-                               bonsai_stream stream) {
+static bonsai_status gemv_common(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
+                                 void* ws, int64_t ws_bytes, bonsai_stream stream) {
+  bonsai_status st = check_weights(w);
+  if (st != BONSAI_OK) return st;
+  if (!x || !y) return BONSAI_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
+  st = check_workspace(ws, ws_bytes);
+  if (st != BONSAI_OK) return st;
+  return gemv_any(w, x, y, ws, ws_bytes, stream);
+}
+
+bonsai_status bonsai_gemv(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
+                          bonsai_stream stream) {
+  return gemv_common(w, x, y, nullptr, 0, stream);
+}
+
+int64_t bonsai_gemv_workspace_bytes(const bonsai_weights* w) {
+  if (check_weights(w) != BONSAI_OK) return 0;
+  return gemv_lut_workspace_bytes(w);
+}
+
+bonsai_status bonsai_gemv_ws(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
+                             void* workspace, int64_t workspace_bytes, bonsai_stream stream) {
+  return gemv_common(w, x, y, workspace, workspace_bytes, stream);
+}
+
+static bonsai_status gemv_host_common(const bonsai_weights* w, const uint16_t* x_host,
+                                      uint16_t* x_dev, uint16_t* y_dev, uint16_t* y_host,
+                                      void* ws, int64_t ws_bytes, bonsai_stream stream) {
   bonsai_status st = check_weights(w);
   if (st != BONSAI_OK) return st;
   if (!x_host || !x_dev || !y_dev || !y_host) return BONSAI_ERR_INVALID_ARG;
   if (!aligned16(x_dev) || !aligned16(y_dev)) return BONSAI_ERR_ALIGN;
+  st = check_workspace(ws, ws_bytes);
+  if (st != BONSAI_OK) return st;
   // Page-locked host buffers are mapped into the device address space: the
   // activations are then read by a small kernel and the result is written by
   // the product kernel itself, so no copy-engine transfer (with its fixed
@@ -266,13 +304,25 @@ bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
   }
   if (st != BONSAI_OK) return st;
   uint16_t* y_out = ym ? static_cast<uint16_t*>(ym) : y_dev;
-  st = gemv_launch(w, x_dev, 1, y_out, false, stream);
-  if (st == BONSAI_ERR_UNSUPPORTED) st = gemm_launch(w, x_dev, 1, y_out, false, stream);
+  st = gemv_any(w, x_dev, y_out, ws, ws_bytes, stream);
   if (st != BONSAI_OK || ym) return st;
   if (cudaMemcpyAsync(y_host, y_dev, (size_t)w->n * 2, cudaMemcpyDeviceToHost, stream) !=
       cudaSuccess)
     return BONSAI_ERR_CUDA;
   return BONSAI_OK;
+}
+
+bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
+                               uint16_t* x_dev, uint16_t* y_dev, uint16_t* y_host,
+                               bonsai_stream stream) {
+  return gemv_host_common(w, x_host, x_dev, y_dev, y_host, nullptr, 0, stream);
+}
+
+bonsai_status bonsai_gemv_host_ws(const bonsai_weights* w, const uint16_t* x_host,
+                                  uint16_t* x_dev, uint16_t* y_dev, uint16_t* y_host,
+                                  void* workspace, int64_t workspace_bytes,
+                                  bonsai_stream stream) {
+  return gemv_host_common(w, x_host, x_dev, y_dev, y_host, workspace, workspace_bytes, stream);
 }
 
 bonsai_status bonsai_gemv_splitk_static(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
@@ -294,8 +344,12 @@ static bonsai_status gemm_common(const bonsai_weights* w, const uint16_t* x, int
   if (swiglu && w->n % 16) return BONSAI_ERR_SHAPE;
   if (m > kMaxM) return BONSAI_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(y)) return BONSAI_ERR_ALIGN;
-  if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return BONSAI_ERR_INVALID_ARG;
-  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return BONSAI_ERR_ALIGN;
+  st = check_workspace(ws, ws_bytes);
+  if (st != BONSAI_OK) return st;
+  if (m == 1) {
+    st = gemv_lut_launch(w, x, y, swiglu, ws, ws_bytes, stream);
+    if (st != BONSAI_ERR_UNSUPPORTED) return st;
+  }
   if (m <= 8) {
     st = gemv_launch(w, x, m, y, swiglu, stream);
     if (st != BONSAI_ERR_UNSUPPORTED) return st;
@@ -314,7 +368,9 @@ bonsai_status bonsai_gemm_swiglu(const bonsai_weights* w, const uint16_t* x, int
 }
 
 int64_t bonsai_gemm_workspace_bytes(const bonsai_weights* w, int64_t m) {
-  if (check_weights(w) != BONSAI_OK || m <= 8 || m > kMaxM) return 0;
+  if (check_weights(w) != BONSAI_OK || m < 1 || m > kMaxM) return 0;
+  if (m == 1) return gemv_lut_workspace_bytes(w);
+  if (m <= 8) return 0;
   return gemm_workspace_bytes(w, m);
 }
 
@@ -442,9 +498,10 @@ bonsai_status bonsai_selftest_wait_timeout(uint64_t limit_ns, bonsai_stream stre
 
 bonsai_status bonsai_check_async(bonsai_stream stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return BONSAI_ERR_CUDA;
-  const unsigned int codes[6] = {read_clear_status_pack(), read_clear_status_gemv(),
-                                 read_clear_status_gemm(), read_clear_status_xnor(),
-                                 read_clear_status_xnor_tc(), read_clear_status_selftest()};
+  const unsigned int codes[7] = {read_clear_status_pack(),    read_clear_status_gemv(),
+                                 read_clear_status_gemm(),    read_clear_status_xnor(),
+                                 read_clear_status_xnor_tc(), read_clear_status_lut(),
+                                 read_clear_status_selftest()};
   if (cudaGetLastError() != cudaSuccess) return BONSAI_ERR_CUDA;
   for (unsigned int c : codes)
     if (c != 0) return static_cast<bonsai_status>(c);

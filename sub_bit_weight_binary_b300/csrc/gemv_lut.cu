@@ -1,0 +1,463 @@
+// gemv_lut.cu -- one-token ternary decode product through per-position tables
+// of partial sums, with K split across thread blocks.
+//
+// "Multiplication degenerates to addition and sign flip" (三值权重 page): a
+// packed byte holds five codes, so x . w over those five codes is one of 243
+// numbers fixed by x alone. The kernel tabulates them in FP32 for every byte
+// position of a slice of K, and each byte of each row then costs one table
+// load and one add; no code is expanded into an operand.
+//
+// Structure (sm_103a):
+//  * K is cut into slices of 640 codes (128 packed bytes, five whole 128-code
+//    groups); the rows into C chunks. One CTA per (chunk, slice), at most one
+//    per SM, 16 warps.
+//  * Tables, one bank per lane: lane p handles bytes 4p..4p+3 of every row
+//    (one 32-bit word), and the table of byte 4p+j is stored entry-major with
+//    entry e of lane p at e*256 + (j&1)*128 + 4p in table pair j>>1, so the
+//    32 lookups of a warp hit 32 banks. One PRMT puts the byte into bits
+//    8..15, one add gives the address, one LDS fetches the FP32 sum.
+//  * Group scales (one FP16 per 128 codes, OpenBonsai page, "工作原理"): the
+//    slice's group edges fall inside bytes 25, 51, 76 and 102. The table of
+//    such a byte holds only its codes below the edge; its codes above the
+//    edge are looked up in a small table by the byte's upper base-3 digits
+//    (index = byte / 3^k, a multiply-high). The lane adds them, with any
+//    later bytes of its word (all above the edge), into a hand-over sum that
+//    the next lane (whose four bytes are all in the upper group) takes with
+//    one shuffle. So every lane multiplies by exactly one scale per row.
+//  * Streaming: a row's slice is only 128 bytes, and a 2-D TMA box of such
+//    short rows costs the copy engine far more per byte than wide boxes
+//    (measured: ~190 ns per 8-row stage from one issuing thread). So every
+//    warp streams its own stages (8 rows of weights and their scales) with
+//    16-byte cp.async copies into four private ring slots, three stages
+//    ahead of the one it reads; warp w takes stages w, w+16, ...
+//  * A warp sums its 8 rows' lane values with a transposed butterfly and
+//    stores one FP32 partial per (row, slice) in the caller's workspace.
+//    The chunk's rows are split into S parts with one arrival counter each;
+//    the CTA that completes a part adds its S partials in slice order (the
+//    same order every call) and writes FP16 y, or silu(g)*u for a gated
+//    feed-forward weight, then re-arms the counter.
+#include "common.cuh"
+
+namespace bonsai {
+BONSAI_DEFINE_STATUS(g_status_lut)
+
+unsigned int read_clear_status_lut() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_status_lut, sizeof(v));
+  cudaMemcpyToSymbol(g_status_lut, &z, sizeof(z));
+  return v;
+}
+
+namespace lut {
+
+constexpr int kWarps = 16;  // every warp streams its own rows
+constexpr int kThreads = kWarps * 32;
+constexpr int kRows = 8;           // rows per stage
+constexpr int kDepth = 3;          // a warp's stages in flight beyond the one it reads
+constexpr int kWarpSlots = kDepth + 1;
+constexpr int kSlots = kWarps * kWarpSlots;
+constexpr int kSliceBytes = 128;   // packed bytes per row per slice
+constexpr int kSliceCodes = 640;
+constexpr int kStageW = kRows * kSliceBytes;  // weights of a stage
+constexpr int kScaleRow = 32;                 // 16 scales per row and stage
+constexpr int kStageBytes = kStageW + kRows * kScaleRow;
+constexpr int kEntries = 256;                 // 243 byte values; 256 keeps any byte in bounds
+constexpr int kPairBytes = kEntries * 256;    // two byte positions per 256-byte table row
+constexpr int kHRows = 86;                    // upper-digit table rows (255 / 3 + 1)
+constexpr int kMaxSlices = 160;
+
+constexpr int kOffT = 0;
+constexpr int kOffH = kOffT + 2 * kPairBytes;
+constexpr int kOffX = kOffH + kHRows * 128;
+constexpr int kOffFlags = kOffX + kSliceCodes * 4;
+constexpr int kOffRing = kOffFlags + kMaxSlices * 4;
+constexpr int kSmem = kOffRing + kSlots * kStageBytes;
+static_assert(kOffRing % 128 == 0, "ring stages are 128-byte aligned");
+static_assert(kSmem <= 232448, "fits the opt-in shared memory of one SM");
+
+struct Params {
+  const uint8_t* packed;
+  const __half* scales;
+  const __half* x;
+  __half* y;
+  float* ws;          // partial sums [chunk][slice][rc]
+  unsigned int* cnt;  // arrival counters [chunk][part]
+  long long row_bytes;
+  int n, k, G, S, C, rc, part_rows;
+  int prefetch, swiglu;
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// Shared-memory reads by 32-bit shared address. Not volatile, so the
+// compiler may schedule them freely across the unrolled rows; the reads of a
+// ring stage take their address from a value produced after the stage's
+// copies were waited for (opaque_zero), which keeps them behind that wait.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_h2f(uint32_t a) {
+  unsigned short v;
+  asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return __half2float(__ushort_as_half(v));
+}
+__device__ __forceinline__ uint32_t opaque_zero() {
+  uint32_t z;
+  asm volatile("mov.u32 %0, 0;" : "=r"(z)::"memory");
+  return z;
+}
+
+// 16-byte asynchronous copy global -> shared; with src_bytes 0 the 16 bytes
+// are zero-filled and nothing is read.
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The four bytes whose codes cross a group edge inside one slice, as
+// (lane, byte of the lane's word, digits below the edge): bytes 25, 51, 76
+// and 102 hold codes 125..129, 255..259, 380..384 and 510..514.
+__host__ __device__ constexpr int edge_byte(int lane) {
+  return lane == 6 ? 1 : lane == 12 ? 3 : lane == 19 ? 0 : lane == 25 ? 2 : -1;
+}
+__host__ __device__ constexpr int edge_low_digits(int lane) {
+  return lane == 6 ? 3 : lane == 12 ? 1 : lane == 19 ? 4 : lane == 25 ? 2 : 0;
+}
+
+// Stage i of the chunk (rows row0+8i .. row0+8i+7, slice s) into the ring
+// slot at dst, issued by one warp: the weights as 8 rows x 8 pieces of 16
+// bytes (two per lane), the scales of the 16-group window from group sx as
+// 8 rows x 2 pieces (lanes 0..15). Rows past n re-read row n-1 (their sums
+// are never used); bytes past the row and groups past k/128 read as zero.
+__device__ __forceinline__ void load_stage(const Params& p, uint32_t dst, int row0, int i, int s,
+                                           int sx, int lane) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int piece = lane + 32 * h, r = piece >> 3, col = piece & 7;
+    int row = row0 + kRows * i + r;
+    row = row < p.n ? row : p.n - 1;
+    const long long off = (long long)s * kSliceBytes + 16 * col;
+    const bool in = off < p.row_bytes;
+    cp16(dst + r * kSliceBytes + 16 * col, p.packed + (size_t)row * p.row_bytes + (in ? off : 0),
+         in ? 16u : 0u);
+  }
+  if (lane < 16) {
+    const int r = lane >> 1, hh = lane & 1;
+    int row = row0 + kRows * i + r;
+    row = row < p.n ? row : p.n - 1;
+    const int g0 = sx + 8 * hh;
+    const bool in = g0 < p.G;
+    cp16(dst + kStageW + r * kScaleRow + 16 * hh, p.scales + (size_t)row * p.G + (in ? g0 : 0),
+         in ? 16u : 0u);
+  }
+}
+
+// Tables of the CTA's slice from x (FP32, zero past K). T: for the 128 byte
+// positions, every byte value's sum over the codes below the position's
+// group edge (all five codes but for the four edge bytes); H: for the edge
+// bytes, the sum over the codes above the edge by the upper digits (row 0
+// of the other lanes is zero: their index is always 0). Both with the same
+// unrolled code: a byte value (or upper-digit index) e = a + 27*b, digits
+// 0..2 in a and digits 3..4 in b, sums A[a] + B[b].
+__device__ __forceinline__ void table_rows(float* dst, int stride, const float (&xv)[5], int q,
+                                           int limit) {
+  float A[27];
+#pragma unroll
+  for (int a = 0; a < 27; ++a) {
+    const int d0 = a % 3, d1 = (a / 3) % 3, d2 = a / 9;
+    float v = d0 == 0 ? -xv[0] : d0 == 2 ? xv[0] : 0.f;
+    v += d1 == 0 ? -xv[1] : d1 == 2 ? xv[1] : 0.f;
+    v += d2 == 0 ? -xv[2] : d2 == 2 ? xv[2] : 0.f;
+    A[a] = v;
+  }
+  for (int b = q; 27 * b < limit; b += 4) {
+    const int d3 = b % 3, d4 = b / 3;
+    const float B = (d3 == 0 ? -xv[3] : d3 == 2 ? xv[3] : 0.f) +
+                    (d4 == 0 ? -xv[4] : d4 == 2 ? xv[4] : 0.f);
+    float* rb = dst + 27 * stride * b;
+#pragma unroll
+    for (int a = 0; a < 27; ++a)
+      if (27 * b + a < limit) rb[a * stride] = A[a] + B;
+  }
+}
+
+__device__ __forceinline__ void build_tables(const Params& p, uint8_t* smem, int s) {
+  float* xs = reinterpret_cast<float*>(smem + kOffX);
+  const int t = threadIdx.x;
+  for (int i = t; i < kSliceCodes; i += kThreads) {
+    const int kk = s * kSliceCodes + i;
+    xs[i] = kk < p.k ? __half2float(p.x[kk]) : 0.f;
+  }
+  if (t < 32 && edge_byte(t) < 0) reinterpret_cast<float*>(smem + kOffH)[t] = 0.f;
+  __syncthreads();
+  const int pos = t & 127, q = t >> 7;
+  const int pj = pos >> 5, pl = pos & 31;
+  const int byte = 4 * pl + pj;
+  const bool edge = edge_byte(pl) == pj;
+  const int nd = edge ? edge_low_digits(pl) : 5;
+  float xv[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) xv[i] = i < nd ? xs[5 * byte + i] : 0.f;
+  table_rows(reinterpret_cast<float*>(smem + kOffT + (pj >> 1) * kPairBytes + (pj & 1) * 128) + pl,
+             64, xv, q, 243);
+  if (edge) {  // the codes above the edge, as digits 0.. of the index
+#pragma unroll
+    for (int i = 0; i < 5; ++i) xv[i] = i + nd < 5 ? xs[5 * byte + nd + i] : 0.f;
+    const int lim = nd == 1 ? 81 : nd == 2 ? 27 : nd == 3 ? 9 : 3;
+    table_rows(reinterpret_cast<float*>(smem + kOffH) + pl, 32, xv, q, lim);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_ter_lut_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const int s = blockIdx.x % p.S, c = blockIdx.x / p.S;
+  const int row0 = c * p.rc;
+  const int rows = min(p.rc, p.n - row0);
+  const int nst = (rows + kRows - 1) / kRows;
+  const int mine = nst > warp ? (nst - warp + kWarps - 1) / kWarps : 0;  // stages warp, warp+16, ..
+  const int sx = 8 * ((5 * s) / 8);  // first group of the 16-byte aligned scale window
+  const uint32_t ring = sbase + kOffRing + warp * kWarpSlots * kStageBytes;
+  pdl_launch_dependents();
+
+  // weights never depend on earlier work on the stream: with the prefetch
+  // flag the first stages stream in while the previous kernel finishes
+  if (!p.prefetch) pdl_wait();
+  for (int d = 0; d < kDepth; ++d) {
+    if (d < mine) load_stage(p, ring + d * kStageBytes, row0, warp + kWarps * d, s, sx, lane);
+    cp_commit();
+  }
+
+  // lane constants
+  const int js = edge_byte(lane);
+  const uint32_t magic = lane == 6 ? 2428u : lane == 12 ? 21846u : lane == 19 ? 810u
+                         : lane == 25 ? 7282u : 0u;  // ceil(2^16 / 3^k)
+  const float b1 = (js >= 0 && 1 > js) ? 1.f : 0.f;  // byte 1..3 wholly above the edge
+  const float b2 = (js >= 0 && 2 > js) ? 1.f : 0.f;
+  const float b3 = (js >= 0 && 3 > js) ? 1.f : 0.f;
+  const float a1 = 1.f - b1, a2 = 1.f - b2, a3 = 1.f - b3;
+  // table address of byte j: tq[j] + (byte << 8) (pair j>>1, half j&1, lane)
+  const uint32_t tq0 = sbase + kOffT + 4u * lane, tq1 = tq0 + 128u;
+  const uint32_t tq2 = tq0 + kPairBytes, tq3 = tq1 + kPairBytes;
+  const uint32_t hq = sbase + kOffH + 4u * lane;
+  const uint32_t sel_e = 0x4440u | uint32_t(js < 0 ? 0 : js);
+  const int g = (20 * lane) >> 7;  // the lane's (lower) group in the slice
+  const uint32_t so = 2u * uint32_t(5 * s - sx + g);
+
+  pdl_wait();  // x, y and the workspace are used by earlier work on the stream
+  build_tables(p, smem, s);
+  __syncthreads();
+
+  float* part = p.ws + (size_t)(c * p.S + s) * p.rc;
+  for (int j = 0; j < mine; ++j) {
+    const int jn = j + kDepth;
+    if (jn < mine)
+      load_stage(p, ring + (jn % kWarpSlots) * kStageBytes, row0, warp + kWarps * jn, s, sx, lane);
+    cp_commit();
+    cp_wait<kDepth>();  // this lane's copies of stage j have landed
+    __syncwarp();       // and every other lane's
+    const uint32_t st = ring + (j % kWarpSlots) * kStageBytes + opaque_zero();
+    float cr[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const uint32_t w = lds_u32(st + r * kSliceBytes + 4 * lane);
+      const float v0 = lds_f32(tq0 + prmt(w, 0u, 0x4404u));
+      const float v1 = lds_f32(tq1 + prmt(w, 0u, 0x4414u));
+      const float v2 = lds_f32(tq2 + prmt(w, 0u, 0x4424u));
+      const float v3 = lds_f32(tq3 + prmt(w, 0u, 0x4434u));
+      const uint32_t e = prmt(w, 0u, sel_e);
+      const float h = lds_f32(hq + (((e * magic) >> 9) & ~127u));
+      const float hs = fmaf(b3, v3, fmaf(b2, v2, fmaf(b1, v1, h)));
+      const float own = fmaf(a3, v3, fmaf(a2, v2, fmaf(a1, v1, v0)));
+      const float hp = __shfl_up_sync(0xFFFFFFFFu, hs, 1);  // lane 0: its own, 0
+      const float sc = lds_h2f(st + kStageW + r * kScaleRow + so);
+      cr[r] = sc * (own + hp);
+    }
+    // transposed butterfly over the 32 lanes: lanes 4R..4R+3 end with row R
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float t4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float keep = h16 ? cr[q + 4] : cr[q];
+      const float send = h16 ? cr[q] : cr[q + 4];
+      t4[q] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+    float t2[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float keep = h8 ? t4[q + 2] : t4[q];
+      const float send = h8 ? t4[q] : t4[q + 2];
+      t2[q] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+    float v = (h4 ? t2[1] : t2[0]) + __shfl_xor_sync(0xFFFFFFFFu, h4 ? t2[0] : t2[1], 4);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    if ((lane & 3) == 0) part[(warp + kWarps * j) * kRows + (lane >> 2)] = v;
+    __syncwarp();  // the slot is refilled by the next iteration's copies
+  }
+  cp_wait<0>();
+  __threadfence();  // this thread's partials before the arrival below
+  __syncthreads();
+
+  // arrivals: one counter per part of the chunk's rows
+  unsigned int* flags = reinterpret_cast<unsigned int*>(smem + kOffFlags);
+  if (threadIdx.x < p.S) {
+    unsigned int* ctr = p.cnt + c * p.S + threadIdx.x;
+    const unsigned int old = atomicAdd(ctr, 1u);
+    const bool last = old == unsigned(p.S - 1);
+    if (last) {
+      *ctr = 0u;  // every CTA of the chunk has arrived: re-arm for the next call
+      __threadfence();
+    }
+    flags[threadIdx.x] = last ? 1u : 0u;
+  }
+  __syncthreads();
+  // the parts this CTA completed, all rows at once
+  const float* base = p.ws + (size_t)c * p.S * p.rc;
+  int nf = 0;
+  for (int q = 0; q < p.S; ++q) nf += flags[q] ? 1 : 0;
+  const int span = p.swiglu ? p.part_rows / 2 : p.part_rows;  // outputs per part
+  for (int o = threadIdx.x; o < nf * span; o += kThreads) {
+    int q = -1;
+    for (int u = o / span; u >= 0; --u)  // the (o/span)-th completed part
+      do ++q; while (!flags[q]);
+    const int oi = o - (o / span) * span;
+    if (!p.swiglu) {
+      const int r = q * p.part_rows + oi;
+      if (r >= rows) continue;
+      float sum = 0.f;
+      for (int j0 = 0; j0 < p.S; j0 += 8) {  // 8 loads in flight, added in slice order
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = j0 + u < p.S ? __ldcg(base + (size_t)(j0 + u) * p.rc + r) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sum += v[u];
+      }
+      p.y[row0 + r] = __float2half_rn(sum);
+    } else {
+      // 16-row blocks: 8 gate rows, then the 8 up rows of the same features
+      const int f = q * (p.part_rows / 2) + oi;
+      const int r = (f >> 3) * 16 + (f & 7);
+      if (r >= rows) continue;
+      float gs = 0.f, us = 0.f;
+      for (int j0 = 0; j0 < p.S; j0 += 8) {
+        float vg[8], vu[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const bool in = j0 + u < p.S;
+          vg[u] = in ? __ldcg(base + (size_t)(j0 + u) * p.rc + r) : 0.f;
+          vu[u] = in ? __ldcg(base + (size_t)(j0 + u) * p.rc + r + 8) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          gs += vg[u];
+          us += vu[u];
+        }
+      }
+      p.y[row0 / 2 + f] = __float2half_rn(silu(gs) * us);
+    }
+  }
+}
+
+
+struct Shape {
+  int S, C, rc, part_rows;
+};
+
+}  // namespace lut
+
+// Rows per CTA below which the tables cost more than they save.
+constexpr int kLutMinRows = 192;
+
+static bool lut_shape(const bonsai_weights* w, lut::Shape& sh) {
+  using namespace lut;
+  if (w->format != BONSAI_FMT_TERNARY) return false;
+  const int64_t k = w->k, n = w->n;
+  if ((k / 128) % 8) return false;  // the scale rows' pitch must be 16-byte aligned
+  const int sms = device_sm_count();
+  if (device_max_smem_optin() < kSmem) return false;
+  const int64_t S = (k + kSliceCodes - 1) / kSliceCodes;
+  if (S > sms || S > kMaxSlices) return false;
+  int64_t C = sms / S;
+  int64_t rc = ((n + C - 1) / C + 15) / 16 * 16;
+  if (rc < kLutMinRows) return false;
+  C = (n + rc - 1) / rc;
+  if (C * S * rc > (int64_t(1) << 31)) return false;
+  sh.S = (int)S;
+  sh.C = (int)C;
+  sh.rc = (int)rc;
+  sh.part_rows = (int)(((rc + S - 1) / S + 15) / 16 * 16);
+  return true;
+}
+
+static int64_t lut_ws_bytes(const lut::Shape& sh) {
+  const int64_t parts = (int64_t)sh.C * sh.S * sh.rc * 4;
+  return (parts + (int64_t)sh.C * sh.S * 4 + 255) / 256 * 256;
+}
+
+int64_t gemv_lut_workspace_bytes(const bonsai_weights* w) {
+  lut::Shape sh;
+  return lut_shape(w, sh) ? lut_ws_bytes(sh) : 0;
+}
+
+// UNSUPPORTED when the shape does not take the tables or the workspace is
+// smaller than gemv_lut_workspace_bytes (nothing launched then).
+bonsai_status gemv_lut_launch(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
+                              bool swiglu, void* ws, int64_t ws_bytes, cudaStream_t stream) {
+  using namespace lut;
+  Shape sh;
+  if (!ws || !lut_shape(w, sh) || ws_bytes < lut_ws_bytes(sh)) return BONSAI_ERR_UNSUPPORTED;
+  Params p{};
+  p.packed = static_cast<const uint8_t*>(w->packed);
+  p.scales = reinterpret_cast<const __half*>(w->scales);
+  p.x = reinterpret_cast<const __half*>(x);
+  p.y = reinterpret_cast<__half*>(y);
+  p.ws = static_cast<float*>(ws);
+  p.cnt = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) +
+                                          (int64_t)sh.C * sh.S * sh.rc * 4);
+  p.row_bytes = w->row_bytes;
+  p.n = (int)w->n;
+  p.k = (int)w->k;
+  p.G = (int)(w->k / 128);
+  p.S = sh.S;
+  p.C = sh.C;
+  p.rc = sh.rc;
+  p.part_rows = sh.part_rows;
+  p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
+  p.swiglu = swiglu ? 1 : 0;
+  if (ensure_dynamic_smem((const void*)gemv_ter_lut_kernel, kSmem) != cudaSuccess)
+    return BONSAI_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(sh.C * sh.S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&p};
+  return cuda_status(cudaLaunchKernelExC(&cfg, (const void*)gemv_ter_lut_kernel, args));
+}
+
+}  // namespace bonsai
