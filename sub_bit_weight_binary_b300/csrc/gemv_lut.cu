@@ -140,33 +140,48 @@ __host__ __device__ constexpr int edge_low_digits(int lane) {
   return lane == 6 ? 3 : lane == 12 ? 1 : lane == 19 ? 4 : lane == 25 ? 2 : 0;
 }
 
-// Stage i of the chunk (rows row0+8i .. row0+8i+7, slice s) into the ring
-// slot at dst, issued by one warp: the weights as 8 rows x 8 pieces of 16
-// bytes (two per lane), the scales of the 16-group window from group sx as
-// 8 rows x 2 pieces (lanes 0..15). Rows past n re-read row n-1 (their sums
-// are never used); bytes past the row and groups past k/128 read as zero.
-__device__ __forceinline__ void load_stage(const Params& p, uint32_t dst, int row0, int i, int s,
-                                           int sx, int lane) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int piece = lane + 32 * h, r = piece >> 3, col = piece & 7;
-    int row = row0 + kRows * i + r;
-    row = row < p.n ? row : p.n - 1;
+// A warp's copies of one stage (8 rows x 128 bytes of weights, and the 8
+// rows' 16-group scale window from group sx) into a ring slot: two 16-byte
+// pieces of weights per lane (rows r and r+4, piece col of the row's slice),
+// one piece of scales for lanes 0..15. The per-lane offsets are fixed for
+// the kernel; bytes past the row and groups past k/128 read as zero, and
+// rows past n re-read row n-1 (their sums are never used).
+struct StageCopy {
+  const uint8_t* w;      // weights of row 0 of the chunk, at this lane's piece
+  const __half* sc;      // scales of row 0 of the chunk, at this lane's piece
+  long long row_bytes;
+  int G, n, r_w, r_s;
+  uint32_t wbytes, sbytes, dw, ds;
+
+  __device__ __forceinline__ StageCopy(const Params& p, int row0, int s, int sx, int lane) {
+    const int col = lane & 7;
+    r_w = lane >> 3;
+    r_s = lane >> 1;
     const long long off = (long long)s * kSliceBytes + 16 * col;
-    const bool in = off < p.row_bytes;
-    cp16(dst + r * kSliceBytes + 16 * col, p.packed + (size_t)row * p.row_bytes + (in ? off : 0),
-         in ? 16u : 0u);
+    wbytes = off < p.row_bytes ? 16u : 0u;
+    w = p.packed + (size_t)row0 * p.row_bytes + (wbytes ? off : 0);
+    const int g0 = sx + 8 * (lane & 1);
+    sbytes = (lane < 16 && g0 < p.G) ? 16u : 0u;
+    sc = p.scales + (size_t)row0 * p.G + (g0 < p.G ? g0 : 0);
+    row_bytes = p.row_bytes;
+    G = p.G;
+    n = p.n - row0;  // rows of the chunk that exist (and beyond)
+    dw = r_w * kSliceBytes + 16 * col;
+    ds = kStageW + (r_s & 7) * kScaleRow + 16 * (lane & 1);
   }
-  if (lane < 16) {
-    const int r = lane >> 1, hh = lane & 1;
-    int row = row0 + kRows * i + r;
-    row = row < p.n ? row : p.n - 1;
-    const int g0 = sx + 8 * hh;
-    const bool in = g0 < p.G;
-    cp16(dst + kStageW + r * kScaleRow + 16 * hh, p.scales + (size_t)row * p.G + (in ? g0 : 0),
-         in ? 16u : 0u);
+  // stage i: rows 8i .. 8i+7 of the chunk
+  __device__ __forceinline__ void issue(uint32_t dst, int i, int lane) const {
+    int ra = kRows * i + r_w, rb = ra + 4, rs = kRows * i + (r_s & 7);
+    if (kRows * i + kRows > n) {
+      ra = min(ra, n - 1);
+      rb = min(rb, n - 1);
+      rs = min(rs, n - 1);
+    }
+    cp16(dst + dw, w + (size_t)ra * row_bytes, wbytes);
+    cp16(dst + dw + 4 * kSliceBytes, w + (size_t)rb * row_bytes, wbytes);
+    if (lane < 16) cp16(dst + ds, sc + (size_t)rs * G, sbytes);
   }
-}
+};
 
 // Tables of the CTA's slice from x (FP32, zero past K). T: for the 128 byte
 // positions, every byte value's sum over the codes below the position's
@@ -240,23 +255,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // weights never depend on earlier work on the stream: with the prefetch
   // flag the first stages stream in while the previous kernel finishes
+  const StageCopy cpy(p, row0, s, sx, lane);
   if (!p.prefetch) pdl_wait();
   for (int d = 0; d < kDepth; ++d) {
-    if (d < mine) load_stage(p, ring + d * kStageBytes, row0, warp + kWarps * d, s, sx, lane);
+    if (d < mine) cpy.issue(ring + d * kStageBytes, warp + kWarps * d, lane);
     cp_commit();
   }
 
   // lane constants
   const int js = edge_byte(lane);
-  const uint32_t magic = lane == 6 ? 2428u : lane == 12 ? 21846u : lane == 19 ? 810u
-                         : lane == 25 ? 7282u : 0u;  // ceil(2^16 / 3^k)
+  // upper-digit index byte / 3^k as the high word of byte * ceil(2^16 / 3^k) * 2^16
+  const uint32_t magic = (lane == 6 ? 2428u : lane == 12 ? 21846u : lane == 19 ? 810u
+                          : lane == 25 ? 7282u : 0u) << 16;
   const float b1 = (js >= 0 && 1 > js) ? 1.f : 0.f;  // byte 1..3 wholly above the edge
   const float b2 = (js >= 0 && 2 > js) ? 1.f : 0.f;
   const float b3 = (js >= 0 && 3 > js) ? 1.f : 0.f;
   const float a1 = 1.f - b1, a2 = 1.f - b2, a3 = 1.f - b3;
-  // table address of byte j: tq[j] + (byte << 8) (pair j>>1, half j&1, lane)
-  const uint32_t tq0 = sbase + kOffT + 4u * lane, tq1 = tq0 + 128u;
-  const uint32_t tq2 = tq0 + kPairBytes, tq3 = tq1 + kPairBytes;
+  // table address of byte j: the pair's base (the same for every lane) plus
+  // PRMT(word, c) = byte << 8 | the lane's offset in its half of the row
+  const uint32_t tb0 = sbase + kOffT, tb1 = tb0 + kPairBytes;
+  const uint32_t c0 = 4u * lane, c1 = 128u + 4u * lane;
   const uint32_t hq = sbase + kOffH + 4u * lane;
   const uint32_t sel_e = 0x4440u | uint32_t(js < 0 ? 0 : js);
   const int g = (20 * lane) >> 7;  // the lane's (lower) group in the slice
@@ -267,32 +285,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   float* part = p.ws + (size_t)(c * p.S + s) * p.rc;
-  for (int j = 0; j < mine; ++j) {
-    const int jn = j + kDepth;
-    if (jn < mine)
-      load_stage(p, ring + (jn % kWarpSlots) * kStageBytes, row0, warp + kWarps * jn, s, sx, lane);
-    cp_commit();
-    cp_wait<kDepth>();  // this lane's copies of stage j have landed
-    __syncwarp();       // and every other lane's
-    const uint32_t st = ring + (j % kWarpSlots) * kStageBytes + opaque_zero();
-    float cr[kRows];
+  // One stage's rows in two phases, so that no shuffle sits between one row's
+  // loads and the next row's: first every shared-memory load of the 8 rows,
+  // then the arithmetic with the 8 hand-over shuffles back to back.
+  struct Loads {
+    float v0[kRows], v1[kRows], v2[kRows], v3[kRows], h[kRows], sc[kRows];
+  };
+  auto stage_loads = [&](uint32_t st, Loads& L) {
+    uint32_t w[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) w[r] = lds_u32(st + r * kSliceBytes + 4 * lane);
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
-      const uint32_t w = lds_u32(st + r * kSliceBytes + 4 * lane);
-      const float v0 = lds_f32(tq0 + prmt(w, 0u, 0x4404u));
-      const float v1 = lds_f32(tq1 + prmt(w, 0u, 0x4414u));
-      const float v2 = lds_f32(tq2 + prmt(w, 0u, 0x4424u));
-      const float v3 = lds_f32(tq3 + prmt(w, 0u, 0x4434u));
-      const uint32_t e = prmt(w, 0u, sel_e);
-      const float h = lds_f32(hq + (((e * magic) >> 9) & ~127u));
-      const float hs = fmaf(b3, v3, fmaf(b2, v2, fmaf(b1, v1, h)));
-      const float own = fmaf(a3, v3, fmaf(a2, v2, fmaf(a1, v1, v0)));
-      const float hp = __shfl_up_sync(0xFFFFFFFFu, hs, 1);  // lane 0: its own, 0
-      const float sc = lds_h2f(st + kStageW + r * kScaleRow + so);
-      cr[r] = sc * (own + hp);
+      L.v0[r] = lds_f32(tb0 + prmt(w[r], c0, 0x5504u));
+      L.v1[r] = lds_f32(tb0 + prmt(w[r], c1, 0x5514u));
+      L.v2[r] = lds_f32(tb1 + prmt(w[r], c0, 0x5524u));
+      L.v3[r] = lds_f32(tb1 + prmt(w[r], c1, 0x5534u));
+      L.h[r] = lds_f32(hq + 128u * __umulhi(prmt(w[r], 0u, sel_e), magic));
+      L.sc[r] = lds_h2f(st + kStageW + r * kScaleRow + so);
     }
-    // transposed butterfly over the 32 lanes: lanes 4R..4R+3 end with row R
-    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+  };
+  auto stage_values = [&](const Loads& L, float (&cr)[kRows]) {
+    float hs[kRows], own[kRows], hp[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      hs[r] = fmaf(b3, L.v3[r], fmaf(b2, L.v2[r], fmaf(b1, L.v1[r], L.h[r])));
+      own[r] = fmaf(a3, L.v3[r], fmaf(a2, L.v2[r], fmaf(a1, L.v1[r], L.v0[r])));
+    }
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) hp[r] = __shfl_up_sync(0xFFFFFFFFu, hs[r], 1);  // lane 0: 0
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) cr[r] = L.sc[r] * (own[r] + hp[r]);
+  };
+  // transposed butterfly over the 32 lanes (lanes 4R..4R+3 end with row R)
+  // and the stage's 8 partial sums to the workspace
+  const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+  auto reduce_store = [&](const float (&cr)[kRows], int stage) {
     float t4[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -310,23 +338,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     float v = (h4 ? t2[1] : t2[0]) + __shfl_xor_sync(0xFFFFFFFFu, h4 ? t2[0] : t2[1], 4);
     v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
     v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    if ((lane & 3) == 0) part[(warp + kWarps * j) * kRows + (lane >> 2)] = v;
+    if ((lane & 3) == 0) part[stage * kRows + (lane >> 2)] = v;
+  };
+  // software pipeline: stage j's lookups, then stage j-1's butterfly, so the
+  // butterfly's dependent shuffles overlap the next stage's loads
+  float prev[kRows];
+  for (int j = 0; j < mine; ++j) {
+    const int jn = j + kDepth;
+    if (jn < mine) cpy.issue(ring + (jn % kWarpSlots) * kStageBytes, warp + kWarps * jn, lane);
+    cp_commit();
+    cp_wait<kDepth>();  // this lane's copies of stage j have landed
+    __syncwarp();       // and every other lane's
+    Loads L;
+    stage_loads(ring + (j % kWarpSlots) * kStageBytes + opaque_zero(), L);
+    if (j > 0) reduce_store(prev, warp + kWarps * (j - 1));  // overlaps the loads
+    float cur[kRows];
+    stage_values(L, cur);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) prev[r] = cur[r];
     __syncwarp();  // the slot is refilled by the next iteration's copies
   }
+  if (mine > 0) reduce_store(prev, warp + kWarps * (mine - 1));
   cp_wait<0>();
-  __threadfence();  // this thread's partials before the arrival below
-  __syncthreads();
+  __syncthreads();  // every partial of the CTA is written (program order)
 
-  // arrivals: one counter per part of the chunk's rows
+  // arrivals: one counter per part of the chunk's rows. Release: the CTA's
+  // partials before the arrival; acquire: the other CTAs' partials after it
+  // (the barrier below extends both to the whole CTA).
   unsigned int* flags = reinterpret_cast<unsigned int*>(smem + kOffFlags);
   if (threadIdx.x < p.S) {
     unsigned int* ctr = p.cnt + c * p.S + threadIdx.x;
-    const unsigned int old = atomicAdd(ctr, 1u);
+    unsigned int old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(ctr)
+                 : "memory");
     const bool last = old == unsigned(p.S - 1);
-    if (last) {
-      *ctr = 0u;  // every CTA of the chunk has arrived: re-arm for the next call
-      __threadfence();
-    }
+    if (last) *ctr = 0u;  // every CTA of the chunk has arrived: re-arm for the next call
     flags[threadIdx.x] = last ? 1u : 0u;
   }
   __syncthreads();
@@ -340,41 +388,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = o / span; u >= 0; --u)  // the (o/span)-th completed part
       do ++q; while (!flags[q]);
     const int oi = o - (o / span) * span;
-    if (!p.swiglu) {
-      const int r = q * p.part_rows + oi;
-      if (r >= rows) continue;
-      float sum = 0.f;
-      for (int j0 = 0; j0 < p.S; j0 += 8) {  // 8 loads in flight, added in slice order
-        float v[8];
+    // row of the output (the gate row with swiglu: 8 gate rows, then the 8
+    // up rows of the same features, per 16-row block)
+    const int f = q * span + oi;
+    const int r = p.swiglu ? (f >> 3) * 16 + (f & 7) : f;
+    if (r >= rows) continue;
+    float a = 0.f, b = 0.f;
+    for (int j0 = 0; j0 < p.S; j0 += 8) {  // 8 (16) loads in flight, added in slice order
+      float va[8], vb[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          v[u] = j0 + u < p.S ? __ldcg(base + (size_t)(j0 + u) * p.rc + r) : 0.f;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) sum += v[u];
+      for (int u = 0; u < 8; ++u) {
+        const bool in = j0 + u < p.S;
+        const float* src = base + (size_t)(j0 + u) * p.rc + r;
+        va[u] = in ? __ldcg(src) : 0.f;
+        vb[u] = in && p.swiglu ? __ldcg(src + 8) : 0.f;
       }
-      p.y[row0 + r] = __float2half_rn(sum);
-    } else {
-      // 16-row blocks: 8 gate rows, then the 8 up rows of the same features
-      const int f = q * (p.part_rows / 2) + oi;
-      const int r = (f >> 3) * 16 + (f & 7);
-      if (r >= rows) continue;
-      float gs = 0.f, us = 0.f;
-      for (int j0 = 0; j0 < p.S; j0 += 8) {
-        float vg[8], vu[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const bool in = j0 + u < p.S;
-          vg[u] = in ? __ldcg(base + (size_t)(j0 + u) * p.rc + r) : 0.f;
-          vu[u] = in ? __ldcg(base + (size_t)(j0 + u) * p.rc + r + 8) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          gs += vg[u];
-          us += vu[u];
-        }
+      for (int u = 0; u < 8; ++u) {
+        a += va[u];
+        b += vb[u];
       }
-      p.y[row0 / 2 + f] = __float2half_rn(silu(gs) * us);
     }
+    if (p.swiglu) p.y[row0 / 2 + f] = __float2half_rn(silu(a) * b);
+    else p.y[row0 + r] = __float2half_rn(a);
   }
 }
 
@@ -385,8 +421,12 @@ struct Shape {
 
 }  // namespace lut
 
-// Rows per CTA below which the tables cost more than they save.
-constexpr int kLutMinRows = 192;
+// Rows per CTA below which the streaming kernel is faster: the tables and the
+// cross-block sums cost ~3.5 us per launch (measured on B300: ~6.5 ns per row
+// of 640 codes in the loop, 13.3 us for 976 rows against 13.9 us for the
+// streaming kernel), so only products of about a thousand rows per block
+// and slice gain.
+constexpr int kLutMinRows = 768;
 
 static bool lut_shape(const bonsai_weights* w, lut::Shape& sh) {
   using namespace lut;

@@ -4,9 +4,10 @@ with m = 1) against the oracle (needs a GPU).
 
 Shapes: the decode products of the pages' 27B decoder (N=17408 x K=5120, the
 down product N=5120 x K=17408 with a partial last 640-code slice), K=1024
-and K=3072 (partial last slice, ragged last chunk of rows), rows with few or
-no nonzero codes, activations over many binades, and the gated feed-forward
-epilogue."""
+and K=3072 (partial last slice, ragged last chunk of rows, a last stage of
+4 rows), rows with few or no nonzero codes, activations over many binades,
+and the gated feed-forward epilogue. The kernel takes products with at
+least 768 rows per thread block, hence the row counts."""
 import numpy as np
 import pytest
 
@@ -59,7 +60,7 @@ def ternary_from_codes(codes, seed):
     return sb.Weights(TER, n, k, packed_gpu, dev(scales)), oracle.pack_ternary(codes), scales
 
 
-@pytest.mark.parametrize("n,k", [(17408, 5120), (5120, 17408), (14300, 1024), (6000, 3072)])
+@pytest.mark.parametrize("n,k", [(17408, 5120), (5120, 17408), (57000, 1024), (22300, 3072)])
 def test_lut_full(n, k):
     """Every output against the oracle; a second call is bit-identical and
     the counters are zero again after each call."""
@@ -106,11 +107,14 @@ def test_lut_agrees_with_streaming_kernel():
 def test_lut_sparse_and_zero_rows(per_mille):
     """Rows with few (or no) nonzero codes meet the bound against their own
     small norm; all-zero rows give exactly zero."""
-    n, k = 3600, 5120
-    wr = synth.words(320 + per_mille, 0x51, 0, n * k)
-    keep = (wr >> np.uint64(54)) < np.uint64(per_mille * 1024 // 1000)
-    codes = np.where(keep, np.where((wr & np.uint64(1)) == 1, 1, -1), 0).astype(np.int8)
-    codes = codes.reshape(n, k)
+    n, k = 14000, 5120
+    codes = np.empty((n, k), dtype=np.int8)
+    for r0 in range(0, n, 1000):  # in row blocks: bounded host memory
+        rows = min(1000, n - r0)
+        wr = synth.words(320 + per_mille, 0x51, r0 * k, rows * k)
+        keep = (wr >> np.uint64(54)) < np.uint64(per_mille * 1024 // 1000)
+        codes[r0:r0 + rows] = np.where(keep, np.where((wr & np.uint64(1)) == 1, 1, -1),
+                                       0).astype(np.int8).reshape(rows, k)
     codes[::5] = 0  # every fifth row all zero
     w, packed, scales = ternary_from_codes(codes, 321)
     ws = sb.gemv_workspace(w)
@@ -128,7 +132,7 @@ def test_lut_sparse_and_zero_rows(per_mille):
 
 def test_lut_wide_range_activations():
     """x over seven binades, both signs, one tenth exact zeros."""
-    n, k = 4096, 5120
+    n, k = 14000, 5120
     w, packed, scales = weights(TER, 330, n, k)
     rng = np.random.default_rng(331)
     mag = 10.0 ** rng.uniform(-4, 3, size=k)
@@ -166,7 +170,7 @@ def test_lut_swiglu():
 
 def test_lut_gemm_ws_one_token_is_the_same_kernel():
     t = torch()
-    n, k = 6000, 3072
+    n, k = 22300, 3072
     w, _, _ = weights(TER, 350, n, k)
     x = dev(synth.gen_x(351, 1, k))
     ws = sb.gemv_workspace(w)
@@ -260,4 +264,5 @@ def test_lut_shapes_that_do_not_take_it():
     assert sb.bonsai_gemv_workspace_bytes(weights(BIN, 390, 17408, 5120)[0]) == 0
     assert sb.bonsai_gemv_workspace_bytes(weights(TER, 391, 17408, 1280)[0]) == 0
     assert sb.bonsai_gemv_workspace_bytes(weights(TER, 392, 512, 5120)[0]) == 0
+    assert sb.bonsai_gemv_workspace_bytes(weights(TER, 394, 4096, 5120)[0]) == 0
     assert sb.bonsai_gemv_workspace_bytes(weights(TER, 393, 17408, 5120)[0]) > 0
