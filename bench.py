@@ -129,7 +129,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no clock samples"]}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "samples": len(self.samples), "reasons": sorted(self.reasons),
-                "source": "nvml" if self.nv else "nvidia-smi -lms 20 during the timed region"}
+                "source": "nvml" if self.nv else "nvidia-smi -lms 20, timed region"}
 
 
 def dist_setup():
@@ -425,13 +425,13 @@ class GemvWorkload:
         return {"bound": "hbm", "kernel": kern,
                 "achieved": round(a, 1), "peak": pk["hbm"], "unit": "GB/s",
                 "frac": round(a / pk["hbm"], 4), "traffic": profiled_traffic(prof) if prof else None,
-                "peak_src": "%s HBM copy (burst)" % pk["src"],
+                "peak_src": "%s copy (burst)" % pk["src"],
                 "bytes_per_launch": self.unit_bytes()}
 
     def config(self):
         return {"workload": self.name, "m": 1, "k": self.k, "n": self.n,
                 "format": "ternary" if self.fmt == 2 else "binary",
-                "timing": "K launches captured in one CUDA graph",
+                "timing": "K launches in one CUDA graph",
                 "l2": "%d rotating weight replicas, %.0f MB > L2" % (
                     self.reps, self.reps * self.unit_bytes() / 1e6)}
 
@@ -455,7 +455,7 @@ class GemvWorkload:
             if el >= min_seconds or el > 30:
                 break
         done = passes * rows * (packed.shape[1] + 2 * (self.k // 128))
-        return done / el / 1e9, "GB/s", "%d passes over rows 0..%d of %d, 1 thread, %.1f s" % (
+        return done / el / 1e9, "GB/s", "%d passes, rows 0..%d of %d, 1 thread, %.1f s" % (
             passes, rows - 1, self.n, el)
 
 
@@ -493,7 +493,7 @@ def oracle_all_cores(fmt, n, k, seed, min_seconds=5.0):
     with mp.get_context("spawn").Pool(cores) as pool:
         res = pool.map(_oracle_rows_worker, jobs)
     gbs = sum(b / el for b, el in res) / 1e9
-    return gbs, cores, "%d procs x rows %d..%d of %d, %.0f s" % (
+    return gbs, cores, "%d procs x rows %d..%d of %d, %.0fs" % (
         cores, 0, rows - 1, n, min_seconds)
 
 
@@ -689,7 +689,7 @@ class SweepWorkload:
                     "gemv_binary_lut_kernel", self.layers * len(SWEEP_SHAPES))),
                 "achieved": round(a, 1),
                 "peak": pk["hbm"], "unit": "GB/s", "frac": round(a / pk["hbm"], 4),
-                "traffic": None, "peak_src": "%s HBM copy (burst)" % pk["src"],
+                "traffic": None, "peak_src": "%s copy (burst)" % pk["src"],
                 "bytes_per_token": self.unit_bytes()}
 
     def config(self):
@@ -956,7 +956,7 @@ class HadamardWorkload:
         return {"bound": "hbm", "kernel": "hadamard_kernel<7>", "achieved": round(a, 1),
                 "peak": pk["hbm"], "unit": "GB/s", "frac": round(a / pk["hbm"], 4),
                 "traffic": profiled_traffic("hadamard_m512_k5120_b128.md"),
-                "peak_src": "%s HBM copy (burst)" % pk["src"],
+                "peak_src": "%s copy (burst)" % pk["src"],
                 "bytes_per_launch": self.unit_bytes()}
 
     def config(self):
@@ -1201,7 +1201,7 @@ def run_ours(args, world, rank):
         "metric": METRIC, "value": round(val * world, 3), "unit": unit, "n_gpus": world,
         "steps": r["steps"], "warmup": args.warmup, "ms_per_step": round(ms / r["steps"], 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic (seeded generator; random weights)",
+        "data": "synthetic (seeded; random weights)",
         "config": dict(wl.config(), parallelism="replicas only, %d GPU(s)" % world),
         "roofline": wl.roofline(r, pk) if wl.kind != "xnor" else
         wl.roofline(r, pk, clk.report().get("sm_mhz")),
@@ -1223,8 +1223,9 @@ def run_ours(args, world, rank):
         # faster of the two) is the value; the prepared plan is beside it
         line["e2e"] = {"value": round(ee * world, 3), "unit": unit, "h2d_bytes_per_step": bi,
                        "d2h_bytes_per_step": bo, "steps": e2e_steps,
-                       "how": "median of %d runs of %d bonsai_gemv_host calls: pinned x in, y out" % (
-                           TIMED_REPS, e2e_steps),
+                       "how": "%s per step, pinned x in, y out; median of %d" % (
+                           "bonsai_gemv_host_ws" if getattr(wl, "ws", None) is not None
+                           else "bonsai_gemv_host", TIMED_REPS),
                        "plan": {"value": round(ev * world, 3), "how": "GemvHostPlan replay"}}
     sb.check()
     if rank == 0 and not args.no_cpu_baseline and world == 1 and hasattr(wl, "cpu_sample"):
