@@ -383,37 +383,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   int nf = 0;
   for (int q = 0; q < p.S; ++q) nf += flags[q] ? 1 : 0;
   const int span = p.swiglu ? p.part_rows / 2 : p.part_rows;  // outputs per part
-  for (int o = threadIdx.x; o < nf * span; o += kThreads) {
-    int q = -1;
-    for (int u = o / span; u >= 0; --u)  // the (o/span)-th completed part
-      do ++q; while (!flags[q]);
-    const int oi = o - (o / span) * span;
-    // row of the output (the gate row with swiglu: 8 gate rows, then the 8
-    // up rows of the same features, per 16-row block)
-    const int f = q * span + oi;
-    const int r = p.swiglu ? (f >> 3) * 16 + (f & 7) : f;
-    if (r >= rows) continue;
-    float a = 0.f, b = 0.f;
-    for (int j0 = 0; j0 < p.S; j0 += 8) {  // 8 (16) loads in flight, added in slice order
-      float va[8], vb[8];
+  const int total = nf * span;
+  // two outputs per thread and pass, all their partials loaded at once (one
+  // L2 round trip), each output's partials added in slice order
+  for (int o0 = threadIdx.x; o0 < total; o0 += 2 * kThreads) {
+    int rr[2], ff[2];
+    bool ok[2];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const bool in = j0 + u < p.S;
-        const float* src = base + (size_t)(j0 + u) * p.rc + r;
-        va[u] = in ? __ldcg(src) : 0.f;
-        vb[u] = in && p.swiglu ? __ldcg(src + 8) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        a += va[u];
-        b += vb[u];
+    for (int t = 0; t < 2; ++t) {
+      const int o = o0 + t * kThreads;
+      ok[t] = false;
+      rr[t] = ff[t] = 0;
+      if (o < total) {
+        int q = -1;
+        for (int u = o / span; u >= 0; --u)  // the (o/span)-th completed part
+          do ++q; while (!flags[q]);
+        // row of the output (the gate row with swiglu: 8 gate rows, then the
+        // 8 up rows of the same features, per 16-row block)
+        ff[t] = q * span + (o - (o / span) * span);
+        rr[t] = p.swiglu ? (ff[t] >> 3) * 16 + (ff[t] & 7) : ff[t];
+        ok[t] = rr[t] < rows;
       }
     }
-    if (p.swiglu) p.y[row0 / 2 + f] = __float2half_rn(silu(a) * b);
-    else p.y[row0 + r] = __float2half_rn(a);
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [output][gate or plain, up]
+    for (int j0 = 0; j0 < p.S; j0 += 8) {
+      float v[2][2][8];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const bool in = ok[t] && j0 + u < p.S && (hh == 0 || p.swiglu);
+            v[t][hh][u] = in ? __ldcg(base + (size_t)(j0 + u) * p.rc + rr[t] + 8 * hh) : 0.f;
+          }
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[t][hh] += v[t][hh][u];
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (!ok[t]) continue;
+      if (p.swiglu) p.y[row0 / 2 + ff[t]] = __float2half_rn(silu(acc[t][0]) * acc[t][1]);
+      else p.y[row0 + rr[t]] = __float2half_rn(acc[t][0]);
+    }
   }
 }
-
 
 struct Shape {
   int S, C, rc, part_rows;
