@@ -432,7 +432,7 @@ class GemvWorkload:
         return {"workload": self.name, "m": 1, "k": self.k, "n": self.n,
                 "format": "ternary" if self.fmt == 2 else "binary",
                 "timing": "K launches in one CUDA graph",
-                "l2": "%d rotating weight replicas, %.0f MB > L2" % (
+                "l2": "%d weight replicas, %.0f MB > L2" % (
                     self.reps, self.reps * self.unit_bytes() / 1e6)}
 
     def cpu_sample(self, min_seconds=10.0, max_rows=None):
