@@ -418,9 +418,10 @@ class GemvWorkload:
         a = self.unit_bytes() / (r["kernel_ms"] / 1e3) / 1e9
         prof = {(2, 17408, 5120, False): "gemv_ternary_k5120_n17408.md",
                 (2, 17408, 5120, True): "gemv_ter_lut_k5120_n17408.md",
+                (1, 17408, 5120, True): "gemv_bin_lut_k5120_n17408.md",
                 (1, 17408, 5120, False): "gemv_binary_k5120_n17408.md"}.get(
                     (self.fmt, self.n, self.k, self.lut))
-        kern = "gemv_ter_lut_kernel" if self.lut else \
+        kern = ("gemv_%s_lut_kernel" % ("ter" if self.fmt == 2 else "bin")) if self.lut else \
             "gemv_%s_kernel" % ("ternary" if self.fmt == 2 else "binary")
         return {"bound": "hbm", "kernel": kern,
                 "achieved": round(a, 1), "peak": pk["hbm"], "unit": "GB/s",
@@ -686,7 +687,7 @@ class SweepWorkload:
                                            % (self.layers * len(SWEEP_SHAPES)) if self.plan else
                                            "%s (%d per token)" % (
                     "gemv_ternary_kernel / gemv_ter_lut_kernel" if self.fmt == 2 else
-                    "gemv_binary_lut_kernel", self.layers * len(SWEEP_SHAPES))),
+                    "gemv_binary_lut_kernel / gemv_bin_lut_kernel", self.layers * len(SWEEP_SHAPES))),
                 "achieved": round(a, 1),
                 "peak": pk["hbm"], "unit": "GB/s", "frac": round(a / pk["hbm"], 4),
                 "traffic": None, "peak_src": "%s copy (burst)" % pk["src"],

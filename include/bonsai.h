@@ -161,15 +161,16 @@ bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
                                uint16_t* x_dev, uint16_t* y_dev, uint16_t* y_host,
                                bonsai_stream stream);
 
-/* Workspace variants of bonsai_gemv and bonsai_gemv_host. For TERNARY
- * weights of a shape that takes it (k/128 a multiple of 8, and enough rows
- * to keep every SM busy; bonsai_gemv_workspace_bytes says which), the
- * product runs on a kernel that needs no operand per code: a packed byte
- * holds five codes, so x . w over them is one of 243 sums fixed by x alone
- * ("multiplication degenerates to addition and sign flip", 三值权重 page).
- * K is split into slices of 640 codes across thread blocks; each block
- * tabulates the sums of its slice in FP32 and then spends one table lookup
- * and one add per packed byte. Its FP32 partial sums per row go to the
+/* Workspace variants of bonsai_gemv and bonsai_gemv_host. For weights of a
+ * shape that takes it (k/128 a multiple of 8, and enough rows to keep every
+ * SM busy; bonsai_gemv_workspace_bytes says which), the product runs on a
+ * kernel that needs no operand per code: a packed ternary byte holds five
+ * codes (a binary byte eight), so x . w over them is one of 243 (256) sums
+ * fixed by x alone ("multiplication degenerates to addition and sign flip",
+ * 三值权重 page). K is split into slices of 640 (1024) codes across thread
+ * blocks; each block tabulates the sums of its slice in FP32 and then
+ * spends one table lookup and one add per packed byte. Its FP32 partial
+ * sums per row go to the
  * workspace, and the block that completes a part of the rows adds them in
  * slice order and rounds once to FP16. Results of two calls with the same
  * inputs are bit-identical; they differ from bonsai_gemv's only by the
@@ -185,10 +186,10 @@ bonsai_status bonsai_gemv_host(const bonsai_weights* w, const uint16_t* x_host,
  * Other arguments, errors and behaviour as bonsai_gemv / bonsai_gemv_host,
  * plus BONSAI_ERR_ALIGN for a workspace not 256-byte aligned.
  * bonsai_gemv_workspace_bytes returns 0 when the shape does not take the
- * table kernel (binary weights, k/128 not a multiple of 8, too few rows per
- * block) or w is invalid. bonsai_gemm_workspace_bytes(w, 1) returns the
- * same size, and bonsai_gemm_ws / bonsai_gemm_swiglu_ws with m = 1 run the
- * same kernel (with swiglu, its final sums give silu(g) * u). */
+ * table kernel (k/128 not a multiple of 8, too few rows per block) or w is
+ * invalid. bonsai_gemm_workspace_bytes(w, 1) returns the same size, and
+ * bonsai_gemm_ws / bonsai_gemm_swiglu_ws with m = 1 run the same kernel
+ * (with swiglu, its final sums give silu(g) * u). */
 int64_t bonsai_gemv_workspace_bytes(const bonsai_weights* w);
 bonsai_status bonsai_gemv_ws(const bonsai_weights* w, const uint16_t* x, uint16_t* y,
                              void* workspace, int64_t workspace_bytes,

@@ -1,5 +1,6 @@
-// gemv_lut.cu -- one-token ternary decode product through per-position tables
-// of partial sums, with K split across thread blocks.
+// gemv_lut.cu -- one-token decode product (ternary, and binary at the end of
+// the file) through per-position tables of partial sums, with K split
+// across thread blocks.
 //
 // "Multiplication degenerates to addition and sign flip" (三值权重 page): a
 // packed byte holds five codes, so x . w over those five codes is one of 243
@@ -433,6 +434,238 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ binary
+// The same structure for binary weights: a byte holds eight codes, so a
+// position's table has 256 entries (the sum of +-x over the eight codes,
+// bit i of the byte giving the sign of code i) and a slice is 1024 codes
+// (eight whole groups); a lane's 32 codes are a quarter of one group, so
+// there is no group edge inside a lane's word and no hand-over.
+constexpr int kBinSliceCodes = 1024;
+constexpr int kBinOffFlags = kOffX + kBinSliceCodes * 4;
+constexpr int kBinOffRing = kBinOffFlags + kMaxSlices * 4;
+constexpr int kBinSmem = kBinOffRing + kSlots * kStageBytes;
+static_assert(kBinOffRing % 128 == 0 && kBinSmem <= 232448, "binary layout fits one SM");
+
+// Entry e = a + 16*b: the low nibble (codes 0..3) in a, the high one (codes
+// 4..7) in b, sums A[a] + B[b]; thread q of a position writes b = q, q+4,
+// q+8, q+12.
+__device__ __forceinline__ void binary_rows(float* dst, const float (&xv)[8], int q) {
+  float A[16], Bv[4];
+#pragma unroll
+  for (int a = 0; a < 16; ++a) {
+    float v = (a & 1) ? xv[0] : -xv[0];
+    v += (a & 2) ? xv[1] : -xv[1];
+    v += (a & 4) ? xv[2] : -xv[2];
+    v += (a & 8) ? xv[3] : -xv[3];
+    A[a] = v;
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int bb = q + 4 * u;
+    float v = (bb & 1) ? xv[4] : -xv[4];
+    v += (bb & 2) ? xv[5] : -xv[5];
+    v += (bb & 4) ? xv[6] : -xv[6];
+    v += (bb & 8) ? xv[7] : -xv[7];
+    Bv[u] = v;
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    float* rb = dst + 16 * 64 * (q + 4 * u);
+#pragma unroll
+    for (int a = 0; a < 16; ++a) rb[a * 64] = A[a] + Bv[u];
+  }
+}
+
+__device__ __forceinline__ void build_tables_bin(const Params& p, uint8_t* smem, int s) {
+  float* xs = reinterpret_cast<float*>(smem + kOffX);
+  const int t = threadIdx.x;
+  for (int i = t; i < kBinSliceCodes; i += kThreads) {
+    const int kk = s * kBinSliceCodes + i;
+    xs[i] = kk < p.k ? __half2float(p.x[kk]) : 0.f;
+  }
+  __syncthreads();
+  const int pos = t & 127, q = t >> 7;
+  const int pj = pos >> 5, pl = pos & 31;
+  const int byte = 4 * pl + pj;
+  float xv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) xv[i] = xs[8 * byte + i];
+  binary_rows(reinterpret_cast<float*>(smem + kOffT + (pj >> 1) * kPairBytes + (pj & 1) * 128) + pl,
+              xv, q);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_bin_lut_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const int s = blockIdx.x % p.S, c = blockIdx.x / p.S;
+  const int row0 = c * p.rc;
+  const int rows = min(p.rc, p.n - row0);
+  const int nst = (rows + kRows - 1) / kRows;
+  const int mine = nst > warp ? (nst - warp + kWarps - 1) / kWarps : 0;  // stages warp, warp+16, ..
+  const int sx = 8 * s;  // the slice's eight groups: one 16-byte scale piece per row
+  const uint32_t ring = sbase + kBinOffRing + warp * kWarpSlots * kStageBytes;
+  pdl_launch_dependents();
+
+  // weights never depend on earlier work on the stream: with the prefetch
+  // flag the first stages stream in while the previous kernel finishes
+  const StageCopy cpy(p, row0, s, sx, lane);
+  if (!p.prefetch) pdl_wait();
+  for (int d = 0; d < kDepth; ++d) {
+    if (d < mine) cpy.issue(ring + d * kStageBytes, warp + kWarps * d, lane);
+    cp_commit();
+  }
+
+  // lane constants: table address of byte j as for ternary; the lane's 32
+  // codes are one quarter of a group, so one scale per row and no hand-over
+  const uint32_t tb0 = sbase + kOffT, tb1 = tb0 + kPairBytes;
+  const uint32_t c0 = 4u * lane, c1 = 128u + 4u * lane;
+  const uint32_t so = 2u * uint32_t(lane >> 2);
+
+  pdl_wait();  // x, y and the workspace are used by earlier work on the stream
+  build_tables_bin(p, smem, s);
+  __syncthreads();
+
+  float* part = p.ws + (size_t)(c * p.S + s) * p.rc;
+  // One stage's rows: every shared-memory load of the 8 rows first, then the
+  // arithmetic.
+  struct Loads {
+    float v0[kRows], v1[kRows], v2[kRows], v3[kRows], sc[kRows];
+  };
+  auto stage_loads = [&](uint32_t st, Loads& L) {
+    uint32_t w[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) w[r] = lds_u32(st + r * kSliceBytes + 4 * lane);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      L.v0[r] = lds_f32(tb0 + prmt(w[r], c0, 0x5504u));
+      L.v1[r] = lds_f32(tb0 + prmt(w[r], c1, 0x5514u));
+      L.v2[r] = lds_f32(tb1 + prmt(w[r], c0, 0x5524u));
+      L.v3[r] = lds_f32(tb1 + prmt(w[r], c1, 0x5534u));
+      L.sc[r] = lds_h2f(st + kStageW + r * kScaleRow + so);
+    }
+  };
+  auto stage_values = [&](const Loads& L, float (&cr)[kRows]) {
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) cr[r] = L.sc[r] * ((L.v0[r] + L.v1[r]) + (L.v2[r] + L.v3[r]));
+  };
+  // transposed butterfly over the 32 lanes (lanes 4R..4R+3 end with row R)
+  // and the stage's 8 partial sums to the workspace
+  const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+  auto reduce_store = [&](const float (&cr)[kRows], int stage) {
+    float t4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float keep = h16 ? cr[q + 4] : cr[q];
+      const float send = h16 ? cr[q] : cr[q + 4];
+      t4[q] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+    float t2[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float keep = h8 ? t4[q + 2] : t4[q];
+      const float send = h8 ? t4[q] : t4[q + 2];
+      t2[q] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+    float v = (h4 ? t2[1] : t2[0]) + __shfl_xor_sync(0xFFFFFFFFu, h4 ? t2[0] : t2[1], 4);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    if ((lane & 3) == 0) part[stage * kRows + (lane >> 2)] = v;
+  };
+  // software pipeline: stage j's lookups, then stage j-1's butterfly, so the
+  // butterfly's dependent shuffles overlap the next stage's loads
+  float prev[kRows];
+  for (int j = 0; j < mine; ++j) {
+    const int jn = j + kDepth;
+    if (jn < mine) cpy.issue(ring + (jn % kWarpSlots) * kStageBytes, warp + kWarps * jn, lane);
+    cp_commit();
+    cp_wait<kDepth>();  // this lane's copies of stage j have landed
+    __syncwarp();       // and every other lane's
+    Loads L;
+    stage_loads(ring + (j % kWarpSlots) * kStageBytes + opaque_zero(), L);
+    if (j > 0) reduce_store(prev, warp + kWarps * (j - 1));  // overlaps the loads
+    float cur[kRows];
+    stage_values(L, cur);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) prev[r] = cur[r];
+    __syncwarp();  // the slot is refilled by the next iteration's copies
+  }
+  if (mine > 0) reduce_store(prev, warp + kWarps * (mine - 1));
+  cp_wait<0>();
+  __syncthreads();  // every partial of the CTA is written (program order)
+
+  // arrivals: one counter per part of the chunk's rows. Release: the CTA's
+  // partials before the arrival; acquire: the other CTAs' partials after it
+  // (the barrier below extends both to the whole CTA).
+  unsigned int* flags = reinterpret_cast<unsigned int*>(smem + kBinOffFlags);
+  if (threadIdx.x < p.S) {
+    unsigned int* ctr = p.cnt + c * p.S + threadIdx.x;
+    unsigned int old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(ctr)
+                 : "memory");
+    const bool last = old == unsigned(p.S - 1);
+    if (last) *ctr = 0u;  // every CTA of the chunk has arrived: re-arm for the next call
+    flags[threadIdx.x] = last ? 1u : 0u;
+  }
+  __syncthreads();
+  // the parts this CTA completed, all rows at once
+  const float* base = p.ws + (size_t)c * p.S * p.rc;
+  int nf = 0;
+  for (int q = 0; q < p.S; ++q) nf += flags[q] ? 1 : 0;
+  const int span = p.swiglu ? p.part_rows / 2 : p.part_rows;  // outputs per part
+  const int total = nf * span;
+  // two outputs per thread and pass, all their partials loaded at once (one
+  // L2 round trip), each output's partials added in slice order
+  for (int o0 = threadIdx.x; o0 < total; o0 += 2 * kThreads) {
+    int rr[2], ff[2];
+    bool ok[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int o = o0 + t * kThreads;
+      ok[t] = false;
+      rr[t] = ff[t] = 0;
+      if (o < total) {
+        int q = -1;
+        for (int u = o / span; u >= 0; --u)  // the (o/span)-th completed part
+          do ++q; while (!flags[q]);
+        // row of the output (the gate row with swiglu: 8 gate rows, then the
+        // 8 up rows of the same features, per 16-row block)
+        ff[t] = q * span + (o - (o / span) * span);
+        rr[t] = p.swiglu ? (ff[t] >> 3) * 16 + (ff[t] & 7) : ff[t];
+        ok[t] = rr[t] < rows;
+      }
+    }
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [output][gate or plain, up]
+    for (int j0 = 0; j0 < p.S; j0 += 8) {
+      float v[2][2][8];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const bool in = ok[t] && j0 + u < p.S && (hh == 0 || p.swiglu);
+            v[t][hh][u] = in ? __ldcg(base + (size_t)(j0 + u) * p.rc + rr[t] + 8 * hh) : 0.f;
+          }
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[t][hh] += v[t][hh][u];
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (!ok[t]) continue;
+      if (p.swiglu) p.y[row0 / 2 + ff[t]] = __float2half_rn(silu(acc[t][0]) * acc[t][1]);
+      else p.y[row0 + rr[t]] = __float2half_rn(acc[t][0]);
+    }
+  }
+}
+
 struct Shape {
   int S, C, rc, part_rows;
 };
@@ -440,24 +673,30 @@ struct Shape {
 }  // namespace lut
 
 // Rows per CTA below which the streaming kernel is faster: the tables and the
-// cross-block sums cost ~3.5 us per launch (measured on B300: ~6.5 ns per row
-// of 640 codes in the loop, 13.3 us for 976 rows against 13.9 us for the
-// streaming kernel), so only products of about a thousand rows per block
-// and slice gain.
-constexpr int kLutMinRows = 768;
+// cross-block sums cost ~3.5-4 us per launch (measured on B300, ternary:
+// ~6.5 ns per row of 640 codes in the loop, 12.6 us for 976 rows against
+// 13.9 us for the streaming kernel), so only products of about a thousand
+// rows per block and slice gain. A binary row of a slice (1024 codes) costs
+// less than half a ternary one, against a streaming binary kernel that is
+// itself faster per code (measured: 9.0 against 8.75 us at 608 rows per
+// block, N=17408 K=5120; the 64-layer binary decode gains 16% with gate/up
+// and down on the tables).
+constexpr int kLutMinRowsTer = 768;
+constexpr int kLutMinRowsBin = 640;
 
 static bool lut_shape(const bonsai_weights* w, lut::Shape& sh) {
   using namespace lut;
-  if (w->format != BONSAI_FMT_TERNARY) return false;
+  const bool bin = w->format == BONSAI_FMT_BINARY;
   const int64_t k = w->k, n = w->n;
   if ((k / 128) % 8) return false;  // the scale rows' pitch must be 16-byte aligned
   const int sms = device_sm_count();
-  if (device_max_smem_optin() < kSmem) return false;
-  const int64_t S = (k + kSliceCodes - 1) / kSliceCodes;
+  if (device_max_smem_optin() < (bin ? kBinSmem : kSmem)) return false;
+  const int64_t sc = bin ? kBinSliceCodes : kSliceCodes;
+  const int64_t S = (k + sc - 1) / sc;
   if (S > sms || S > kMaxSlices) return false;
   int64_t C = sms / S;
   int64_t rc = ((n + C - 1) / C + 15) / 16 * 16;
-  if (rc < kLutMinRows) return false;
+  if (rc < (bin ? kLutMinRowsBin : kLutMinRowsTer)) return false;
   C = (n + rc - 1) / rc;
   if (C * S * rc > (int64_t(1) << 31)) return false;
   sh.S = (int)S;
@@ -502,12 +741,14 @@ bonsai_status gemv_lut_launch(const bonsai_weights* w, const uint16_t* x, uint16
   p.part_rows = sh.part_rows;
   p.prefetch = (w->flags & BONSAI_WEIGHTS_PREFETCH) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
-  if (ensure_dynamic_smem((const void*)gemv_ter_lut_kernel, kSmem) != cudaSuccess)
-    return BONSAI_ERR_CUDA;
+  const bool bin = w->format == BONSAI_FMT_BINARY;
+  const void* fn = bin ? (const void*)gemv_bin_lut_kernel : (const void*)gemv_ter_lut_kernel;
+  const int smem = bin ? kBinSmem : kSmem;
+  if (ensure_dynamic_smem(fn, smem) != cudaSuccess) return BONSAI_ERR_CUDA;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(sh.C * sh.S);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -515,7 +756,7 @@ bonsai_status gemv_lut_launch(const bonsai_weights* w, const uint16_t* x, uint16
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&p};
-  return cuda_status(cudaLaunchKernelExC(&cfg, (const void*)gemv_ter_lut_kernel, args));
+  return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
 }
 
 }  // namespace bonsai

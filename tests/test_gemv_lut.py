@@ -1,4 +1,4 @@
-"""One-token ternary product on the per-position table kernel
+"""One-token binary and ternary products on the per-position table kernels
 (bonsai_gemv_ws, bonsai_gemv_host_ws, bonsai_gemm_ws / bonsai_gemm_swiglu_ws
 with m = 1) against the oracle (needs a GPU).
 
@@ -6,8 +6,9 @@ Shapes: the decode products of the pages' 27B decoder (N=17408 x K=5120, the
 down product N=5120 x K=17408 with a partial last 640-code slice), K=1024
 and K=3072 (partial last slice, ragged last chunk of rows, a last stage of
 4 rows), rows with few or no nonzero codes, activations over many binades,
-and the gated feed-forward epilogue. The kernel takes products with at
-least 768 rows per thread block, hence the row counts."""
+and the gated feed-forward epilogue; binary at the same decode shapes and
+K=1024 / 3072. The kernels take products with at least 768 (ternary) or 640
+(binary) rows per thread block, hence the row counts."""
 import numpy as np
 import pytest
 
@@ -35,10 +36,11 @@ def sms():
     return torch().cuda.get_device_properties(0).multi_processor_count
 
 
-def counters(ws, n, k):
+def counters(ws, n, k, fmt=None):
     """The workspace's arrival counters (after the partial sums): all zero
-    after a completed call. Layout: slices of 640 codes, chunks of rc rows."""
-    s = -(-k // 640)
+    after a completed call. Layout: slices of 640 (ternary) or 1024 (binary)
+    codes, chunks of rc rows."""
+    s = -(-k // (1024 if fmt == BIN else 640))
     c0 = sms() // s
     rc = -(-(-(-n // c0)) // 16) * 16
     c = -(-n // rc)
@@ -60,12 +62,14 @@ def ternary_from_codes(codes, seed):
     return sb.Weights(TER, n, k, packed_gpu, dev(scales)), oracle.pack_ternary(codes), scales
 
 
-@pytest.mark.parametrize("n,k", [(17408, 5120), (5120, 17408), (57000, 1024), (22300, 3072)])
-def test_lut_full(n, k):
+@pytest.mark.parametrize("fmt,n,k", [(TER, 17408, 5120), (TER, 5120, 17408), (TER, 57000, 1024),
+                                     (TER, 22300, 3072), (BIN, 20000, 5120), (BIN, 5120, 17408),
+                                     (BIN, 95000, 1024), (BIN, 40000, 3072)])
+def test_lut_full(fmt, n, k):
     """Every output against the oracle; a second call is bit-identical and
     the counters are zero again after each call."""
     t = torch()
-    w, packed, scales = weights(TER, 300 + k % 11, n, k)
+    w, packed, scales = weights(fmt, 300 + k % 11, n, k)
     x = synth.gen_x(301 + n % 7, 1, k)
     ws = sb.gemv_workspace(w)
     assert ws is not None, "this shape should take the table kernel"
@@ -73,23 +77,24 @@ def test_lut_full(n, k):
     y2 = Guarded((n,), t.float16)
     sb.bonsai_gemv_ws(w, dev(x[0]), y1.t, ws)
     assert sb.bonsai_check_async() == 0
-    assert counters(ws, n, k).max() == 0
+    assert counters(ws, n, k, fmt).max() == 0
     sb.bonsai_gemv_ws(w, dev(x[0]), y2.t, ws)
     assert sb.bonsai_check_async() == 0
-    assert counters(ws, n, k).max() == 0
+    assert counters(ws, n, k, fmt).max() == 0
     assert t.equal(y1.t.view(t.int16), y2.t.view(t.int16))
-    y_ref, nrm = oracle.linear(TER, packed, scales, x)
-    assert_close(host(y1.t), y_ref[0], nrm[0], "table kernel n=%d k=%d" % (n, k))
+    y_ref, nrm = oracle.linear(fmt, packed, scales, x)
+    assert_close(host(y1.t), y_ref[0], nrm[0], "table kernel fmt=%d n=%d k=%d" % (fmt, n, k))
     y1.check()
     y2.check()
 
 
-def test_lut_agrees_with_streaming_kernel():
+@pytest.mark.parametrize("fmt", [BIN, TER])
+def test_lut_agrees_with_streaming_kernel(fmt):
     """The table kernel and bonsai_gemv's kernel each meet the bound, so they
     agree within twice it."""
     t = torch()
-    n, k = 17408, 5120
-    w, packed, scales = weights(TER, 310, n, k)
+    n, k = 20000 if fmt == BIN else 17408, 5120
+    w, packed, scales = weights(fmt, 310, n, k)
     x = dev(synth.gen_x(311, 1, k)[0])
     ws = sb.gemv_workspace(w)
     y0 = t.empty(n, dtype=t.float16, device="cuda")
@@ -97,7 +102,7 @@ def test_lut_agrees_with_streaming_kernel():
     sb.bonsai_gemv(w, x, y0)
     sb.bonsai_gemv_ws(w, x, y1, ws)
     assert sb.bonsai_check_async() == 0
-    _, nrm = oracle.linear(TER, packed, scales, host(x)[None, :], n_sel=np.arange(0, n, 7))
+    _, nrm = oracle.linear(fmt, packed, scales, host(x)[None, :], n_sel=np.arange(0, n, 7))
     a = f16(host(y0))[::7]
     b = f16(host(y1))[::7]
     assert np.all(np.abs(a - b) <= 2 * TOL * nrm[0] + 1e-30)
@@ -130,10 +135,11 @@ def test_lut_sparse_and_zero_rows(per_mille):
     y.check()
 
 
-def test_lut_wide_range_activations():
+@pytest.mark.parametrize("fmt", [BIN, TER])
+def test_lut_wide_range_activations(fmt):
     """x over seven binades, both signs, one tenth exact zeros."""
-    n, k = 14000, 5120
-    w, packed, scales = weights(TER, 330, n, k)
+    n, k = 20000 if fmt == BIN else 17408, 5120
+    w, packed, scales = weights(fmt, 330, n, k)
     rng = np.random.default_rng(331)
     mag = 10.0 ** rng.uniform(-4, 3, size=k)
     xv = (mag * rng.choice([-1.0, 1.0], size=k)).astype(np.float16)
@@ -144,17 +150,19 @@ def test_lut_wide_range_activations():
     y = Guarded((n,), torch().float16)
     sb.bonsai_gemv_ws(w, dev(x[0]), y.t, ws)
     assert sb.bonsai_check_async() == 0
-    y_ref, nrm = oracle.linear(TER, packed, scales, x)
-    assert_close(host(y.t), y_ref[0], nrm[0], "table kernel wide-range x")
+    y_ref, nrm = oracle.linear(fmt, packed, scales, x)
+    assert_close(host(y.t), y_ref[0], nrm[0], "table kernel wide-range x fmt=%d" % fmt)
     y.check()
 
 
-def test_lut_swiglu():
-    """Gated feed-forward input of one token (F=8704 features from 2F
-    interleaved rows): every h against the oracle's silu(g)*u bound."""
+@pytest.mark.parametrize("fmt", [BIN, TER])
+def test_lut_swiglu(fmt):
+    """Gated feed-forward input of one token (F=8704 ternary / 10240 binary
+    features from 2F interleaved rows): every h against the oracle's
+    silu(g)*u bound."""
     t = torch()
-    f, k = 8704, 5120
-    w, packed, scales = weights(TER, 340, 2 * f, k)
+    f, k = 10240 if fmt == BIN else 8704, 5120
+    w, packed, scales = weights(fmt, 340, 2 * f, k)
     x = synth.gen_x(341, 1, k)
     ws = sb.gemv_workspace(w)
     assert ws is not None
@@ -162,9 +170,9 @@ def test_lut_swiglu():
     h = Guarded((1, f), t.float16)
     sb.bonsai_gemm_swiglu_ws(w, dev(x), h.t, ws)
     assert sb.bonsai_check_async() == 0
-    assert counters(ws, 2 * f, k).max() == 0
-    href, g, u, ng, nu = oracle.swiglu(TER, packed, scales, x)
-    assert_swiglu_close(host(h.t), href, g, u, ng, nu, "table kernel swiglu")
+    assert counters(ws, 2 * f, k, fmt).max() == 0
+    href, g, u, ng, nu = oracle.swiglu(fmt, packed, scales, x)
+    assert_swiglu_close(host(h.t), href, g, u, ng, nu, "table kernel swiglu fmt=%d" % fmt)
     h.check()
 
 
@@ -259,9 +267,12 @@ def test_lut_rejects_unaligned_workspace():
 
 
 def test_lut_shapes_that_do_not_take_it():
-    """Binary weights, K/128 not a multiple of 8, and too few rows per block
-    report no workspace."""
-    assert sb.bonsai_gemv_workspace_bytes(weights(BIN, 390, 17408, 5120)[0]) == 0
+    """K/128 not a multiple of 8 and too few rows per block report no
+    workspace."""
+    assert sb.bonsai_gemv_workspace_bytes(weights(BIN, 390, 4096, 5120)[0]) == 0
+    assert sb.bonsai_gemv_workspace_bytes(weights(BIN, 395, 17408, 1280)[0]) == 0
+    assert sb.bonsai_gemv_workspace_bytes(weights(BIN, 396, 17408, 5120)[0]) == 0
+    assert sb.bonsai_gemv_workspace_bytes(weights(BIN, 397, 20000, 5120)[0]) > 0
     assert sb.bonsai_gemv_workspace_bytes(weights(TER, 391, 17408, 1280)[0]) == 0
     assert sb.bonsai_gemv_workspace_bytes(weights(TER, 392, 512, 5120)[0]) == 0
     assert sb.bonsai_gemv_workspace_bytes(weights(TER, 394, 4096, 5120)[0]) == 0
