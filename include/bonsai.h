@@ -54,9 +54,10 @@
  *     device, a file-scope __device__ variable, written by kernels that
  *     detect bad input codes or a bounded wait that ran out, plus the fixed
  *     scratch array of bonsai_gemv_splitk_static (declared below).
- *   - Calls enqueue work on `stream` and return without synchronising (they
- *     can be captured in a CUDA graph). A non-OK return means nothing was
- *     launched. Kernel-side problems are reported by bonsai_check_async.
+ *   - Calls enqueue work on `stream` and return without synchronising (the
+ *     compute calls other than bonsai_gemv_splitk_static can be captured in
+ *     a CUDA graph). A non-OK return means nothing was launched. Kernel-side
+ *     problems are reported by bonsai_check_async.
  *   - Compute calls use programmatic dependent launch: a kernel may be
  *     scheduled while the previous kernel on the stream is still running,
  *     but it reads x (and writes y) only after that kernel has finished.
@@ -214,9 +215,8 @@ bonsai_status bonsai_gemv_host_ws(const bonsai_weights* w, const uint16_t* x_hos
  *   rows), with nothing launched; BONSAI_ERR_CUDA if the scratch address
  *   cannot be obtained.
  * The first call on a device looks up the scratch address
- * (cudaGetSymbolAddress) and enqueues a clear of the counters on `stream`;
- * make that first call before starting any stream capture that is to contain
- * later calls. Calls share the scratch: two calls that overlap in time
+ * (cudaGetSymbolAddress) and enqueues a clear of the counters on `stream`.
+ * Calls share the scratch: two calls that overlap in time
  * (different streams, or different host threads on one device) corrupt each
  * other's sums, so order them on one stream or synchronise between them.
  * Results of two ordered calls with the same inputs are bit-identical.
